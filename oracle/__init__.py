@@ -1,0 +1,10 @@
+"""fp64 CPU oracle for tree verification — test infrastructure only.
+
+Imported by the tests, the smoke check and the benchmark's CPU-baseline leg;
+never by the product path.
+"""
+from .treeverify_oracle import *  # noqa: F401,F403
+from .treeverify_oracle import (tree_build_mask, tree_verify_attn, tree_accept_greedy,  # noqa: F401
+                                tree_accept_sampling, kv_commit_path, node_plan, softmax_t,
+                                inverse_cdf, accept_test, ancestors_or_self, bf16_to_f64,
+                                tree_is_valid)

@@ -1,0 +1,421 @@
+"""fp64 CPU oracle for EAGLE-style tree verification.
+
+TEST INFRASTRUCTURE ONLY.  Only the test-suite, the package's smoke check and
+the benchmark's CPU-baseline / reference arm may import this module.  The
+product path (the CUDA library and its binding) never calls it, and this
+module imports nothing from the product package.
+
+Each function is the plain definition of one step of the verification step,
+written for readability rather than speed: explicit loops over requests,
+nodes and heads, numpy fp64 arithmetic, no blocking, fusion or reordering.
+
+Sources (the three pages on EAGLE speculative decoding):
+  * "SGLang EAGLE-2 Speculative Decoding" (Tech Radar), section 2,
+    "Dynamic Tree-Attention Masking": a candidate tree of at most 64 nodes is
+    encoded as a mask M in {0,1}^{KxK} with M[i][j] = 1 iff j is an ancestor
+    of i or i itself; one forward pass scores every branch; the target then
+    keeps the KV of the accepted branch and drops the wrong ones (sequence
+    diagram of the same section).
+  * "EAGLE - Draft head ..." (troisinh.com), section "Why it works",
+    paragraph on verification probability: verification is rejection
+    sampling; a wrong draft is resampled from the correct distribution, so the
+    output distribution equals plain autoregressive decoding.
+  * "EAGLE" study note (estelledc.github.io), case 3: accept a candidate the
+    target finds likely, otherwise reject with the difference probability and
+    resample; case 1: k drafted hits advance k+1 tokens.
+
+Readings where the pages are silent (each one is listed in the design notes):
+  * multi-child rule: children are tried in ascending node index with the
+    draft distribution q fixed; after a rejected child the target
+    distribution is replaced by the normalised residual max(0, p - q);
+  * ties: argmax -> lowest vocab index; deepest accepted node -> lowest node
+    index; inverse CDF -> first index j with u*S < C_j (strict);
+  * temperature: softmax(z / T); T = 0 means greedy;
+  * GQA: query head h reads KV head h // (Hq / Hkv);
+  * scale is given by the caller (1/sqrt(D) in every workload); the
+    log-sum-exp is in natural log.
+
+Every function here is pinned by tests in ``tests/test_oracle_*.py`` against
+facts that do not come from this file (library routines, closed forms,
+brute force, enumeration and hand-derived fixtures).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# Device status bits, restated from the library's interface definition.
+STATUS_OK = 0
+STATUS_BAD_TREE = 1
+STATUS_PAGE_OOB = 2
+STATUS_CAPACITY = 4
+STATUS_TIMEOUT = 8
+STATUS_BAD_TOKEN = 16
+
+MAX_NODES = 64
+NEAR_BOUNDARY = 1e-6
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Decode raw bf16 bit patterns (uint16) to float64 exactly."""
+    return (np.asarray(bits).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def tree_is_valid(parents_row: np.ndarray, n: int) -> bool:
+    """A tree is 1..64 nodes, node 0 is the root (parent -1) and every other
+    node's parent precedes it."""
+    if n < 1 or n > MAX_NODES:
+        return False
+    if int(parents_row[0]) != -1:
+        return False
+    for i in range(1, n):
+        p = int(parents_row[i])
+        if p < 0 or p >= i:
+            return False
+    return True
+
+
+def ancestors_or_self(parents_row: np.ndarray, i: int) -> list:
+    """Walk parent links from node i up to the root; returns root-first list
+    [0, ..., parent(i), i]."""
+    path = [i]
+    while path[-1] != 0:
+        path.append(int(parents_row[path[-1]]))
+    return path[::-1]
+
+
+# --------------------------------------------------------------------------
+# step 1: tree mask
+# --------------------------------------------------------------------------
+def tree_build_mask(parents: np.ndarray, n_nodes: np.ndarray):
+    """Ancestor mask of each node as a 64-bit word: bit j set iff node j is an
+    ancestor of i or i itself (Tech Radar section 2, the mask M), plus the
+    node's depth (root = 0).
+
+    Returns (anc_mask uint64 [B, n_max], depth int32 [B, n_max], status int32 [B]).
+    Entries past n_nodes[b] are 0 (mask) and -1 (depth); an invalid tree gets
+    STATUS_BAD_TREE and all-zero / -1 outputs.
+    """
+    parents = np.asarray(parents)
+    B, n_max = parents.shape
+    anc = np.zeros((B, n_max), dtype=np.uint64)
+    depth = np.full((B, n_max), -1, dtype=np.int32)
+    status = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        n = int(n_nodes[b])
+        if n > n_max or not tree_is_valid(parents[b], n):
+            status[b] = STATUS_BAD_TREE
+            continue
+        for i in range(n):
+            path = ancestors_or_self(parents[b], i)
+            word = 0
+            for j in path:
+                word |= 1 << j
+            anc[b, i] = np.uint64(word)
+            depth[b, i] = len(path) - 1
+    return anc, depth, status
+
+
+# --------------------------------------------------------------------------
+# step 2: tree-verify attention
+# --------------------------------------------------------------------------
+def _request_pages_ok(page_table_row, L, N, num_pages, page_size):
+    need = (L + N + page_size - 1) // page_size
+    if need > len(page_table_row):
+        return STATUS_CAPACITY
+    for k in range(need):
+        if not (0 <= int(page_table_row[k]) < num_pages):
+            return STATUS_PAGE_OOB
+    return STATUS_OK
+
+
+def tree_verify_attn(q_bits, k_bits, v_bits, page_table, prefix_len, n_nodes, parents,
+                     scale, page_size=16, rows=None):
+    """Tree-masked attention of every tree node over its request's paged cache.
+
+    For request b, query head h and node i, the visible keys are the prefix
+    positions 0..L-1 and the tree positions L+j for every j that is an
+    ancestor of i or i itself (the mask M of Tech Radar section 2).  The tree's
+    own K/V already sit at positions L..L+N-1 of the request's pages.  Query
+    head h reads KV head h // G with G = Hq / Hkv.
+
+        s_t = scale * <q, k_t>,   o = sum_t softmax(s)_t v_t,
+        lse = log sum_t exp(s_t)  (natural log).
+
+    Inputs are raw bf16 bits (uint16): q [B, n_max, Hq, D],
+    caches [num_pages, Hkv, page_size, D]; page_table int32 [B, max_pages].
+    ``rows`` optionally restricts the work to a list of (b, i, h) triples.
+
+    Returns (out float64 [B, n_max, Hq, D], lse float64 [B, n_max, Hq],
+    status int32 [B]); entries not computed are NaN.
+    """
+    B, n_max, Hq, D = q_bits.shape
+    num_pages, Hkv = k_bits.shape[0], k_bits.shape[1]
+    G = Hq // Hkv
+    out = np.full((B, n_max, Hq, D), np.nan)
+    lse = np.full((B, n_max, Hq), np.nan)
+    status = np.zeros(B, dtype=np.int32)
+
+    if rows is None:
+        wanted = {b: None for b in range(B)}
+    else:
+        wanted = {}
+        for (b, i, h) in rows:
+            wanted.setdefault(int(b), []).append((int(i), int(h)))
+
+    for b, sel in wanted.items():
+        L, N = int(prefix_len[b]), int(n_nodes[b])
+        st = _request_pages_ok(page_table[b], L, N, num_pages, page_size)
+        if not tree_is_valid(parents[b], N):
+            st |= STATUS_BAD_TREE
+        status[b] = st
+        if st != STATUS_OK:
+            continue
+        pairs = sel if sel is not None else [(i, h) for i in range(N) for h in range(Hq)]
+        by_node = {}
+        for (i, h) in pairs:
+            by_node.setdefault(i, []).append(h)
+        for i, heads in by_node.items():
+            # the explicit key sequence of node i: prefix, then its root-to-node path
+            positions = list(range(L)) + [L + j for j in ancestors_or_self(parents[b], i)]
+            pos = np.asarray(positions, dtype=np.int64)
+            page = np.asarray(page_table[b])[pos // page_size]
+            slot = pos % page_size
+            K = bf16_to_f64(k_bits[page, :, slot, :])   # [T, Hkv, D]
+            Vv = bf16_to_f64(v_bits[page, :, slot, :])  # [T, Hkv, D]
+            for h in heads:
+                g = h // G
+                qv = bf16_to_f64(q_bits[b, i, h])       # [D]
+                s = scale * (K[:, g, :] @ qv)           # [T]
+                m = np.max(s)
+                w = np.exp(s - m)
+                out[b, i, h] = (w @ Vv[:, g, :]) / np.sum(w)
+                lse[b, i, h] = m + np.log(np.sum(w))
+    return out, lse, status
+
+
+# --------------------------------------------------------------------------
+# step 3a: greedy acceptance
+# --------------------------------------------------------------------------
+def _first_argmax(row) -> int:
+    """Largest entry, lowest index on ties (numpy.argmax semantics)."""
+    return int(np.argmax(np.asarray(row)))
+
+
+def tree_accept_greedy(target_logits, tokens, parents, n_nodes, V=None):
+    """Greedy (T = 0) acceptance of the longest matching root-to-node path.
+
+    A non-root node j "hits" when its token equals the target's argmax at its
+    parent (the drafter's argmax rule of Tech Radar section 2 applied to the
+    target).  A node c is accepted when every non-root node on its
+    root-to-node path hits.  The result is the accepted node of largest depth
+    (lowest index on ties); the emitted tokens are the path's drafted tokens
+    followed by the target's argmax at the result node (k hits emit k+1
+    tokens: study note, case 1).
+
+    Returns dict with accept_len int32 [B], path_nodes int32 [B, n_max]
+    (root first, -1 padded), out_tokens int32 [B, n_max+1] (-1 padded),
+    status int32 [B].
+    """
+    B, n_max, Vdim = target_logits.shape
+    V = Vdim if V is None else V
+    accept_len = np.zeros(B, dtype=np.int32)
+    path_nodes = np.full((B, n_max), -1, dtype=np.int32)
+    out_tokens = np.full((B, n_max + 1), -1, dtype=np.int32)
+    status = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        n = int(n_nodes[b])
+        if not tree_is_valid(parents[b], n):
+            status[b] = STATUS_BAD_TREE
+            continue
+        if any(not (0 <= int(tokens[b, c]) < V) for c in range(1, n)):
+            status[b] = STATUS_BAD_TOKEN
+            continue
+        best, best_depth = 0, 0
+        for c in range(n):
+            path = ancestors_or_self(parents[b], c)
+            ok = all(int(tokens[b, j]) == _first_argmax(target_logits[b, int(parents[b, j])])
+                     for j in path[1:])
+            if ok and len(path) - 1 > best_depth:
+                best, best_depth = c, len(path) - 1
+        path = ancestors_or_self(parents[b], best)
+        accept_len[b] = best_depth
+        path_nodes[b, : len(path)] = path
+        emitted = [int(tokens[b, j]) for j in path[1:]] + [_first_argmax(target_logits[b, best])]
+        out_tokens[b, : len(emitted)] = emitted
+    return dict(accept_len=accept_len, path_nodes=path_nodes, out_tokens=out_tokens,
+                status=status)
+
+
+# --------------------------------------------------------------------------
+# step 3b: rejection-sampling acceptance
+# --------------------------------------------------------------------------
+def softmax_t(z, T):
+    """softmax(z / T) in fp64."""
+    x = np.asarray(z, dtype=np.float64) / T
+    e = np.exp(x - np.max(x))
+    return e / np.sum(e)
+
+
+def node_plan(p, q, child_tokens):
+    """The acceptance plan at one tree node (multi-child reading of the
+    rejection rule): children are tried in the given (ascending node) order;
+    child k with token x is accepted with probability min(1, cur_k(x)/q(x))
+    where cur_0 = p and, after a rejection, cur_{k+1} = max(0, cur_k - q)
+    normalised (left unchanged if that residual sums to zero).
+
+    Returns (cur_list, final) where cur_list[k] is the distribution the k-th
+    child is tested against and ``final`` the one the bonus token is drawn
+    from when every child is rejected.
+    """
+    cur = np.asarray(p, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    cur_list = []
+    for _x in child_tokens:
+        cur_list.append(cur)
+        r = np.maximum(0.0, cur - q)
+        s = np.sum(r)
+        cur = r / s if s > 0 else cur
+    return cur_list, cur
+
+
+def accept_test(u, cur_x, q_x):
+    """Accept iff u * q(x) < cur(x), i.e. u < min(1, cur(x)/q(x)) without a
+    division; with q(x) = 0 this accepts iff cur(x) > 0."""
+    return u * q_x < cur_x
+
+
+def inverse_cdf(w, u):
+    """First index j with u * S < C_j, C_j = sum_{v<=j} w_v, S = C_{V-1}
+    (zero-weight entries are never chosen).  Returns (j, margin) where margin
+    is min |u*S - C| over C_{j-1}, C_j relative to S."""
+    C = np.cumsum(np.asarray(w, dtype=np.float64))
+    S = C[-1]
+    t = u * S
+    j = int(np.searchsorted(C, t, side="right"))
+    if j >= len(C):                       # u*S >= S only through rounding
+        j = int(np.nonzero(np.asarray(w) > 0)[0][-1])
+    lo = C[j - 1] if j > 0 else 0.0
+    margin = min(abs(t - C[j]), abs(t - lo)) / S
+    return j, margin
+
+
+def tree_accept_sampling(target_logits, draft_logits, tokens, parents, n_nodes, temperature,
+                         u_accept, u_sample, V=None):
+    """Rejection-sampling acceptance at temperature T > 0 (lossless
+    verification: troisinh.com "Why it works"; study note case 3).
+
+    Walk from the root.  At node n set p = softmax(target[n]/T),
+    q = softmax(draft[n]/T) (draft row n is the distribution n's children were
+    drawn from).  Children c of n are tried in ascending index with
+    u = u_accept[c]; the first accepted child becomes the next node.  If no
+    child is accepted (or n is a leaf) the bonus token is drawn from the
+    current distribution (the residual after the rejections, or p at a leaf)
+    by inverse CDF with u = u_sample[n], and the walk ends.
+
+    Returns dict like ``tree_accept_greedy`` plus ``near_boundary`` bool [B]:
+    some decision of the walk had |u - cur(x)/q(x)| < 1e-6 or an inverse-CDF
+    margin below 1e-6, where a rounding difference may legitimately change the
+    outcome.
+    """
+    B, n_max, Vdim = target_logits.shape
+    V = Vdim if V is None else V
+    T = float(temperature)
+    accept_len = np.zeros(B, dtype=np.int32)
+    path_nodes = np.full((B, n_max), -1, dtype=np.int32)
+    out_tokens = np.full((B, n_max + 1), -1, dtype=np.int32)
+    status = np.zeros(B, dtype=np.int32)
+    near = np.zeros(B, dtype=bool)
+    for b in range(B):
+        n_b = int(n_nodes[b])
+        if not tree_is_valid(parents[b], n_b):
+            status[b] = STATUS_BAD_TREE
+            continue
+        if any(not (0 <= int(tokens[b, c]) < V) for c in range(1, n_b)):
+            status[b] = STATUS_BAD_TOKEN
+            continue
+        kids = [[] for _ in range(n_b)]
+        for c in range(1, n_b):
+            kids[int(parents[b, c])].append(c)
+        node, path, emitted = 0, [0], []
+        while True:
+            p = softmax_t(target_logits[b, node], T)
+            q = softmax_t(draft_logits[b, node], T)
+            child_tokens = [int(tokens[b, c]) for c in kids[node]]
+            cur_list, final = node_plan(p, q, child_tokens)
+            nxt = None
+            for c, x, cur in zip(kids[node], child_tokens, cur_list):
+                u = float(u_accept[b, c])
+                if q[x] > 0 and abs(u - cur[x] / q[x]) < NEAR_BOUNDARY:
+                    near[b] = True
+                if accept_test(u, cur[x], q[x]):
+                    nxt = c
+                    break
+            if nxt is not None:
+                node = nxt
+                path.append(node)
+                emitted.append(int(tokens[b, node]))
+                continue
+            j, margin = inverse_cdf(final, float(u_sample[b, node]))
+            if margin < NEAR_BOUNDARY:
+                near[b] = True
+            emitted.append(j)
+            break
+        accept_len[b] = len(path) - 1
+        path_nodes[b, : len(path)] = path
+        out_tokens[b, : len(emitted)] = emitted
+    return dict(accept_len=accept_len, path_nodes=path_nodes, out_tokens=out_tokens,
+                status=status, near_boundary=near)
+
+
+# --------------------------------------------------------------------------
+# step 4: KV commit of the accepted path
+# --------------------------------------------------------------------------
+def kv_commit_path(k_layers, v_layers, page_table, prefix_len, n_nodes, accept_len, path_nodes,
+                   page_size=16):
+    """Keep the accepted branch's K/V and drop the rest (Tech Radar section 2,
+    sequence diagram): for k = 1..a, the K and V rows of logical position
+    L + path[k] move to position L + k in every layer and KV head; the root
+    stays at L.  The new length is L + a + 1 and the committed physical slots
+    are page_table[(L+k)//P]*P + (L+k)%P for k = 0..a.
+
+    Caches are given per layer as [n_layers, num_pages, Hkv, P, D] arrays of
+    any dtype; copies are returned.  Moves are applied in increasing k, which
+    reads every source before it can be overwritten (path[k] >= k).
+
+    Returns (k_new, v_new, committed_slots int64 [B, n_max] (-1 padded),
+    new_len int32 [B], status int32 [B]).
+    """
+    k_new = np.array(k_layers, copy=True)
+    v_new = np.array(v_layers, copy=True)
+    B, n_max = path_nodes.shape
+    num_pages = k_new.shape[1]
+    slots = np.full((B, n_max), -1, dtype=np.int64)
+    new_len = np.zeros(B, dtype=np.int32)
+    status = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        L, N, a = int(prefix_len[b]), int(n_nodes[b]), int(accept_len[b])
+        st = _request_pages_ok(page_table[b], L, N, num_pages, page_size)
+        path = [int(x) for x in path_nodes[b, : a + 1]]
+        if a < 0 or a >= N or path[0] != 0 or any(path[k] >= N for k in range(a + 1)) or \
+                any(path[k] <= path[k - 1] for k in range(1, a + 1)):
+            st |= STATUS_BAD_TREE
+        status[b] = st
+        if st != STATUS_OK:
+            new_len[b] = L
+            continue
+        for k in range(1, a + 1):
+            src, dst = L + path[k], L + k
+            if src == dst:
+                continue
+            sp, so = int(page_table[b, src // page_size]), src % page_size
+            dp, do = int(page_table[b, dst // page_size]), dst % page_size
+            k_new[:, dp, :, do, :] = k_new[:, sp, :, so, :]
+            v_new[:, dp, :, do, :] = v_new[:, sp, :, so, :]
+        for k in range(a + 1):
+            pos = L + k
+            slots[b, k] = int(page_table[b, pos // page_size]) * page_size + pos % page_size
+        new_len[b] = L + a + 1
+    return k_new, v_new, slots, new_len, status
