@@ -1,0 +1,573 @@
+// tv_tree_accept: longest accepted root-to-node path of the draft tree.
+//
+// Greedy (T = 0): a non-root node hits when its drafted token equals the
+// target's argmax at its parent (the argmax rule of "SGLang EAGLE-2
+// Speculative Decoding", section 2, applied to the target); the deepest node
+// whose whole root path hits is accepted, and the target's argmax there is
+// the bonus token (study note "EAGLE", case 1: k hits emit k+1 tokens).
+//
+// Sampling (T > 0): rejection sampling with residual resampling
+// (troisinh.com "Why it works"; study note case 3).  At node n with
+// p = softmax(target[n]/T) and q = softmax(draft[n]/T) the children are tried
+// in ascending index: accept iff u*q(x) < p(x); after a rejection p becomes
+// max(0, p - q) normalised.  When every child is rejected (or n is a leaf)
+// the bonus is drawn from the current p by inverse CDF.
+//
+// Design: one thread-block cluster of kCL CTAs per request.  CTA r owns the
+// vocabulary slice [r*chunk, (r+1)*chunk).  Rows are read from HBM only for
+// the nodes the walk visits; in sampling mode the visited node's p and q
+// slices stay in shared memory for the residual passes and the inverse CDF.
+// Cluster-wide reductions go through distributed shared memory and are
+// combined in rank order, so every CTA takes identical decisions (uniform
+// control flow across the cluster).
+#include <cooperative_groups.h>
+#include <cfloat>
+#include <climits>
+#include "tv_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace tv {
+
+constexpr int kCL = 8;
+constexpr int kAccThreads = 512;
+constexpr int kAccWarps = kAccThreads / 32;
+constexpr int kMaxChunk = 26624;  // floats per CTA and array (sampling keeps two arrays)
+
+struct AcceptParams {
+  const float* target;
+  const float* draft;
+  const int32_t* tokens;
+  const int32_t* parents;
+  const int32_t* n_nodes;
+  const float* u_accept;
+  const float* u_sample;
+  int n_max, V, chunk;
+  float k2;          // log2(e) / T   (sampling)
+  int sampling;
+  int32_t* accept_len;
+  int32_t* path_nodes;
+  int32_t* out_tokens;
+  int32_t* status;
+};
+
+struct __align__(16) ClSlot {
+  double d[2];
+  float f[2];
+  int i[2];
+};
+
+struct AccShared {
+  int par[kMaxNodes];
+  int tok[kMaxNodes];
+  int kid_off[kMaxNodes + 1];
+  int kids[kMaxNodes];
+  int am[kMaxNodes];
+  int front[kMaxNodes];
+  int nxt[kMaxNodes];
+  int path[kMaxNodes];
+  float wf[kAccWarps];
+  int wi[kAccWarps];
+  double wd[kAccWarps][2];
+  double thr_excl[kAccThreads];  // exclusive scan of per-thread sums (inverse CDF)
+  ClSlot slot[2];
+  float bf;
+  int bi;
+  double bd[2];
+  int bad;
+  int cnt;
+  int lowest;
+};
+
+// ---------------------------------------------------------------- reductions
+__device__ __forceinline__ void argmax_take(float& v, int& i, float v2, int i2) {
+  if (v2 > v || (v2 == v && i2 < i)) {
+    v = v2;
+    i = i2;
+  }
+}
+
+// Block argmax (ties -> lowest index); result in sh.bf / sh.bi.
+__device__ void block_argmax(float v, int i, AccShared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+    argmax_take(v, i, v2, i2);
+  }
+  if (lane == 0) {
+    sh.wf[warp] = v;
+    sh.wi[warp] = i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float bv = sh.wf[0];
+    int bi = sh.wi[0];
+    for (int w = 1; w < kAccWarps; ++w) argmax_take(bv, bi, sh.wf[w], sh.wi[w]);
+    sh.bf = bv;
+    sh.bi = bi;
+  }
+  __syncthreads();
+}
+
+__device__ void block_max(float v, AccShared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (lane == 0) sh.wf[warp] = v;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = sh.wf[0];
+    for (int w = 1; w < kAccWarps; ++w) m = fmaxf(m, sh.wf[w]);
+    sh.bf = m;
+  }
+  __syncthreads();
+}
+
+// Two sums at once (fp32 inside a warp, fp64 across warps); result in sh.bd.
+__device__ void block_sum2(float a, float b, AccShared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+  }
+  if (lane == 0) {
+    sh.wd[warp][0] = a;
+    sh.wd[warp][1] = b;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double x = 0.0, y = 0.0;
+    for (int w = 0; w < kAccWarps; ++w) {
+      x += sh.wd[w][0];
+      y += sh.wd[w][1];
+    }
+    sh.bd[0] = x;
+    sh.bd[1] = y;
+  }
+  __syncthreads();
+}
+
+// Cluster exchange: thread 0 of every CTA publishes its slot, then every
+// thread reads all kCL slots in rank order.  Slots are double buffered so a
+// slot is never rewritten before every CTA has passed the next cluster barrier.
+struct ClusterEx {
+  cg::cluster_group cl;
+  int buf;
+  __device__ ClusterEx() : cl(cg::this_cluster()), buf(0) {}
+  __device__ ClSlot* publish(AccShared& sh) { return &sh.slot[buf]; }
+  __device__ const ClSlot* remote(AccShared& sh, int r) { return cl.map_shared_rank(&sh.slot[buf], r); }
+  __device__ void sync() { cl.sync(); }
+  __device__ void flip() { buf ^= 1; }
+};
+
+// ---------------------------------------------------------------- the kernel
+__global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
+    tree_accept_kernel(const AcceptParams p) {
+  extern __shared__ __align__(16) float dyn[];
+  __shared__ AccShared sh;
+  ClusterEx ex;
+  const int rank = (int)ex.cl.block_rank();
+  const int b = blockIdx.x / kCL;
+  const int tid = threadIdx.x;
+  const int n_max = p.n_max, V = p.V;
+  const int lo = min(V, rank * p.chunk);
+  const int hi = min(V, lo + p.chunk);
+  const int len = hi - lo;
+  float* wt = dyn;             // sampling: current target weights of this slice
+  float* wq = dyn + p.chunk;   // sampling: draft weights of this slice
+
+  // ---- tree setup and validation (every CTA redundantly, identical results)
+  const int N = p.n_nodes[b];
+  if (tid == 0) {
+    int bad = p.status[b] != 0 ? -1 : 0;
+    if (!bad && (N < 1 || N > n_max)) bad = TV_DEV_BAD_TREE;
+    if (!bad) {
+      int cnt[kMaxNodes];
+      for (int i = 0; i < N; ++i) {
+        const int pi = p.parents[(int64_t)b * n_max + i];
+        const int ti = p.tokens[(int64_t)b * n_max + i];
+        sh.par[i] = pi;
+        sh.tok[i] = ti;
+        cnt[i] = 0;
+        if (i == 0 ? pi != -1 : (pi < 0 || pi >= i)) bad = TV_DEV_BAD_TREE;
+      }
+      if (!bad)
+        for (int i = 1; i < N; ++i)
+          if (sh.tok[i] < 0 || sh.tok[i] >= V) bad = TV_DEV_BAD_TOKEN;
+      if (!bad) {
+        for (int i = 1; i < N; ++i) cnt[sh.par[i]]++;
+        sh.kid_off[0] = 0;
+        for (int i = 0; i < N; ++i) sh.kid_off[i + 1] = sh.kid_off[i] + cnt[i];
+        for (int i = 0; i < N; ++i) cnt[i] = sh.kid_off[i];
+        for (int i = 1; i < N; ++i) sh.kids[cnt[sh.par[i]]++] = i;  // ascending per parent
+      }
+    }
+    sh.bad = bad;
+  }
+  __syncthreads();
+  if (sh.bad != 0) {
+    if (rank == 0) {
+      if (tid == 0) {
+        p.accept_len[b] = 0;
+        if (sh.bad > 0) atomicOr(p.status + b, sh.bad);
+      }
+      for (int k = tid; k < n_max; k += kAccThreads) p.path_nodes[(int64_t)b * n_max + k] = -1;
+      for (int k = tid; k <= n_max; k += kAccThreads) p.out_tokens[(int64_t)b * (n_max + 1) + k] = -1;
+    }
+    return;  // uniform across the cluster: every CTA computed the same flag
+  }
+
+  const bool vec4 = (V & 3) == 0;
+  int best = 0;
+  int bonus = -1;
+
+  if (!p.sampling) {
+    // ================================================ greedy: level-synchronous walk
+    int nf = 1;
+    if (tid == 0) sh.front[0] = 0;
+    __syncthreads();
+    while (nf > 0) {
+      for (int f = 0; f < nf; ++f) {
+        const int node = sh.front[f];
+        const float* row = p.target + ((int64_t)b * n_max + node) * V;
+        float bv = -FLT_MAX;
+        int bi = INT_MAX;
+        if (vec4) {
+          const float4* r4 = reinterpret_cast<const float4*>(row + lo);
+          for (int j = tid; j < (len >> 2); j += kAccThreads) {
+            const float4 x = __ldg(r4 + j);
+            const int base = lo + 4 * j;
+            argmax_take(bv, bi, x.x, base);
+            argmax_take(bv, bi, x.y, base + 1);
+            argmax_take(bv, bi, x.z, base + 2);
+            argmax_take(bv, bi, x.w, base + 3);
+          }
+        } else {
+          for (int j = tid; j < len; j += kAccThreads) argmax_take(bv, bi, __ldg(row + lo + j), lo + j);
+        }
+        block_argmax(bv, bi, sh);
+        if (tid == 0) {
+          ClSlot* s = ex.publish(sh);
+          s->f[0] = sh.bf;
+          s->i[0] = sh.bi;
+        }
+        ex.sync();
+        float gv = -FLT_MAX;
+        int gi = INT_MAX;
+        for (int r = 0; r < kCL; ++r) {
+          const ClSlot* s = ex.remote(sh, r);
+          argmax_take(gv, gi, s->f[0], s->i[0]);
+        }
+        ex.flip();
+        if (tid == 0) sh.am[node] = gi;  // identical in every CTA
+      }
+      __syncthreads();
+      if (tid == 0) {
+        // next frontier: children of frontier nodes whose token is the parent's argmax
+        int cnt = 0, lowest = INT_MAX;
+        for (int f = 0; f < nf; ++f) {
+          const int node = sh.front[f];
+          for (int k = sh.kid_off[node]; k < sh.kid_off[node + 1]; ++k) {
+            const int c = sh.kids[k];
+            if (sh.tok[c] == sh.am[node]) {
+              sh.nxt[cnt++] = c;
+              lowest = min(lowest, c);
+            }
+          }
+        }
+        for (int k = 0; k < cnt; ++k) sh.front[k] = sh.nxt[k];
+        sh.cnt = cnt;
+        sh.lowest = lowest;
+      }
+      __syncthreads();
+      nf = sh.cnt;
+      if (nf > 0) best = sh.lowest;  // all next-frontier nodes share one depth
+      __syncthreads();
+    }
+    bonus = sh.am[best];
+  } else {
+    // ================================================ sampling: walk from the root
+    int node = 0;
+    bool first = true;
+    for (;;) {
+      if (!first) ex.sync();  // every CTA finished reading this CTA's slices
+      first = false;
+      const float* trow = p.target + ((int64_t)b * n_max + node) * V + lo;
+      const float* drow = p.draft + ((int64_t)b * n_max + node) * V + lo;
+      float mt = -FLT_MAX, mq = -FLT_MAX;
+      if (vec4) {
+        const float4* t4 = reinterpret_cast<const float4*>(trow);
+        const float4* d4 = reinterpret_cast<const float4*>(drow);
+        for (int j = tid; j < (len >> 2); j += kAccThreads) {
+          const float4 x = __ldg(t4 + j);
+          const float4 y = __ldg(d4 + j);
+          reinterpret_cast<float4*>(wt)[j] = x;
+          reinterpret_cast<float4*>(wq)[j] = y;
+          mt = fmaxf(mt, fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
+          mq = fmaxf(mq, fmaxf(fmaxf(y.x, y.y), fmaxf(y.z, y.w)));
+        }
+      } else {
+        for (int j = tid; j < len; j += kAccThreads) {
+          const float x = __ldg(trow + j), y = __ldg(drow + j);
+          wt[j] = x;
+          wq[j] = y;
+          mt = fmaxf(mt, x);
+          mq = fmaxf(mq, y);
+        }
+      }
+      block_max(mt, sh);
+      const float bmt = sh.bf;
+      block_max(mq, sh);
+      const float bmq = sh.bf;
+      if (tid == 0) {
+        ClSlot* s = ex.publish(sh);
+        s->f[0] = bmt;
+        s->f[1] = bmq;
+      }
+      ex.sync();
+      float Mt = -FLT_MAX, Mq = -FLT_MAX;
+      for (int r = 0; r < kCL; ++r) {
+        const ClSlot* s = ex.remote(sh, r);
+        Mt = fmaxf(Mt, s->f[0]);
+        Mq = fmaxf(Mq, s->f[1]);
+      }
+      ex.flip();
+      // exponentiate in place: w = 2^((z - max) * log2(e)/T)
+      float st = 0.f, sq = 0.f;
+      for (int j = tid; j < len; j += kAccThreads) {
+        const float et = exp2f((wt[j] - Mt) * p.k2);
+        const float eq = exp2f((wq[j] - Mq) * p.k2);
+        wt[j] = et;
+        wq[j] = eq;
+        st += et;
+        sq += eq;
+      }
+      block_sum2(st, sq, sh);
+      if (tid == 0) {
+        ClSlot* s = ex.publish(sh);
+        s->d[0] = sh.bd[0];
+        s->d[1] = sh.bd[1];
+      }
+      ex.sync();
+      double St = 0.0, Sq = 0.0;
+      for (int r = 0; r < kCL; ++r) {
+        const ClSlot* s = ex.remote(sh, r);
+        St += s->d[0];
+        Sq += s->d[1];
+      }
+      ex.flip();
+      float Sw = (float)St;            // normaliser of the current target weights wt
+      const float SqF = (float)Sq;     // normaliser of wq
+
+      int accepted = -1;
+      for (int k = sh.kid_off[node]; k < sh.kid_off[node + 1]; ++k) {
+        const int c = sh.kids[k];
+        const int x = sh.tok[c];
+        const int owner = x / p.chunk;
+        const int off = x - owner * p.chunk;
+        const float* rwt = ex.cl.map_shared_rank(wt, owner);
+        const float* rwq = ex.cl.map_shared_rank(wq, owner);
+        const float cur_x = rwt[off] / Sw;
+        const float q_x = rwq[off] / SqF;
+        const float u = p.u_accept[(int64_t)b * n_max + c];
+        if (u * q_x < cur_x) {
+          accepted = c;
+          break;
+        }
+        // rejected: residual max(0, cur - q), normalised (kept if it sums to 0)
+        float z = 0.f;
+        for (int j = tid; j < len; j += kAccThreads) z += fmaxf(0.f, wt[j] / Sw - wq[j] / SqF);
+        block_sum2(z, 0.f, sh);
+        if (tid == 0) {
+          ClSlot* s = ex.publish(sh);
+          s->d[0] = sh.bd[0];
+        }
+        ex.sync();
+        double Z = 0.0;
+        for (int r = 0; r < kCL; ++r) Z += ex.remote(sh, r)->d[0];
+        ex.flip();
+        if (Z > 0.0) {
+          for (int j = tid; j < len; j += kAccThreads) wt[j] = fmaxf(0.f, wt[j] / Sw - wq[j] / SqF);
+          Sw = (float)Z;
+        }
+        ex.sync();  // residual slices complete before anyone reads them
+      }
+      if (accepted >= 0) {
+        node = accepted;
+        continue;
+      }
+      // ---- bonus token: inverse CDF of wt with u_sample[node]
+      {
+        const int per = (len + kAccThreads - 1) / kAccThreads;
+        const int a0 = min(len, tid * per), a1 = min(len, a0 + per);
+        float tsum = 0.f;
+        for (int j = a0; j < a1; ++j) tsum += wt[j];
+        // exclusive scan over threads (fp64), thread 0 sequentially over warps
+        double v = tsum;
+        const int lane = tid & 31, warp = tid >> 5;
+        double incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (lane == 31) sh.wd[warp][0] = incl;
+        __syncthreads();
+        if (tid == 0) {
+          double run = 0.0;
+          for (int w = 0; w < kAccWarps; ++w) {
+            const double t = sh.wd[w][0];
+            sh.wd[w][1] = run;
+            run += t;
+          }
+          sh.bd[0] = run;
+        }
+        __syncthreads();
+        sh.thr_excl[tid] = sh.wd[warp][1] + incl - v;
+        const double s_r = sh.bd[0];
+        if (tid == 0) {
+          ClSlot* s = ex.publish(sh);
+          s->d[0] = s_r;
+        }
+        ex.sync();
+        double pre[kCL];
+        double S = 0.0;
+        for (int r = 0; r < kCL; ++r) {
+          pre[r] = S;
+          S += ex.remote(sh, r)->d[0];
+        }
+        ex.flip();
+        const double t = (double)p.u_sample[(int64_t)b * n_max + node] * S;
+        int rstar = -1, rlast = -1;
+        for (int r = 0; r < kCL; ++r) {
+          const double sr = (r + 1 < kCL ? pre[r + 1] : S) - pre[r];
+          if (sr > 0.0) rlast = r;
+          if (rstar < 0 && pre[r] + sr > t) rstar = r;
+        }
+        const bool fallback_rank = rstar < 0;
+        if (fallback_rank) rstar = rlast;
+        int found = -1;
+        if (rank == rstar) {
+          // thread whose range crosses t (or the last non-empty one on fallback)
+          const double base = pre[rank] + sh.thr_excl[tid];
+          const bool crosses = !fallback_rank && tsum > 0.f && base + (double)tsum > t && base <= t;
+          const bool nonempty = tsum > 0.f;
+          if (tid == 0) {
+            sh.bi = INT_MAX;
+            sh.wi[0] = -1;
+          }
+          __syncthreads();
+          if (crosses) atomicMin(&sh.bi, tid);
+          if (nonempty) atomicMax(&sh.wi[0], tid);
+          __syncthreads();
+          int kstar = sh.bi;
+          const bool fb = (kstar == INT_MAX);
+          if (fb) kstar = sh.wi[0];
+          if (tid == kstar) {
+            double acc = pre[rank] + sh.thr_excl[tid];
+            int j_found = -1, j_last = -1;
+            for (int j = a0; j < a1; ++j) {
+              if (wt[j] > 0.f) j_last = j;
+              acc += (double)wt[j];
+              if (!fb && j_found < 0 && acc > t && wt[j] > 0.f) j_found = j;
+            }
+            sh.bd[1] = (double)(lo + (j_found >= 0 ? j_found : j_last));
+          }
+          __syncthreads();
+          found = (int)sh.bd[1];
+        }
+        if (tid == 0) {
+          ClSlot* s = ex.publish(sh);
+          s->i[0] = found;
+        }
+        ex.sync();
+        int tokv = -1;
+        for (int r = 0; r < kCL; ++r) tokv = max(tokv, ex.remote(sh, r)->i[0]);
+        ex.flip();
+        bonus = tokv;
+      }
+      best = node;
+      break;
+    }
+  }
+
+  // ---- outputs (rank 0)
+  if (rank == 0 && tid == 0) {
+    int len_path = 0;
+    for (int j = best; j != 0; j = sh.par[j]) sh.path[len_path++] = j;
+    // sh.path holds best .. first child; emit root-first
+    int32_t* pn = p.path_nodes + (int64_t)b * n_max;
+    int32_t* ot = p.out_tokens + (int64_t)b * (n_max + 1);
+    pn[0] = 0;
+    for (int k = 1; k <= len_path; ++k) {
+      const int nd = sh.path[len_path - k];
+      pn[k] = nd;
+      ot[k - 1] = sh.tok[nd];
+    }
+    ot[len_path] = bonus;
+    for (int k = len_path + 1; k < n_max; ++k) pn[k] = -1;
+    for (int k = len_path + 1; k <= n_max; ++k) ot[k] = -1;
+    p.accept_len[b] = len_path;
+  }
+  ex.sync();  // no CTA exits while others may still read its shared memory
+}
+
+}  // namespace tv
+
+extern "C" size_t tv_tree_accept_workspace(int, int, int) { return 0; }
+
+extern "C" int tv_tree_accept(const float* target_logits, const float* draft_logits, const int32_t* tokens,
+                              const int32_t* parents, const int32_t* n_nodes, const uint64_t* anc_mask,
+                              const int32_t* depth, int B, int n_max, int V, float temperature,
+                              const float* u_accept, const float* u_sample, int32_t* accept_len,
+                              int32_t* path_nodes, int32_t* out_tokens, void* ws, size_t ws_bytes,
+                              int32_t* status, void* stream) {
+  (void)anc_mask;
+  (void)depth;
+  (void)ws;
+  (void)ws_bytes;
+  tv::clear_error();
+  const bool sampling = temperature > 0.f;
+  TV_REQUIRE(target_logits && tokens && parents && n_nodes && accept_len && path_nodes && out_tokens && status,
+             TV_ERR_INVALID_ARG, "tv_tree_accept: NULL pointer");
+  TV_REQUIRE(!sampling || (draft_logits && u_accept && u_sample), TV_ERR_INVALID_ARG,
+             "tv_tree_accept: sampling needs draft_logits, u_accept and u_sample");
+  TV_REQUIRE(temperature >= 0.f && temperature == temperature, TV_ERR_INVALID_ARG,
+             "tv_tree_accept: temperature must be >= 0");
+  TV_REQUIRE(B >= 0 && V >= 1, TV_ERR_INVALID_ARG, "tv_tree_accept: bad sizes B=%d V=%d", B, V);
+  TV_REQUIRE(n_max >= 1 && n_max <= tv::kMaxNodes, TV_ERR_UNSUPPORTED,
+             "tv_tree_accept: n_max = %d not in [1, 64]", n_max);
+  TV_REQUIRE(tv::aligned16(target_logits) && (!sampling || tv::aligned16(draft_logits)), TV_ERR_INVALID_ARG,
+             "tv_tree_accept: logits must be 16-byte aligned");
+  const int per = (V + tv::kCL - 1) / tv::kCL;
+  const int chunk = (per + 3) & ~3;
+  TV_REQUIRE(!sampling || chunk <= tv::kMaxChunk, TV_ERR_UNSUPPORTED,
+             "tv_tree_accept: V = %d too large for on-chip sampling (max %d)", V, tv::kMaxChunk * tv::kCL);
+  if (B == 0) return TV_OK;
+  TV_REQUIRE((int64_t)B * tv::kCL < (1ll << 31), TV_ERR_UNSUPPORTED, "tv_tree_accept: B too large");
+  tv::AcceptParams p;
+  p.target = target_logits;
+  p.draft = draft_logits;
+  p.tokens = tokens;
+  p.parents = parents;
+  p.n_nodes = n_nodes;
+  p.u_accept = u_accept;
+  p.u_sample = u_sample;
+  p.n_max = n_max;
+  p.V = V;
+  p.chunk = chunk;
+  p.k2 = sampling ? (float)(1.4426950408889634 / (double)temperature) : 0.f;
+  p.sampling = sampling ? 1 : 0;
+  p.accept_len = accept_len;
+  p.path_nodes = path_nodes;
+  p.out_tokens = out_tokens;
+  p.status = status;
+  const size_t smem = sampling ? 2ull * chunk * sizeof(float) : 0;
+  TV_CUDA_CHECK(tv::ensure_smem_attr((const void*)tv::tree_accept_kernel, 2ull * tv::kMaxChunk * sizeof(float)));
+  tv::tree_accept_kernel<<<B * tv::kCL, tv::kAccThreads, smem, tv::as_stream(stream)>>>(p);
+  TV_CUDA_CHECK(cudaGetLastError());
+  return TV_OK;
+}

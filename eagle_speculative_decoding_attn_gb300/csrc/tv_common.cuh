@@ -1,0 +1,47 @@
+// Shared host/device helpers of libtreeverify: status codes, argument checks,
+// per-thread error text and device properties.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <cstdio>
+#include <string>
+#include "../../include/treeverify.h"
+#include "tv_ptx.cuh"
+
+namespace tv {
+
+constexpr int kPageSize = 16;
+constexpr int kMaxNodes = 64;
+
+// ---------------------------------------------------------------- host errors
+void set_error(const char* fmt, ...);
+void clear_error();
+
+#define TV_REQUIRE(cond, code, ...)      \
+  do {                                   \
+    if (!(cond)) {                       \
+      ::tv::set_error(__VA_ARGS__);      \
+      return (code);                     \
+    }                                    \
+  } while (0)
+
+#define TV_CUDA_CHECK(expr)                                                        \
+  do {                                                                             \
+    cudaError_t _e = (expr);                                                       \
+    if (_e != cudaSuccess) {                                                       \
+      ::tv::set_error("%s failed: %s", #expr, cudaGetErrorString(_e));             \
+      return TV_ERR_CUDA;                                                          \
+    }                                                                              \
+  } while (0)
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// SM count of the current device (cached per device id).
+int current_sm_count();
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (device, kernel).
+cudaError_t ensure_smem_attr(const void* func, size_t bytes);
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace tv

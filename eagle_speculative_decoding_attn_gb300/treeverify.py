@@ -1,0 +1,208 @@
+"""Python binding of libtreeverify.so (ctypes; argument marshalling only).
+
+Every step of the tree-verification path runs in the library's CUDA kernels;
+this module only passes torch tensors' device pointers, sizes and the current
+CUDA stream through the C ABI declared in ``include/treeverify.h``, and
+allocates output tensors with torch when the caller does not supply them.
+There is no CPU fallback: when the library is missing or a call fails, an
+exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtreeverify.so")
+
+TV_OK = 0
+TV_ERR_INVALID_ARG = -1
+TV_ERR_UNSUPPORTED = -2
+TV_ERR_WORKSPACE = -3
+TV_ERR_CUDA = -4
+
+TV_DEV_BAD_TREE = 1
+TV_DEV_PAGE_OOB = 2
+TV_DEV_CAPACITY = 4
+TV_DEV_TIMEOUT = 8
+TV_DEV_BAD_TOKEN = 16
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_F = ctypes.c_float
+
+_SIGNATURES = {
+    "tv_tree_build_mask": (_I, [_P, _P, _I, _I, _P, _P, _P, _P]),
+    "tv_tree_verify_attn_workspace": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "tv_tree_verify_attn": (_I, [_P, _P, _P, _I64, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P,
+                                 _SZ, _P, _P]),
+    "tv_tree_accept_workspace": (_SZ, [_I, _I, _I]),
+    "tv_tree_accept": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "tv_kv_commit_path": (_I, [_P, _P, _I, _I64, _I64, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "tv_last_error": (ctypes.c_char_p, []),
+    "tv_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+class TreeVerifyError(RuntimeError):
+    pass
+
+
+def load_library(path: Optional[str] = None):
+    """Load libtreeverify.so (once) and declare every entry point's signature."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise TreeVerifyError(
+            f"{p} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(rc: int, what: str):
+    if rc != TV_OK:
+        msg = load_library().tv_last_error().decode(errors="replace")
+        raise TreeVerifyError(f"{what} failed with code {rc}: {msg}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise TreeVerifyError("tensors passed to the library must live on a CUDA device")
+    if not t.is_contiguous():
+        raise TreeVerifyError("tensors passed to the library must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _expect(t: torch.Tensor, dtype, shape, name):
+    if t.dtype != dtype:
+        raise TreeVerifyError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise TreeVerifyError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+# --------------------------------------------------------------------------
+def tree_build_mask(parents: torch.Tensor, n_nodes: torch.Tensor, *, anc_mask=None, depth=None, status=None):
+    """Ancestor bit-mask (int64 view of the uint64 words) and depth per node.
+
+    parents int32 [B, n_max], n_nodes int32 [B] -> (anc_mask int64 [B, n_max],
+    depth int32 [B, n_max], status int32 [B]).
+    """
+    B, n_max = parents.shape
+    dev = parents.device
+    anc_mask = torch.empty((B, n_max), dtype=torch.int64, device=dev) if anc_mask is None else anc_mask
+    depth = torch.empty((B, n_max), dtype=torch.int32, device=dev) if depth is None else depth
+    status = torch.empty((B,), dtype=torch.int32, device=dev) if status is None else status
+    _expect(parents, torch.int32, (B, n_max), "parents")
+    _expect(n_nodes, torch.int32, (B,), "n_nodes")
+    rc = load_library().tv_tree_build_mask(_ptr(parents), _ptr(n_nodes), B, n_max, _ptr(anc_mask), _ptr(depth),
+                                           _ptr(status), _stream(dev))
+    _check(rc, "tv_tree_build_mask")
+    return anc_mask, depth, status
+
+
+def tree_verify_attn_workspace_bytes(B, n_max, Hq, Hkv, D, max_kv_len=0) -> int:
+    return int(load_library().tv_tree_verify_attn_workspace(B, n_max, Hq, Hkv, D, max_kv_len))
+
+
+def tree_verify_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_table: torch.Tensor,
+                     prefix_len: torch.Tensor, n_nodes: torch.Tensor, anc_mask: torch.Tensor, scale: float,
+                     status: torch.Tensor, *, out=None, lse=None, want_lse=True, workspace=None):
+    """Tree-masked paged attention.  q bf16 [B, n_max, Hq, D]; caches bf16
+    [num_pages, Hkv, 16, D]; page_table int32 [B, max_pages]; anc_mask int64
+    [B, n_max].  Returns (out bf16 [B, n_max, Hq, D], lse f32 [B, n_max, Hq] or None)."""
+    B, n_max, Hq, D = q.shape
+    num_pages, Hkv, P, Dk = k_cache.shape
+    dev = q.device
+    if Dk != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise TreeVerifyError("k_cache / v_cache shapes do not match q")
+    for t, nm in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        if t.dtype != torch.bfloat16:
+            raise TreeVerifyError(f"{nm} must be bfloat16")
+    _expect(page_table, torch.int32, page_table.shape, "page_table")
+    _expect(anc_mask, torch.int64, (B, n_max), "anc_mask")
+    out = torch.empty_like(q) if out is None else out
+    if lse is None and want_lse:
+        lse = torch.empty((B, n_max, Hq), dtype=torch.float32, device=dev)
+    if workspace is None:
+        nbytes = tree_verify_attn_workspace_bytes(B, n_max, Hq, Hkv, D)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    rc = load_library().tv_tree_verify_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), num_pages, _ptr(page_table), page_table.shape[1],
+        _ptr(prefix_len), _ptr(n_nodes), _ptr(anc_mask), B, n_max, Hq, Hkv, D, P, float(scale), _ptr(out),
+        _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev))
+    _check(rc, "tv_tree_verify_attn")
+    return out, lse
+
+
+def tree_accept(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor], tokens: torch.Tensor,
+                parents: torch.Tensor, n_nodes: torch.Tensor, anc_mask: Optional[torch.Tensor],
+                depth: Optional[torch.Tensor], temperature: float, u_accept: Optional[torch.Tensor],
+                u_sample: Optional[torch.Tensor], status: torch.Tensor, *, outputs=None):
+    """Greedy (temperature 0) or rejection-sampling acceptance.  Returns
+    (accept_len int32 [B], path_nodes int32 [B, n_max], out_tokens int32 [B, n_max+1])."""
+    B, n_max, V = target_logits.shape
+    dev = target_logits.device
+    if outputs is None:
+        accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+        path_nodes = torch.empty((B, n_max), dtype=torch.int32, device=dev)
+        out_tokens = torch.empty((B, n_max + 1), dtype=torch.int32, device=dev)
+    else:
+        accept_len, path_nodes, out_tokens = outputs
+    rc = load_library().tv_tree_accept(
+        _ptr(target_logits), _ptr(draft_logits), _ptr(tokens), _ptr(parents), _ptr(n_nodes), _ptr(anc_mask),
+        _ptr(depth), B, n_max, V, float(temperature), _ptr(u_accept), _ptr(u_sample), _ptr(accept_len),
+        _ptr(path_nodes), _ptr(out_tokens), None, 0, _ptr(status), _stream(dev))
+    _check(rc, "tv_tree_accept")
+    return accept_len, path_nodes, out_tokens
+
+
+def kv_commit_path(k_cache: torch.Tensor, v_cache: torch.Tensor, page_table: torch.Tensor,
+                   prefix_len: torch.Tensor, n_nodes: torch.Tensor, accept_len: torch.Tensor,
+                   path_nodes: torch.Tensor, status: torch.Tensor, *, outputs=None):
+    """Compact the accepted path's K/V in place.  Caches bf16 [num_pages, Hkv,
+    16, D] (one layer) or [n_layers, num_pages, Hkv, 16, D].  Returns
+    (committed_slots int64 [B, n_max], new_len int32 [B])."""
+    if k_cache.dim() == 4:
+        n_layers, (num_pages, Hkv, P, D) = 1, k_cache.shape
+        stride = num_pages * Hkv * P * D
+    else:
+        n_layers, num_pages, Hkv, P, D = k_cache.shape
+        stride = num_pages * Hkv * P * D
+    B, n_max = path_nodes.shape
+    dev = k_cache.device
+    if outputs is None:
+        slots = torch.empty((B, n_max), dtype=torch.int64, device=dev)
+        new_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    else:
+        slots, new_len = outputs
+    rc = load_library().tv_kv_commit_path(
+        _ptr(k_cache), _ptr(v_cache), n_layers, stride, num_pages, _ptr(page_table), page_table.shape[1],
+        _ptr(prefix_len), _ptr(n_nodes), _ptr(accept_len), _ptr(path_nodes), B, n_max, Hkv, D, P, _ptr(slots),
+        _ptr(new_len), _ptr(status), _stream(dev))
+    _check(rc, "tv_kv_commit_path")
+    return slots, new_len
+
+
+def version() -> str:
+    return load_library().tv_version().decode()

@@ -1,0 +1,196 @@
+/*
+ * treeverify.h — C ABI of the GB300 (sm_103a) tree-verification library
+ * (libtreeverify.so).
+ *
+ * The library implements the target model's verification step of EAGLE-style
+ * speculative decoding: a draft tree of at most 64 nodes (a parent-index
+ * array, node 0 = root) is scored by one tree-masked attention pass over each
+ * request's paged KV cache; the longest accepted root-to-node path is found
+ * (greedy argmax match, or rejection sampling with residual resampling at
+ * temperature T); the accepted branch's K/V is compacted into contiguous
+ * cache slots and the rejected branches are dropped.
+ *
+ * Sources (three pages on EAGLE speculative decoding):
+ *  - "SGLang EAGLE-2 Speculative Decoding" (Tech Radar), section 2,
+ *    "Dynamic Tree-Attention Masking": tree of <= 64 candidates, mask
+ *    M[i][j] = 1 iff j is an ancestor of i or i itself; one forward pass over
+ *    the whole tree; the sequence diagram of the same section: keep the KV of
+ *    the accepted branch, drop the wrong branches, return the verified tokens.
+ *  - troisinh.com "EAGLE — Draft head ...", "Why it works": verification is
+ *    rejection sampling and is lossless.
+ *  - study note "EAGLE" (estelledc.github.io), case 1 (k hits emit k+1
+ *    tokens) and case 3 (reject by the difference probability, resample).
+ *
+ * Conventions shared by every call
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, except
+ *    where stated.  The library never allocates device memory, keeps no state
+ *    across calls other than cached kernel attributes, and never synchronises
+ *    the stream; all work is enqueued on `stream` (a cudaStream_t passed as
+ *    void*; NULL = the legacy default stream).
+ *  - B = number of requests, n_max = row stride of the per-node arrays
+ *    (1 <= n_nodes[b] <= n_max <= 64).  Hq / Hkv = query / KV heads,
+ *    G = Hq / Hkv query heads share KV head h / G.  D = head dim (64 or 128).
+ *    page_size must be 16.
+ *  - Host-side argument errors return a negative TV_ERR_* code before any
+ *    launch.  Data errors found on the device never trap: they are OR-ed into
+ *    the per-request int32 `status` word as TV_DEV_* bits and that request's
+ *    outputs are written as documented (zeros / -1).  tv_tree_build_mask
+ *    writes `status`; the other calls read it on entry, skip requests whose
+ *    status is non-zero and OR in their own bits.
+ *  - Return value: TV_OK (0) or a negative TV_ERR_* code; tv_last_error()
+ *    gives a message for the calling thread's last failure.
+ */
+#ifndef TREEVERIFY_H_
+#define TREEVERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* host return codes */
+#define TV_OK                0
+#define TV_ERR_INVALID_ARG  (-1)  /* NULL pointer, bad size, misaligned pointer          */
+#define TV_ERR_UNSUPPORTED  (-2)  /* D not in {64,128}, page_size != 16, Hq % Hkv != 0 ... */
+#define TV_ERR_WORKSPACE    (-3)  /* workspace smaller than the *_workspace() query        */
+#define TV_ERR_CUDA         (-4)  /* a CUDA runtime call or launch failed                  */
+
+/* device status bits (per request, OR-ed) */
+#define TV_DEV_BAD_TREE   1   /* parent[0] != -1, parent[i] not in [0, i), n_nodes not in [1, n_max] */
+#define TV_DEV_PAGE_OOB   2   /* a needed page id is outside [0, num_pages)                        */
+#define TV_DEV_CAPACITY   4   /* L + N positions do not fit in max_pages * page_size               */
+#define TV_DEV_TIMEOUT    8   /* a bounded on-chip wait gave up (about one second)                */
+#define TV_DEV_BAD_TOKEN 16   /* a drafted token id is outside [0, V)                              */
+
+/*
+ * tv_tree_build_mask — the tree-attention mask (Tech Radar section 2, the mask
+ * M: bit j of anc_mask[b][i] is set iff node j is an ancestor of node i or i
+ * itself) and each node's depth (root = 0; RoPE positions are L + depth).
+ *
+ *  parents  int32 [B, n_max]  parent index per node, parents[b][0] = -1
+ *  n_nodes  int32 [B]         nodes of request b
+ *  anc_mask uint64 [B, n_max] out; entries i >= n_nodes[b] are 0
+ *  depth    int32 [B, n_max]  out; entries i >= n_nodes[b] are -1
+ *  status   int32 [B]         out (written, not OR-ed): 0 or TV_DEV_BAD_TREE
+ *                             (an invalid tree gets all-zero mask / -1 depth)
+ */
+int tv_tree_build_mask(const int32_t* parents, const int32_t* n_nodes, int B, int n_max,
+                       uint64_t* anc_mask, int32_t* depth, int32_t* status, void* stream);
+
+/*
+ * Workspace size in bytes that tv_tree_verify_attn needs for these sizes
+ * (split-KV partial outputs, the work list and scheduling counters).
+ * max_kv_len bounds prefix_len[b] + n_nodes[b] over the batch.
+ */
+size_t tv_tree_verify_attn_workspace(int B, int n_max, int Hq, int Hkv, int D, int max_kv_len);
+
+/*
+ * tv_tree_verify_attn — one tree-masked attention pass of every tree node over
+ * its request's paged KV cache (Tech Radar section 2: one forward pass scores
+ * every branch, with the mask M).  For request b, query head h, node i:
+ *
+ *   visible keys = prefix positions 0..L-1  and  tree positions L+j, j in A(i)
+ *   s_t = scale * <q, k_t>,  out = sum_t softmax(s)_t v_t,
+ *   lse = ln sum_t exp(s_t)
+ *
+ * where L = prefix_len[b] and A(i) = ancestors of i plus i (anc_mask[b][i]).
+ * The tree's own K/V must already sit at logical positions L..L+N-1 of the
+ * request's pages; logical position t lives in physical page
+ * page_table[b][t / 16], row t % 16.
+ *
+ *  q          bf16 [B, n_max, Hq, D]          (16-byte aligned)
+ *  k_cache    bf16 [num_pages, Hkv, 16, D]     (16-byte aligned)
+ *  v_cache    bf16 [num_pages, Hkv, 16, D]     (16-byte aligned)
+ *  page_table int32 [B, max_pages]
+ *  prefix_len int32 [B], n_nodes int32 [B], anc_mask uint64 [B, n_max]
+ *  out        bf16 [B, n_max, Hq, D]  out; rows i >= n_nodes[b] untouched,
+ *                                      a request with non-zero status gets zeros
+ *  lse        float [B, n_max, Hq]    out, may be NULL
+ *  ws/ws_bytes  device workspace of at least tv_tree_verify_attn_workspace() bytes
+ *  status     int32 [B]  in/out: TV_DEV_PAGE_OOB | TV_DEV_CAPACITY | TV_DEV_TIMEOUT
+ *
+ * Returns TV_ERR_UNSUPPORTED for D not in {64,128}, page_size != 16,
+ * Hq % Hkv != 0 or 128 % G != 0.
+ */
+int tv_tree_verify_attn(const void* q, const void* k_cache, const void* v_cache, int64_t num_pages,
+                        const int32_t* page_table, int max_pages, const int32_t* prefix_len,
+                        const int32_t* n_nodes, const uint64_t* anc_mask, int B, int n_max, int Hq,
+                        int Hkv, int D, int page_size, float scale, void* out, float* lse, void* ws,
+                        size_t ws_bytes, int32_t* status, void* stream);
+
+/*
+ * Workspace size in bytes that tv_tree_accept needs (currently 0: the
+ * acceptance keeps its per-node rows on chip).
+ */
+size_t tv_tree_accept_workspace(int B, int n_max, int V);
+
+/*
+ * tv_tree_accept — find the longest accepted root-to-node path and the tokens
+ * to emit.
+ *
+ * Greedy (temperature == 0): node j (non-root) hits iff tokens[j] equals the
+ * argmax of target_logits at parent(j) (lowest index on ties); node c is
+ * accepted iff every non-root node on its root path hits; the result is the
+ * deepest accepted node (lowest index on ties); the bonus token is the argmax
+ * at the result (k hits emit k+1 tokens: study note case 1).
+ *
+ * Sampling (temperature > 0): walk from the root; at node n let
+ * p = softmax(target[n]/T), q = softmax(draft[n]/T); try n's children c in
+ * ascending index: accept iff u_accept[c] * q(x_c) < p(x_c); on rejection
+ * replace p by max(0, p - q) normalised (unchanged if that sums to 0).  The
+ * first accepted child becomes the next node.  When no child is accepted (or n
+ * is a leaf) the bonus token is min{ j : u_sample[n] * S < C_j } over the
+ * running sum C of the current p (troisinh.com "Why it works"; study note
+ * case 3).
+ *
+ *  target_logits float [B, n_max, V]; draft_logits float [B, n_max, V] (row n =
+ *    the distribution n's children were drawn from; may be NULL when greedy)
+ *  tokens   int32 [B, n_max]  drafted token of each node (root entry ignored)
+ *  parents, n_nodes, anc_mask, depth: as produced by tv_tree_build_mask
+ *  u_accept, u_sample  float [B, n_max] uniforms in [0, 1) (unused when greedy)
+ *  accept_len  int32 [B]          out: accepted non-root nodes a
+ *  path_nodes  int32 [B, n_max]   out: 0, n_1 .. n_a, then -1
+ *  out_tokens  int32 [B, n_max+1] out: tokens of n_1..n_a, the bonus, then -1
+ *  status      int32 [B]          in/out: TV_DEV_BAD_TOKEN
+ */
+int tv_tree_accept(const float* target_logits, const float* draft_logits, const int32_t* tokens,
+                   const int32_t* parents, const int32_t* n_nodes, const uint64_t* anc_mask,
+                   const int32_t* depth, int B, int n_max, int V, float temperature,
+                   const float* u_accept, const float* u_sample, int32_t* accept_len,
+                   int32_t* path_nodes, int32_t* out_tokens, void* ws, size_t ws_bytes,
+                   int32_t* status, void* stream);
+
+/*
+ * tv_kv_commit_path — keep the accepted branch's K/V, drop the rejected ones
+ * (Tech Radar section 2, sequence diagram).  For k = 1..a (a = accept_len[b],
+ * n_k = path_nodes[b][k]) the K and V rows at logical position L + n_k move
+ * to L + k, in every layer and KV head; the root stays at L.  Moves with
+ * n_k == k are skipped; a source is always read before any overlapping
+ * destination is written.
+ *
+ *  k_cache, v_cache   bf16; layer l's cache [num_pages, Hkv, 16, D] starts
+ *                     layer_stride_elems elements after layer l-1's (16-byte aligned)
+ *  committed_slots    int64 [B, n_max] out: page_table[(L+k)/16]*16 + (L+k)%16
+ *                     for k = 0..a, then -1
+ *  new_len            int32 [B] out: L + a + 1 (L for a request with non-zero status)
+ *  status             int32 [B] in/out: TV_DEV_PAGE_OOB | TV_DEV_CAPACITY | TV_DEV_BAD_TREE
+ *                     (a path that is not a root-first increasing chain)
+ */
+int tv_kv_commit_path(void* k_cache, void* v_cache, int n_layers, int64_t layer_stride_elems,
+                      int64_t num_pages, const int32_t* page_table, int max_pages,
+                      const int32_t* prefix_len, const int32_t* n_nodes, const int32_t* accept_len,
+                      const int32_t* path_nodes, int B, int n_max, int Hkv, int D, int page_size,
+                      int64_t* committed_slots, int32_t* new_len, int32_t* status, void* stream);
+
+/* Message for the calling thread's last failed call ("" if none). */
+const char* tv_last_error(void);
+
+/* Library version string. */
+const char* tv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TREEVERIFY_H_ */

@@ -122,6 +122,11 @@ def tree_build_mask(parents: np.ndarray, n_nodes: np.ndarray):
 # step 2: tree-verify attention
 # --------------------------------------------------------------------------
 def _request_pages_ok(page_table_row, L, N, num_pages, page_size):
+    """CAPACITY when the prefix length is negative or the L + N positions do
+    not fit in the request's page-table row; otherwise PAGE_OOB when one of
+    the pages holding them is outside [0, num_pages)."""
+    if L < 0 or N < 1:
+        return STATUS_CAPACITY
     need = (L + N + page_size - 1) // page_size
     if need > len(page_table_row):
         return STATUS_CAPACITY
@@ -398,8 +403,9 @@ def kv_commit_path(k_layers, v_layers, page_table, prefix_len, n_nodes, accept_l
     for b in range(B):
         L, N, a = int(prefix_len[b]), int(n_nodes[b]), int(accept_len[b])
         st = _request_pages_ok(page_table[b], L, N, num_pages, page_size)
-        path = [int(x) for x in path_nodes[b, : a + 1]]
-        if a < 0 or a >= N or path[0] != 0 or any(path[k] >= N for k in range(a + 1)) or \
+        path = [int(x) for x in path_nodes[b, : max(a, 0) + 1]]
+        if N < 1 or N > n_max or a < 0 or a >= N or path[0] != 0 or \
+                any(path[k] >= N for k in range(a + 1)) or \
                 any(path[k] <= path[k - 1] for k in range(1, a + 1)):
             st |= STATUS_BAD_TREE
         status[b] = st

@@ -1,0 +1,87 @@
+"""Shared helpers of the GPU parity tests: move a workload to the device and
+run the library through its C ABI (via the ctypes binding)."""
+import numpy as np
+import pytest
+import torch
+
+from eagle_speculative_decoding_attn_gb300 import treeverify as tvb
+
+ATOL_MAX = 1e-2     # attention: max |gpu - oracle| (bf16 inputs, fp32 accumulation, bf16 output)
+ATOL_MEAN = 1e-3    # attention: mean |gpu - oracle|
+LSE_ATOL = 2e-3     # log-sum-exp (fp32 accumulation of ~1e4 terms, ex2.approx)
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for gpu-marked tests")
+    tvb.load_library()
+    return torch.device("cuda:0")
+
+
+def to_dev(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+
+def bf16_dev(bits, dev):
+    return to_dev(np.ascontiguousarray(bits).view(np.int16), dev).view(torch.bfloat16)
+
+
+class DevWorkload:
+    def __init__(self, w, dev, logits=True):
+        self.w = w
+        self.dev = dev
+        self.parents = to_dev(w.parents, dev)
+        self.n_nodes = to_dev(w.n_nodes, dev)
+        self.prefix_len = to_dev(w.prefix_len, dev)
+        self.page_table = to_dev(w.page_table, dev)
+        self.q = bf16_dev(w.q_bits, dev)
+        self.k = bf16_dev(w.k_bits, dev)
+        self.v = bf16_dev(w.v_bits, dev)
+        self.tokens = to_dev(w.tokens, dev)
+        self.u_accept = to_dev(w.u_accept, dev)
+        self.u_sample = to_dev(w.u_sample, dev)
+        self.target = to_dev(w.target_logits, dev) if (logits and w.target_logits is not None) else None
+        self.draft = to_dev(w.draft_logits, dev) if (logits and w.draft_logits is not None) else None
+
+    def mask(self):
+        return tvb.tree_build_mask(self.parents, self.n_nodes)
+
+    def attn(self, status=None, anc=None, k=None, v=None, page_table=None):
+        if anc is None or status is None:
+            anc, _, status = self.mask()
+        out, lse = tvb.tree_verify_attn(self.q, self.k if k is None else k, self.v if v is None else v,
+                                        self.page_table if page_table is None else page_table, self.prefix_len,
+                                        self.n_nodes, anc, self.w.scale, status)
+        torch.cuda.synchronize()
+        return out.float().cpu().numpy(), lse.cpu().numpy(), status.cpu().numpy()
+
+
+def compare_attn(out, lse, ref_out, ref_lse, w, rows=None):
+    """Element-wise comparison on every computed oracle row; returns (max, mean)."""
+    if rows is None:
+        rows = [(b, i, h) for b in range(w.B) for i in range(int(w.n_nodes[b])) for h in range(w.Hq)]
+    got = np.stack([out[b, i, h] for (b, i, h) in rows])
+    ref = np.stack([ref_out[b, i, h] for (b, i, h) in rows])
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)), "non-finite attention output"
+    mx, mean = float(err.max()), float(err.mean())
+    assert mx <= ATOL_MAX, f"max abs err {mx} > {ATOL_MAX}"
+    assert mean <= ATOL_MEAN, f"mean abs err {mean} > {ATOL_MEAN}"
+    gl = np.array([lse[b, i, h] for (b, i, h) in rows])
+    rl = np.array([ref_lse[b, i, h] for (b, i, h) in rows])
+    assert np.abs(gl - rl).max() <= LSE_ATOL, f"lse err {np.abs(gl - rl).max()}"
+    return mx, mean
+
+
+def sample_rows(w, rng, per_request=12):
+    rows = []
+    for b in range(w.B):
+        n = int(w.n_nodes[b])
+        nodes = {0, n - 1, int(rng.integers(0, n))}
+        for i in nodes:
+            heads = {0, w.Hq - 1, int(rng.integers(0, w.Hq))}
+            rows += [(b, i, h) for h in heads]
+        # every head of one node (covers the whole GQA group mapping)
+        i = int(rng.integers(0, n))
+        rows += [(b, i, h) for h in range(min(w.Hq, per_request))]
+    return sorted(set(rows))
