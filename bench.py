@@ -1,0 +1,488 @@
+#!/usr/bin/env python
+"""Benchmark of the tree-verification step on GB300.
+
+One step = the whole hot path over one batch of synthetic input:
+tv_tree_build_mask -> tv_tree_verify_attn -> tv_tree_accept -> tv_kv_commit_path.
+The default workload is the Llama-2-7B-shaped verify (batch 1, 32 heads MHA,
+head dim 128, prefix 2048, a 64-node depth-6 tree, greedy acceptance over
+32000 logits, commit across 32 layers).
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and torch.cuda.synchronize(); CUDA events on the launching stream.  Each step
+is one replay of a CUDA graph of the four calls; R rotated copies of the
+inputs (KV cache, queries, logits) make the data one step reads exceed 3x L2,
+so no step finds the previous step's inputs in L2.  The attention call and
+the accept+commit pair are then timed on their own (graphs of the same calls
+over the same rotation) for the roofline object.
+
+--impl reference times the fp64 CPU oracle instead (single thread, bounded
+sample of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "tree-verify attention TB/s & % roofline; verified tree nodes/s; accept+commit µs"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="llama2_7b")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-attn", type=int, default=0,
+                    help="only run this many eager tv_tree_verify_attn calls (for profiler captures)")
+    ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ oracle leg
+def oracle_sample_plan(cfg_name):
+    """Bounded sample of the workload for the CPU oracle."""
+    from eagle_speculative_decoding_attn_gb300 import workloads as W
+    cfg = W.CONFIG_BY_NAME[cfg_name]
+    if cfg_name in ("tiny", "llama2_7b"):
+        return dict(B=cfg.B, heads=cfg.Hq, desc="the full step (all requests, all heads)")
+    heads = max(1, cfg.Hq // 16)
+    return dict(B=1, heads=heads,
+                desc=f"one request drawn from the same generator, {heads} of {cfg.Hq} query heads for "
+                     f"attention, full accept/commit; scaled to the full batch by attention key counts")
+
+
+def run_oracle_sample(cfg_name):
+    """Time the oracle (as it stands) on the bounded sample; returns seconds
+    per full step (scaled) and the sample description."""
+    import numpy as np
+    import oracle
+    from eagle_speculative_decoding_attn_gb300 import workloads as W
+    plan = oracle_sample_plan(cfg_name)
+    cfg = W.CONFIG_BY_NAME[cfg_name]
+    w = W.make_workload(cfg_name, B=plan["B"])
+    full = W.make_workload(cfg_name, with_logits=False) if plan["B"] != cfg.B else w
+    rows = [(b, i, h) for b in range(w.B) for i in range(int(w.n_nodes[b])) for h in range(plan["heads"])]
+    t0 = time.perf_counter()
+    oracle.tree_build_mask(w.parents, w.n_nodes)
+    t1 = time.perf_counter()
+    oracle.tree_verify_attn(w.q_bits, w.k_bits, w.v_bits, w.page_table, w.prefix_len, w.n_nodes, w.parents,
+                            w.scale, rows=rows)
+    t2 = time.perf_counter()
+    if w.temperature > 0:
+        acc = oracle.tree_accept_sampling(w.target_logits, w.draft_logits, w.tokens, w.parents, w.n_nodes,
+                                          w.temperature, w.u_accept, w.u_sample)
+    else:
+        acc = oracle.tree_accept_greedy(w.target_logits, w.tokens, w.parents, w.n_nodes)
+    t3 = time.perf_counter()
+    oracle.kv_commit_path(w.k_bits[None], w.v_bits[None], w.page_table, w.prefix_len, w.n_nodes,
+                          acc["accept_len"], acc["path_nodes"])
+    t4 = time.perf_counter()
+    tot_keys = float(np.sum((full.prefix_len.astype(np.float64) + full.n_nodes) * full.n_nodes) * full.Hq)
+    smp_keys = float(sum(int(w.prefix_len[b]) + int(w.n_nodes[b]) for (b, i, h) in rows))
+    f_attn = tot_keys / max(smp_keys, 1.0)
+    f_req = full.B / w.B
+    t_step = (t1 - t0) * f_req + (t2 - t1) * f_attn + (t3 - t2) * f_req + (t4 - t3) * f_req * cfg.n_layers_commit
+    return dict(seconds_per_step=t_step, nodes=float(np.sum(full.n_nodes)), cpu_seconds=t4 - t0,
+                desc=plan["desc"])
+
+
+def oracle_leg_subprocess(cfg_name):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               NUMEXPR_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", "--config", cfg_name],
+                       env=env, capture_output=True, text=True, timeout=1200)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline_obj(res):
+    return {"value": res["nodes"] / res["seconds_per_step"], "unit": "nodes/s", "cores": 1, "kind": "oracle",
+            "sample": f"{res['desc']}; {res['cpu_seconds']:.1f} s of single-thread CPU work, "
+                      f"{res['seconds_per_step']:.1f} s per full step"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, cuda_index):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        self.gpu = ids[cuda_index] if cuda_index < len(ids) and ids[cuda_index].isdigit() else str(cuda_index)
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [[c.strip() for c in r.split(",")] for r in out.strip().splitlines() if r.count(",") >= 8]
+        num = lambda x: x.replace(".", "", 1).isdigit()
+        sm = sorted(float(r[1]) for r in rows if num(r[1]))
+        mx = [float(r[2]) for r in rows if num(r[2])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for k, nm in enumerate(names):
+                if r[5 + k] == "Active":
+                    reasons.add(nm)
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ GPU leg
+def profile_attn(args, W, tvb, dev):
+    """A small self-contained command for profiler captures: mask once, then
+    N eager attention calls on the chosen config."""
+    import numpy as np
+    import torch
+    w = W.make_workload(args.config, with_logits=False)
+    g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    bf = lambda bits: g(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+    parents, n_nodes = g(w.parents), g(w.n_nodes)
+    q, k, v = bf(w.q_bits), bf(w.k_bits), bf(w.v_bits)
+    pt, L = g(w.page_table), g(w.prefix_len)
+    anc, depth, status = tvb.tree_build_mask(parents, n_nodes)
+    ws = tvb.new_attn_workspace(w.B, w.n_max, w.Hq, w.Hkv, w.D, dev)
+    for _ in range(args.profile_attn):
+        tvb.tree_verify_attn(q, k, v, pt, L, n_nodes, anc, w.scale, status, workspace=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_attn": args.config, "calls": args.profile_attn,
+                      "status": status.cpu().numpy().tolist(), "kv_bytes": int(w.k_bits.nbytes * 2)}))
+
+
+def main():
+    args = parse_args()
+    if args.oracle_sample:
+        print(json.dumps(run_oracle_sample(args.config)))
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from eagle_speculative_decoding_attn_gb300 import build as tvbuild
+    from eagle_speculative_decoding_attn_gb300 import treeverify as tvb
+    from eagle_speculative_decoding_attn_gb300 import workloads as W
+
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0:
+        tvbuild.build()
+    if world > 1:
+        dist.barrier()
+    tvb.load_library()
+    if args.profile_attn:
+        return profile_attn(args, W, tvb, dev)
+
+    cfg = W.CONFIG_BY_NAME[args.config]
+    w = W.make_workload(cfg)
+    B, n_max, Hq, Hkv, D, V = w.B, w.n_max, w.Hq, w.Hkv, w.D, w.V
+    sampling = w.temperature > 0
+    layers = cfg.n_layers_commit
+    g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    bf = lambda bits: g(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    # bytes one step reads: layer-0 KV (attention), queries, logits
+    per_copy = w.k_bits.nbytes * 2 + w.q_bits.nbytes + w.target_logits.nbytes * (2 if sampling else 1)
+    R = min(16, max(1, math.ceil(3 * L2_BYTES / per_copy)))
+
+    shared = dict(parents=g(w.parents), n_nodes=g(w.n_nodes), prefix_len=g(w.prefix_len),
+                  page_table=g(w.page_table), tokens=g(w.tokens), u_accept=g(w.u_accept), u_sample=g(w.u_sample))
+    k0, v0, q0, t0 = bf(w.k_bits), bf(w.v_bits), bf(w.q_bits), g(w.target_logits)
+    d0 = g(w.draft_logits) if sampling else None
+    copies = []
+    for _ in range(R):
+        copies.append(dict(
+            k=k0.unsqueeze(0).repeat(layers, 1, 1, 1, 1).contiguous(),
+            v=v0.unsqueeze(0).repeat(layers, 1, 1, 1, 1).contiguous(),
+            q=q0.clone(), target=t0.clone(), draft=d0.clone() if sampling else None,
+            ws=tvb.new_attn_workspace(B, n_max, Hq, Hkv, D, dev),
+            anc=torch.empty((B, n_max), dtype=torch.int64, device=dev),
+            depth=torch.empty((B, n_max), dtype=torch.int32, device=dev),
+            status=torch.empty((B,), dtype=torch.int32, device=dev),
+            out=torch.empty_like(q0), lse=torch.empty((B, n_max, Hq), dtype=torch.float32, device=dev),
+            acc=(torch.empty((B,), dtype=torch.int32, device=dev),
+                 torch.empty((B, n_max), dtype=torch.int32, device=dev),
+                 torch.empty((B, n_max + 1), dtype=torch.int32, device=dev)),
+            com=(torch.empty((B, n_max), dtype=torch.int64, device=dev),
+                 torch.empty((B,), dtype=torch.int32, device=dev))))
+    del k0, v0
+
+    def mask_call(cp):
+        tvb.tree_build_mask(shared["parents"], shared["n_nodes"], anc_mask=cp["anc"], depth=cp["depth"],
+                            status=cp["status"])
+
+    def attn_call(cp):
+        tvb.tree_verify_attn(cp["q"], cp["k"][0], cp["v"][0], shared["page_table"], shared["prefix_len"],
+                             shared["n_nodes"], cp["anc"], w.scale, cp["status"], out=cp["out"], lse=cp["lse"],
+                             workspace=cp["ws"])
+
+    def accept_commit_call(cp):
+        tvb.tree_accept(cp["target"], cp["draft"], shared["tokens"], shared["parents"], shared["n_nodes"],
+                        cp["anc"], cp["depth"], w.temperature, shared["u_accept"] if sampling else None,
+                        shared["u_sample"] if sampling else None, cp["status"], outputs=cp["acc"])
+        tvb.kv_commit_path(cp["k"], cp["v"], shared["page_table"], shared["prefix_len"], shared["n_nodes"],
+                           cp["acc"][0], cp["acc"][1], cp["status"], outputs=cp["com"])
+
+    def step_call(cp):
+        mask_call(cp)
+        attn_call(cp)
+        accept_commit_call(cp)
+
+    launches_per_step = tvb.launches_per_step()
+    for cp in copies:                      # eager warm-up sets kernel attributes before capture
+        step_call(cp)
+    torch.cuda.synchronize()
+
+    side = torch.cuda.Stream(dev)
+    graphs, attn_graph, ac_graph = [], torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        for cp in copies:
+            gph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gph, stream=side):
+                step_call(cp)
+            graphs.append(gph)
+        with torch.cuda.graph(attn_graph, stream=side):
+            for cp in copies:
+                attn_call(cp)
+        with torch.cuda.graph(ac_graph, stream=side):
+            for cp in copies:
+                accept_commit_call(cp)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    K, Wm = args.steps, args.warmup
+    for i in range(Wm):
+        graphs[i % R].replay()
+    barrier()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        graphs[i % R].replay()
+    e1.record(stream)
+    barrier()
+    step_ms = e0.elapsed_time(e1) / K
+
+    # the attention call alone and the accept+commit pair alone, same rotation
+    reps = max(1, K // R)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    attn_graph.replay()
+    a0.record(stream)
+    for _ in range(reps):
+        attn_graph.replay()
+    a1.record(stream)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ac_graph.replay()
+    c0.record(stream)
+    for _ in range(reps):
+        ac_graph.replay()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    attn_us = a0.elapsed_time(a1) * 1000.0 / (reps * R)
+    ac_us = c0.elapsed_time(c1) * 1000.0 / (reps * R)
+
+    # end to end through the public binding with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = dict(q=w.q_bits.view(np.int16), target=w.target_logits, parents=w.parents, n_nodes=w.n_nodes,
+                       prefix_len=w.prefix_len, page_table=w.page_table, tokens=w.tokens)
+        if sampling:
+            host_in.update(draft=w.draft_logits, u_accept=w.u_accept, u_sample=w.u_sample)
+        pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host_in.items()}
+        dev_in = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in pinned.items()}
+        h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+        cp0 = copies[0]
+        res_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                    for t in (cp0["acc"][0], cp0["acc"][1], cp0["acc"][2], cp0["com"][1], cp0["com"][0])]
+        d2h = sum(t.numel() * t.element_size() for t in res_host)
+
+        def e2e_step(k):
+            cpk = copies[k % R]
+            for kk in pinned:
+                dev_in[kk].copy_(pinned[kk], non_blocking=True)
+            anc, depth, st = tvb.tree_build_mask(dev_in["parents"], dev_in["n_nodes"], anc_mask=cpk["anc"],
+                                                 depth=cpk["depth"], status=cpk["status"])
+            tvb.tree_verify_attn(dev_in["q"].view(torch.bfloat16), cpk["k"][0], cpk["v"][0], dev_in["page_table"],
+                                 dev_in["prefix_len"], dev_in["n_nodes"], anc, w.scale, st, out=cpk["out"],
+                                 lse=cpk["lse"], workspace=cpk["ws"])
+            acc = tvb.tree_accept(dev_in["target"], dev_in.get("draft"), dev_in["tokens"], dev_in["parents"],
+                                  dev_in["n_nodes"], anc, depth, w.temperature, dev_in.get("u_accept"),
+                                  dev_in.get("u_sample"), st, outputs=cpk["acc"])
+            com = tvb.kv_commit_path(cpk["k"], cpk["v"], dev_in["page_table"], dev_in["prefix_len"],
+                                     dev_in["n_nodes"], acc[0], acc[1], st, outputs=cpk["com"])
+            for hdst, dsrc in zip(res_host, [acc[0], acc[1], acc[2], com[1], com[0]]):
+                hdst.copy_(dsrc, non_blocking=True)
+
+        K2 = min(K, 500)
+        for k in range(min(Wm, 5)):
+            e2e_step(k)
+        barrier()
+        t_start = time.perf_counter()
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for k in range(K2):
+            e2e_step(k)
+        x1.record(stream)
+        barrier()
+        wall = time.perf_counter() - t_start
+        e2e_ms = max(x0.elapsed_time(x1), wall * 1000.0) / K2
+        e2e = {"value": float(np.sum(w.n_nodes)) / (e2e_ms / 1000.0), "unit": "nodes/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
+               "steps": K2,
+               "note": "python binding calls per step; KV cache resident in HBM; queries, tree, logits and "
+                       "uniforms copied from pinned host memory each step; results copied back"}
+
+    nodes = float(np.sum(w.n_nodes))
+    nodes_total = nodes
+    if world > 1:
+        t = torch.tensor([step_ms, attn_us, ac_us], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, attn_us, ac_us = [float(x) for x in t.tolist()]
+        nn = torch.tensor([nodes], device=dev, dtype=torch.float64)
+        dist.all_reduce(nn)
+        nodes_total = float(nn.item())
+        if e2e is not None:
+            te = torch.tensor([e2e["ms_per_step"]], device=dev, dtype=torch.float64)
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+            e2e["ms_per_step"] = float(te.item())
+            e2e["value"] = nodes_total / (e2e["ms_per_step"] / 1000.0)
+
+    hbm, tf_burst, peak_src = load_peaks()
+    abytes, aflops = w.attn_bytes(), w.attn_flops()
+    t_hbm = abytes / (hbm * 1e9)
+    t_tc = aflops / (tf_burst * 1e12)
+    attn_s = attn_us * 1e-6
+    if t_hbm >= t_tc:
+        bound, achieved, peak, unit = "hbm", abytes / attn_s / 1e9, hbm, "GB/s"
+    else:
+        bound, achieved, peak, unit = "tensor", aflops / attn_s / 1e12, tf_burst, "TFLOP/s"
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", f"traffic_{args.config}.json")
+    if os.path.exists(tr_path):
+        with open(tr_path) as f:
+            traffic = json.load(f).get("dram_bytes_per_launch")
+
+    line = {
+        "metric": METRIC,
+        "value": nodes_total / (step_ms / 1000.0),
+        "unit": "nodes/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": Wm,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64; random bf16 KV/Q ~ N(0,1), Gaussian fp32 logits)",
+        "config": {"workload": f"{cfg.name}: B={B}, Hq={Hq}, Hkv={Hkv}, D={D}, prefix={cfg.prefix}, "
+                               f"nodes={cfg.n_nodes}, V={V}, T={w.temperature}, commit layers={layers}",
+                   "global_batch": B * world, "parallelism": f"replicas x{world}",
+                   "l2": f"{R} rotated input copies ({R * per_copy / 1e6:.0f} MB read per rotation) > 3x L2",
+                   "step": "mask + attention + accept + commit, one CUDA graph replay"},
+        "attn_us": attn_us,
+        "attn_tbps": abytes / attn_s / 1e12,
+        "attn_roofline_frac": max(t_hbm, t_tc) / attn_s,
+        "attn_nodes_per_s": nodes_total / attn_s,
+        "accept_commit_us": ac_us,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                     "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json)",
+                     "algorithmic": {"bytes": abytes, "flops": aflops}},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = cpu_baseline_obj(oracle_leg_subprocess(args.config))
+        except Exception as ex:  # report it, keep the GPU line
+            line["cpu_baseline"] = {"value": None, "error": str(ex)[:300]}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args, world, rank):
+    """The oracle as it stands, on the host cores (single thread), on bounded
+    samples of the same workload."""
+    if rank != 0:
+        return
+    import numpy as np
+    steps = max(1, min(args.steps, 3))
+    warm = 1 if args.warmup > 0 else 0
+    for _ in range(warm):
+        oracle_leg_subprocess(args.config)
+    res, times = None, []
+    for _ in range(steps):
+        res = oracle_leg_subprocess(args.config)
+        times.append(res["seconds_per_step"])
+    sps = float(np.mean(times))
+    value = res["nodes"] / sps
+    print(json.dumps({"impl": "reference", "metric": METRIC, "value": value, "unit": "nodes/s", "n_gpus": world,
+                      "steps": steps, "warmup": warm, "ms_per_step": sps * 1000.0, "higher_is_better": True,
+                      "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                      "config": {"workload": args.config},
+                      "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": 1, "kind": "oracle",
+                                       "sample": res["desc"]},
+                      "e2e": {"value": value, "unit": "nodes/s", "h2d_bytes_per_step": 0,
+                              "d2h_bytes_per_step": 0}}))
+
+
+if __name__ == "__main__":
+    main()

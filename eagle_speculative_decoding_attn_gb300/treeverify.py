@@ -125,6 +125,13 @@ def tree_verify_attn_workspace_bytes(B, n_max, Hq, Hkv, D, max_kv_len=0) -> int:
     return int(load_library().tv_tree_verify_attn_workspace(B, n_max, Hq, Hkv, D, max_kv_len))
 
 
+def new_attn_workspace(B, n_max, Hq, Hkv, D, device) -> torch.Tensor:
+    """A zero-filled workspace for tv_tree_verify_attn, reusable for later
+    calls of the same sizes on the same stream."""
+    nbytes = tree_verify_attn_workspace_bytes(B, n_max, Hq, Hkv, D)
+    return torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
 def tree_verify_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, page_table: torch.Tensor,
                      prefix_len: torch.Tensor, n_nodes: torch.Tensor, anc_mask: torch.Tensor, scale: float,
                      status: torch.Tensor, *, out=None, lse=None, want_lse=True, workspace=None):
@@ -145,8 +152,7 @@ def tree_verify_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     if lse is None and want_lse:
         lse = torch.empty((B, n_max, Hq), dtype=torch.float32, device=dev)
     if workspace is None:
-        nbytes = tree_verify_attn_workspace_bytes(B, n_max, Hq, Hkv, D)
-        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+        workspace = new_attn_workspace(B, n_max, Hq, Hkv, D, dev)
     rc = load_library().tv_tree_verify_attn(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), num_pages, _ptr(page_table), page_table.shape[1],
         _ptr(prefix_len), _ptr(n_nodes), _ptr(anc_mask), B, n_max, Hq, Hkv, D, P, float(scale), _ptr(out),
@@ -206,3 +212,12 @@ def kv_commit_path(k_cache: torch.Tensor, v_cache: torch.Tensor, page_table: tor
 
 def version() -> str:
     return load_library().tv_version().decode()
+
+
+# kernel launches each call enqueues (mask, attention, accept, commit)
+LAUNCHES = {"tree_build_mask": 1, "tree_verify_attn": 3, "tree_accept": 1, "kv_commit_path": 1}
+
+
+def launches_per_step() -> int:
+    """Kernel launches of one verification step (the four calls once each)."""
+    return sum(LAUNCHES.values())
