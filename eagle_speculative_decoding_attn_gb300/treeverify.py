@@ -215,7 +215,7 @@ def version() -> str:
 
 
 # kernel launches each call enqueues (mask, attention, accept, commit)
-LAUNCHES = {"tree_build_mask": 1, "tree_verify_attn": 3, "tree_accept": 1, "kv_commit_path": 1}
+LAUNCHES = {"tree_build_mask": 1, "tree_verify_attn": 1, "tree_accept": 1, "kv_commit_path": 1}
 
 
 def launches_per_step() -> int:

@@ -81,8 +81,11 @@ int tv_tree_build_mask(const int32_t* parents, const int32_t* n_nodes, int B, in
 
 /*
  * Workspace size in bytes that tv_tree_verify_attn needs for these sizes
- * (split-KV partial outputs, the work list and scheduling counters).
- * max_kv_len bounds prefix_len[b] + n_nodes[b] over the batch.
+ * (split-KV partial outputs, split tickets, error bits, an exit counter).
+ * The caller zero-fills the workspace once after allocating it; every call
+ * leaves it zeroed again, so it can be reused by later calls of the same
+ * sizes.  Calls that may overlap in time need separate workspaces.
+ * max_kv_len is accepted for interface stability and is not used.
  */
 size_t tv_tree_verify_attn_workspace(int B, int n_max, int Hq, int Hkv, int D, int max_kv_len);
 
@@ -105,14 +108,16 @@ size_t tv_tree_verify_attn_workspace(int B, int n_max, int Hq, int Hkv, int D, i
  *  v_cache    bf16 [num_pages, Hkv, 16, D]     (16-byte aligned)
  *  page_table int32 [B, max_pages]
  *  prefix_len int32 [B], n_nodes int32 [B], anc_mask uint64 [B, n_max]
- *  out        bf16 [B, n_max, Hq, D]  out; rows i >= n_nodes[b] untouched,
- *                                      a request with non-zero status gets zeros
+ *  out        bf16 [B, n_max, Hq, D]  out; rows i >= n_nodes[b] untouched; a
+ *                                      request with non-zero status gets zeros in
+ *                                      all n_max rows (and in lse)
  *  lse        float [B, n_max, Hq]    out, may be NULL
  *  ws/ws_bytes  device workspace of at least tv_tree_verify_attn_workspace() bytes
  *  status     int32 [B]  in/out: TV_DEV_PAGE_OOB | TV_DEV_CAPACITY | TV_DEV_TIMEOUT
  *
  * Returns TV_ERR_UNSUPPORTED for D not in {64,128}, page_size != 16,
- * Hq % Hkv != 0 or 128 % G != 0.
+ * Hq % Hkv != 0, 128 % G != 0 or B > 1024.  One kernel launch: the work is
+ * divided evenly over the SMs and split key ranges are merged in-kernel.
  */
 int tv_tree_verify_attn(const void* q, const void* k_cache, const void* v_cache, int64_t num_pages,
                         const int32_t* page_table, int max_pages, const int32_t* prefix_len,

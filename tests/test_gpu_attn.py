@@ -181,7 +181,7 @@ def test_attn_host_argument_errors():
     dw = DevWorkload(w, dev, logits=False)
     anc, _, status = dw.mask()
     lib = tvb.load_library()
-    ws = torch.empty(tvb.tree_verify_attn_workspace_bytes(1, w.n_max, 4, 4, 64), dtype=torch.uint8, device=dev)
+    ws = tvb.new_attn_workspace(1, w.n_max, 4, 4, 64, dev)
     o = torch.empty_like(dw.q)
     import ctypes
     P = lambda t: ctypes.c_void_p(t.data_ptr())
