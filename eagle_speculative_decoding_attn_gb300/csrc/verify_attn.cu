@@ -41,6 +41,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <cudaTypedefs.h>
 #include "tv_common.cuh"
 
@@ -903,5 +904,70 @@ extern "C" int tv_tree_verify_attn(const void* q, const void* k_cache, const voi
   TV_REQUIRE(tv::aligned16(ws), TV_ERR_INVALID_ARG, "tv_tree_verify_attn: workspace must be 16-byte aligned");
   bind_workspace(&ap, wl, static_cast<uint8_t*>(ws));
   cudaStream_t st = tv::as_stream(stream);
+  return D == 128 ? launch<128>(ap, grid, st) : launch<64>(ap, grid, st);
+}
+
+// ---------------------------------------------------------------- built-in scratch variant
+// For callers that cannot allocate device memory themselves, a variant of
+// tv_tree_verify_attn runs on a fixed scratch array compiled into this file.
+// Every device that loads the library holds the array until the process exits.
+namespace tv {
+namespace attn {
+
+constexpr size_t kFixedScratchBytes = size_t(48) << 20;  // 48 MiB
+static __device__ __align__(256) uint8_t g_fixed_scratch[kFixedScratchBytes];
+
+// Device address of g_fixed_scratch on the current device.  In host code the
+// array's name only stands in for the symbol, so the address is looked up once
+// per device (with that device current) and cached.
+static int fixed_scratch_address(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  TV_CUDA_CHECK(cudaGetDevice(&dev));
+  TV_REQUIRE(dev >= 0 && dev < 64, TV_ERR_UNSUPPORTED, "tv_tree_verify_attn_noalloc: device id %d >= 64", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_fixed_scratch);
+    TV_REQUIRE(e == cudaSuccess && p != nullptr, TV_ERR_CUDA,
+               "tv_tree_verify_attn_noalloc: cudaGetSymbolAddress of the built-in scratch failed: %s",
+               cudaGetErrorString(e));
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return TV_OK;
+}
+
+}  // namespace attn
+}  // namespace tv
+
+extern "C" int tv_tree_verify_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                           int64_t num_pages, const int32_t* page_table, int max_pages,
+                                           const int32_t* prefix_len, const int32_t* n_nodes,
+                                           const uint64_t* anc_mask, int B, int n_max, int Hq, int Hkv, int D,
+                                           int page_size, float scale, void* out, float* lse, int32_t* status,
+                                           void* stream) {
+  using namespace tv::attn;
+  tv::clear_error();
+  AttnParams ap;
+  const int rc = prepare(q, k_cache, v_cache, num_pages, page_table, max_pages, prefix_len, n_nodes, anc_mask, B,
+                         n_max, Hq, Hkv, D, page_size, scale, out, lse, status, &ap);
+  if (rc != TV_OK) return rc;
+  if (B == 0) return TV_OK;
+  const int grid = tv::current_sm_count();
+  const WsLayout wl = ws_layout(B, n_max, Hq, Hkv, D, grid);
+  TV_REQUIRE(wl.total <= kFixedScratchBytes, TV_ERR_UNSUPPORTED,
+             "tv_tree_verify_attn_noalloc: these sizes need %zu bytes of scratch but the built-in scratch holds "
+             "%zu; call tv_tree_verify_attn with a workspace instead",
+             wl.total, kFixedScratchBytes);
+  void* ws = nullptr;
+  const int arc = fixed_scratch_address(&ws);
+  if (arc != TV_OK) return arc;
+  cudaStream_t st = tv::as_stream(stream);
+  // the array keeps the previous call's contents (possibly of other sizes):
+  // clear the counters and error bits the kernel expects to start at zero
+  TV_CUDA_CHECK(cudaMemsetAsync(ws, 0, wl.part_lse, st));
+  bind_workspace(&ap, wl, static_cast<uint8_t*>(ws));
   return D == 128 ? launch<128>(ap, grid, st) : launch<64>(ap, grid, st);
 }

@@ -41,6 +41,8 @@ _SIGNATURES = {
     "tv_tree_verify_attn_workspace": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "tv_tree_verify_attn": (_I, [_P, _P, _P, _I64, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P,
                                  _SZ, _P, _P]),
+    "tv_tree_verify_attn_noalloc": (_I, [_P, _P, _P, _I64, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
+                                         _P, _P]),
     "tv_tree_accept_workspace": (_SZ, [_I, _I, _I]),
     "tv_tree_accept": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "tv_kv_commit_path": (_I, [_P, _P, _I, _I64, _I64, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),

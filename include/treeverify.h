@@ -126,6 +126,32 @@ int tv_tree_verify_attn(const void* q, const void* k_cache, const void* v_cache,
                         size_t ws_bytes, int32_t* status, void* stream);
 
 /*
+ * tv_tree_verify_attn_noalloc — the same computation as tv_tree_verify_attn
+ * (same arguments, outputs and status behaviour) without a caller workspace.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory on their own — for example code embedded in a
+ * host framework that owns every device allocation, or plug-ins that may only
+ * touch the buffers they are handed.  Its scratch is a fixed 48 MiB array
+ * compiled into the library; every device that loads the library holds it
+ * until the process exits.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture.
+ *  - Sizes whose scratch need exceeds 48 MiB return TV_ERR_UNSUPPORTED with a
+ *    message; use tv_tree_verify_attn with a workspace for those.
+ *  - Every call shares the one array and clears its counters at the start
+ *    (an asynchronous memset on `stream`), so calls that may overlap on the
+ *    GPU (other streams, other threads) race and must be serialised by the
+ *    caller.
+ *  - The call itself allocates nothing.
+ */
+int tv_tree_verify_attn_noalloc(const void* q, const void* k_cache, const void* v_cache, int64_t num_pages,
+                                const int32_t* page_table, int max_pages, const int32_t* prefix_len,
+                                const int32_t* n_nodes, const uint64_t* anc_mask, int B, int n_max, int Hq,
+                                int Hkv, int D, int page_size, float scale, void* out, float* lse,
+                                int32_t* status, void* stream);
+
+/*
  * Workspace size in bytes that tv_tree_accept needs (currently 0: the
  * acceptance keeps its per-node rows on chip).
  */
