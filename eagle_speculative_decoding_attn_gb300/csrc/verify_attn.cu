@@ -58,6 +58,10 @@ constexpr int kRowsPerSlot = kNT * kBM;        // rows of one partial slot
 constexpr int kMaxBatch = 1024;
 constexpr float kRescaleLog2 = 8.0f;           // lazy O rescale threshold (factor 256)
 constexpr float kLog2e = 1.4426950408889634f;
+// register split: 384 threads x 168 at launch = 128 x 88 (warps 0-3) + 256 x 208 (softmax warps)
+constexpr uint32_t kRegsControl = 88;
+constexpr uint32_t kRegsSoftmax = 208;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax == kThreads * 168, "register split must match the launch");
 
 struct AttnParams {
   CUtensorMap tmQ;
@@ -73,7 +77,7 @@ struct AttnParams {
   int32_t* ws_bits;     // [B] device-found status bits of this call (zero between calls)
   int32_t* ws_tickets;  // [B * Hkv * mp_max * 2] split arrival counters (zero between calls)
   int32_t* ws_exit;     // CTA exit counter (zero between calls)
-  float* part_o;        // [2 * gridDim][256][D]
+  float* part_o;        // [2 * gridDim][D/4][256] float4: column group major, rows contiguous
   float* part_lse;      // [2 * gridDim][256]
   int64_t num_pages;
   int B, max_pages, n_max, Hq, Hkv, G, q_box_nodes, mp_max;
@@ -99,7 +103,11 @@ struct Smem {
 // ---------------------------------------------------------------- plan
 __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 __device__ __forceinline__ int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
-__device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return a <= 0 ? 0 : (a + b - 1) / b; }
+// ceil(a / c) for a cost per tile c in {2, 3}, 0 when a <= 0
+__device__ __forceinline__ int64_t ceil_div_c(int64_t a, int c) {
+  if (a <= 0) return 0;
+  return c == 2 ? (a + 1) >> 1 : (a + 2) / 3;
+}
 
 struct PlanView {
   const int64_t* start;  // cost position of each request's first group; start[B] = W
@@ -108,9 +116,16 @@ struct PlanView {
   int B, Hkv;
   int64_t W;             // total cost (< 2^40, so k * W fits in 64 bits)
   int C;                 // CTAs that receive work
+  bool narrow;           // (C + 1) * W < 2^32: 32-bit division suffices
   // first cost position of CTA k, and the CTA owning cost position x
-  __device__ int64_t cut(int k) const { return ((int64_t)k * W + C - 1) / C; }
-  __device__ int owner(int64_t x) const { return (int)imin64(C - 1, x * C / W); }
+  __device__ int64_t cut(int k) const {
+    if (narrow) return ((uint32_t)k * (uint32_t)W + (uint32_t)(C - 1)) / (uint32_t)C;
+    return ((int64_t)k * W + C - 1) / C;
+  }
+  __device__ int owner(int64_t x) const {
+    if (narrow) return (int)min((uint32_t)(C - 1), ((uint32_t)x * (uint32_t)C) / (uint32_t)W);
+    return (int)imin64(C - 1, x * C / W);
+  }
 };
 
 struct Item {
@@ -187,8 +202,8 @@ __device__ bool iter_next(ItemIter& it, const PlanView& pv, int cta, Item& o) {
     const int nt = min(2, MT - 2 * mp);
     const int c = nt + 1;
     const int64_t gs = it.gstart;
-    const int64_t i_lo = imin64(T, ceil_div64(it.lo - gs, c));
-    const int64_t i_hi = imin64(T, ceil_div64(it.hi - gs, c));
+    const int64_t i_lo = imin64(T, ceil_div_c(it.lo - gs, c));
+    const int64_t i_hi = imin64(T, ceil_div_c(it.hi - gs, c));
     const int c_prev = it.c_prev;
     it.gstart += (int64_t)T * c;
     it.c_prev = c;
@@ -273,9 +288,10 @@ __device__ void merge_row(const AttnParams& p, const Item& it, int prow, int64_t
           const int slot = split_slot(it, sp0 + u);
           const float ls = __ldcg(p.part_lse + (int64_t)slot * kRowsPerSlot + prow);
           wv[u] = (ls == -INFINITY) ? 0.f : ex2_approx((ls - m) * kLog2e) * inv;
-          const float4* src = reinterpret_cast<const float4*>(p.part_o + ((int64_t)slot * kRowsPerSlot + prow) * D + c0);
+          const float4* src = reinterpret_cast<const float4*>(p.part_o) +
+                              ((int64_t)slot * (D / 4) + c0 / 4) * kRowsPerSlot + prow;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) x[u][q] = __ldcg(src + q);
+          for (int q = 0; q < 8; ++q) x[u][q] = __ldcg(src + q * kRowsPerSlot);
         } else {
 #pragma unroll
           for (int q = 0; q < 8; ++q) x[u][q] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -397,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
   pv.Hkv = p.Hkv;
   pv.W = plan_W;
   pv.C = plan_C;
+  pv.narrow = (int64_t)(plan_C + 1) * plan_W < (int64_t(1) << 32);
   const bool has_work = pv.W > 0 && cta < pv.C;
 
   uint8_t* sQ = smem + S::kQ;
@@ -406,6 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
 
   if (has_work && warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    setmaxnreg_dec<kRegsControl>();
     if (elect_one_sync()) {
       ItemIter it;
       iter_init(it, pv, cta);
@@ -457,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
     __syncwarp();
   } else if (has_work && warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    setmaxnreg_dec<kRegsControl>();
     if (elect_one_sync()) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
@@ -534,8 +553,11 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
       }
     }
     __syncwarp();
+  } else if (has_work && warp == 2) {
+    setmaxnreg_dec<kRegsControl>();  // TMEM owner: idle until the exit
   } else if (has_work && warp == 3) {
     // ------------------------------------------------------------ page-table check
+    setmaxnreg_dec<kRegsControl>();
     // every needed page of each request this CTA touches
     ItemIter it;
     iter_init(it, pv, cta);
@@ -553,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
     }
   } else if (has_work && warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
+    setmaxnreg_inc<kRegsSoftmax>();
     const int t = (warp - 4) >> 2;
     const int r = (warp & 3) * 32 + lane;                 // row of the M tile = TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -587,31 +610,28 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
         if (!ok) break;
         const int key0 = (item.tile_begin + j) * kBN;
         const bool masked = key0 + kBN > L;
-        uint32_t v[32];
-        // pass 1: row max over the visible keys of this tile
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
-          const uint32_t vis = masked ? visible32(key0 + c0, L, anc) : 0xffffffffu;
-          tmem_ld32(tS + c0, v);
+        // the whole 128-wide S row of this thread in registers (one TMEM load)
+        uint32_t v[kBN];
+        tmem_ld128(tS, v);
+        if (masked) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) mx = fmaxf(mx, ((vis >> c) & 1u) ? __uint_as_float(v[c]) : -INFINITY);
+          for (int c0 = 0; c0 < kBN; c0 += 32) {
+            const uint32_t vis = visible32(key0 + c0, L, anc);
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (!((vis >> c) & 1u)) v[c0 + c] = __float_as_uint(-INFINITY);
+          }
         }
+        // row max as four independent partial maxima
+        float pm[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) pm[u] = __uint_as_float(v[u]);
+#pragma unroll
+        for (int c = 4; c < kBN; ++c) pm[c & 3] = fmaxf(pm[c & 3], __uint_as_float(v[c]));
+        const float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
         const float m_new = fmaxf(m_run, mx * sl2);
         const bool grow = m_new > m_run + kRescaleLog2;
         const float alpha = grow ? ex2_approx(m_run - m_new) : 1.f;  // 0 when m_run = -inf
-        if (__any_sync(0xffffffffu, grow && j > 0)) {
-          // rescale O: the PV of the previous tile completed before S of this tile
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t o[32];
-            tmem_ld32(tO + c0, o);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st16(tO + c0, o);
-            tmem_st16(tO + c0 + 16, o + 16);
-          }
-        }
         if (grow) {
           l_run *= alpha;
           m_run = m_new;
@@ -634,22 +654,31 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
           }
           fence_proxy_async_smem();
         }
-        // pass 2: probabilities -> bf16 P over the S columns already read
-        float rs = 0.f;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
-          const uint32_t vis = masked ? visible32(key0 + c0, L, anc) : 0xffffffffu;
-          tmem_ld32(tS + c0, v);
-          uint32_t pk[16];
+        // probabilities 2^(s*scale*log2e - m), packed in place as bf16 pairs
+        float ps[4];
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const float x0 = ((vis >> c) & 1u) ? __uint_as_float(v[c]) * sl2 - m_use : -INFINITY;
-            const float x1 = ((vis >> (c + 1)) & 1u) ? __uint_as_float(v[c + 1]) * sl2 - m_use : -INFINITY;
-            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-            rs += e0 + e1;
-            pk[c >> 1] = pack_bf16x2(e0, e1);
+        for (int u = 0; u < 4; ++u) ps[u] = 0.f;
+#pragma unroll
+        for (int c = 0; c < kBN; c += 2) {
+          const float e0 = ex2_approx(fmaf(__uint_as_float(v[c]), sl2, -m_use));
+          const float e1 = ex2_approx(fmaf(__uint_as_float(v[c + 1]), sl2, -m_use));
+          ps[(c >> 1) & 3] += e0 + e1;
+          v[c >> 1] = pack_bf16x2(e0, e1);
+        }
+        tmem_st64(tS, v);
+        const float rs = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        if (__any_sync(0xffffffffu, grow && j > 0)) {
+          // rescale O (the PV of the previous tile completed before S of this tile;
+          // the next PV is issued only after this thread arrives on bar_p)
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(tO + c0, o);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            tmem_st16(tO + c0, o);
+            tmem_st16(tO + c0 + 16, o + 16);
           }
-          tmem_st16(tS + (c0 >> 1), pk);
         }
         l_run += rs;
         tmem_st_wait();
@@ -669,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
       const int64_t orow_idx = ((int64_t)item.b * p.n_max + node) * p.Hq + h;
       const bool direct = item.n_splits == 1;
       const int prow = t * kBM + r;
-      float* prow_ptr = p.part_o + ((int64_t)item.my_slot * kRowsPerSlot + prow) * D;
+      float4* pslot = reinterpret_cast<float4*>(p.part_o) + (int64_t)item.my_slot * (D / 4) * kRowsPerSlot + prow;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
@@ -684,10 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
 #pragma unroll
             for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
           } else {
-            float4* dst = reinterpret_cast<float4*>(prow_ptr + c0);
+            float4* dst = pslot + (c0 / 4) * kRowsPerSlot;
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+              dst[q * kRowsPerSlot] = make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
                                    __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
           }
         }
