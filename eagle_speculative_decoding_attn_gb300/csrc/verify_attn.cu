@@ -278,11 +278,11 @@ __device__ void merge_row(const AttnParams& p, const Item& it, int prow, int64_t
 #pragma unroll
     for (int c = 0; c < 32; ++c) acc[c] = 0.f;
 #pragma unroll 1
-    for (int sp0 = 0; sp0 < it.n_splits; sp0 += 2) {
-      float4 x[2][8];
-      float wv[2];
+    for (int sp0 = 0; sp0 < it.n_splits; sp0 += 4) {
+      float4 x[4][8];
+      float wv[4];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int u = 0; u < 4; ++u) {
         wv[u] = 0.f;
         if (sp0 + u < it.n_splits) {
           const int slot = split_slot(it, sp0 + u);
@@ -298,7 +298,7 @@ __device__ void merge_row(const AttnParams& p, const Item& it, int prow, int64_t
         }
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
+      for (int u = 0; u < 4; ++u)
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           acc[4 * q] += wv[u] * x[u][q].x;
@@ -322,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_q, bar_qe, bar_kf[kStages], bar_ke[kStages], bar_vf[kStages], bar_ve[kStages];
-  __shared__ uint64_t bar_s[kNT], bar_p[kNT], bar_o[kNT], bar_of[kNT];
+  __shared__ uint64_t bar_s[kNT], bar_p[kNT], bar_o[kNT], bar_of[kNT], bar_wg[kNT], bar_ml;
+  __shared__ float ml_sh[2][kBM];  // dual mode: warpgroup 1's running max and sum per row
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
   __shared__ int64_t plan_W;
@@ -355,7 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
       mbar_init(&bar_p[t], kBM);
       mbar_init(&bar_o[t], 1);
       mbar_init(&bar_of[t], kBM);
+      mbar_init(&bar_wg[t], kBM);
     }
+    mbar_init(&bar_ml, kBM);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -421,9 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
   uint8_t* sV = smem + S::kV;
   const int G = p.G;
 
-  if (has_work && warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (has_work && (warp == 0 || warp == 2)) {
+    // ------------------------------------------------------------ TMA producers
+    // warp 0 loads Q and the K stages, warp 2 the V stages: a V stage waits for the
+    // PVs of the stage it replaces, which must not hold back later K stages
     setmaxnreg_dec<kRegsControl>();
+    const bool is_k = warp == 0;
     if (elect_one_sync()) {
       ItemIter it;
       iter_init(it, pv, cta);
@@ -432,15 +438,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
       const int qrows_per_tile = p.q_box_nodes * G;
       bool ok = true;
       while (ok && iter_next(it, pv, cta, item)) {
-        // Q of the previous item is free once its last QK^T has completed
-        if (n_item > 0) ok = mbar_wait(&bar_qe, (n_item - 1) & 1u, &abort_sh);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bar_q, (uint32_t)(item.nt * S::kDBlocks * qrows_per_tile * 128));
-        const int node0 = item.mp * kNT * (kBM / G);
-        for (int t = 0; t < item.nt; ++t)
-          for (int db = 0; db < S::kDBlocks; ++db)
-            tma_load_4d(sQ + t * S::kQTile + db * (kBM * 128), &p.tmQ, &bar_q, db * 64, item.g * G,
-                        node0 + t * (kBM / G), item.b);
+        if (is_k) {
+          // Q of the previous item is free once its last QK^T has completed
+          if (n_item > 0) ok = mbar_wait(&bar_qe, (n_item - 1) & 1u, &abort_sh);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bar_q, (uint32_t)(item.nt * S::kDBlocks * qrows_per_tile * 128));
+          const int node0 = item.mp * kNT * (kBM / G);
+          for (int t = 0; t < item.nt; ++t)
+            for (int db = 0; db < S::kDBlocks; ++db)
+              tma_load_4d(sQ + t * S::kQTile + db * (kBM * 128), &p.tmQ, &bar_q, db * 64, item.g * G,
+                          node0 + t * (kBM / G), item.b);
+        }
         const int L = p.prefix_len[item.b], N = p.n_nodes[item.b];
         const int32_t* pt = p.page_table + (int64_t)item.b * p.max_pages;
         for (int tile = item.tile_begin; tile < item.tile_end && ok; ++tile, ++kv_it) {
@@ -454,20 +462,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
           for (int pg = 0; pg < kPagesPerTile; ++pg) pages[pg] = pg < npg ? pt[key0 / kPageSize + pg] : 0;
           // an out-of-range page id reads the TMA fill value (zeros); the request is
           // reported and zero-filled at exit
-          ok = mbar_wait(&bar_ke[s], ph ^ 1u, &abort_sh);
+          uint64_t* empty = is_k ? &bar_ke[s] : &bar_ve[s];
+          uint64_t* full = is_k ? &bar_kf[s] : &bar_vf[s];
+          uint8_t* dst = (is_k ? sK : sV) + s * S::kKVTile;
+          const CUtensorMap* map = is_k ? &p.tmK : &p.tmV;
+          ok = mbar_wait(empty, ph ^ 1u, &abort_sh);
           if (!ok) break;
-          mbar_arrive_expect_tx(&bar_kf[s], bytes);
+          mbar_arrive_expect_tx(full, bytes);
           for (int pg = 0; pg < npg; ++pg)
             for (int db = 0; db < S::kDBlocks; ++db)
-              tma_load_4d(sK + s * S::kKVTile + db * (kBN * 128) + pg * (kPageSize * 128), &p.tmK, &bar_kf[s],
-                          db * 64, 0, item.g, pages[pg]);
-          ok = mbar_wait(&bar_ve[s], ph ^ 1u, &abort_sh);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&bar_vf[s], bytes);
-          for (int pg = 0; pg < npg; ++pg)
-            for (int db = 0; db < S::kDBlocks; ++db)
-              tma_load_4d(sV + s * S::kKVTile + db * (kBN * 128) + pg * (kPageSize * 128), &p.tmV, &bar_vf[s],
-                          db * 64, 0, item.g, pages[pg]);
+              tma_load_4d(dst + db * (kBN * 128) + pg * (kPageSize * 128), map, full, db * 64, 0, item.g, pages[pg]);
         }
         ++n_item;
       }
@@ -479,82 +483,115 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
     if (elect_one_sync()) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
-      auto issue_qk = [&](int t, int s) {
+      // Descriptors of the operand bases; an operand offset is added to the start
+      // address field (bytes / 16), so each MMA costs one add and the issue keeps
+      // pace with the tensor pipe.
+      const uint64_t dq0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(smem_u32(sV), kBN * 128, 1024);
+      // S_t = Q_qt K^T for the K stage in slot s (128 keys)
+      auto issue_qk = [&](int t, int qt, int s) {
         const uint32_t d = tmem + t * 128;
+        const uint64_t a = dq0 + (uint64_t)((qt * S::kQTile) >> 4);
+        const uint64_t b = dk0 + (uint64_t)((s * S::kKVTile) >> 4);
 #pragma unroll
         for (int db = 0; db < S::kDBlocks; ++db)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = sdesc_sw128(smem_u32(sQ + t * S::kQTile + db * (kBM * 128) + kk * 32), 16, 1024);
-            const uint64_t bd = sdesc_sw128(smem_u32(sK + s * S::kKVTile + db * (kBN * 128) + kk * 32), 16, 1024);
-            mma_ss(d, a, bd, idesc_qk, (db | kk) != 0);
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(d, a + (uint64_t)((db * (kBM * 128) + kk * 32) >> 4),
+                   b + (uint64_t)((db * (kBN * 128) + kk * 32) >> 4), idesc_qk, (db | kk) != 0);
       };
+      // O_t (+)= P_t V   (P_t is packed bf16 over the S_t columns)
       auto issue_pv = [&](int t, int s, bool acc) {
         const uint32_t d = tmem + 256 + t * D;
+        const uint64_t b = dv0 + (uint64_t)((s * S::kKVTile) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t bd = sdesc_sw128(smem_u32(sV + s * S::kKVTile + kk * 2048), kBN * 128, 1024);
-          mma_ts(d, tmem + t * 128 + kk * 8, bd, idesc_pv, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(d, tmem + t * 128 + kk * 8, b + (uint64_t)((kk * 2048) >> 4), idesc_pv, (acc || kk > 0) ? 1u : 0u);
       };
       ItemIter it;
       iter_init(it, pv, cta);
       Item item;
       uint32_t kv_it = 0, n_item = 0;
       uint32_t ph_p[kNT] = {0, 0};
-      uint32_t uses[kNT] = {0, 0};  // items that used M tile t so far
+      uint32_t uses[kNT] = {0, 0};  // items that used accumulator t so far
       bool ok = true;
       while (ok && iter_next(it, pv, cta, item)) {
-        ok = mbar_wait(&bar_q, n_item & 1u, &abort_sh);
         const int n_tiles = item.tile_end - item.tile_begin;
-        const int s0 = kv_it % kStages;
-        ok = ok && mbar_wait(&bar_kf[s0], (kv_it / kStages) & 1u, &abort_sh);
-        tc_fence_after();
-        if (!ok) break;
-        for (int t = 0; t < item.nt; ++t) {
-          issue_qk(t, s0);
+        // one active M tile over several KV stages: the two softmax warpgroups take
+        // alternate stages, each with its own S and O (combined in the epilogue)
+        const bool dual = item.nt == 1 && n_tiles >= 2;
+        const int n_wg = dual ? 2 : item.nt;
+        const int nu0 = dual ? (n_tiles + 1) / 2 : n_tiles;             // stages of warpgroup 0
+        const int nu1 = dual ? n_tiles / 2 : (item.nt == 2 ? n_tiles : 0);  // stages of warpgroup 1
+        const int per_stage = dual ? 1 : item.nt;  // warpgroups reading one stage
+        int kf_next = 0, vf_next = 0;              // next stage whose K / V arrival is awaited
+        int qk_cnt = 0, pv_cnt = 0;                // warpgroups done with the oldest unreleased stage
+        int qk_rel = 0, pv_rel = 0;                // oldest unreleased K / V stage
+        int qk_left = nu0 + nu1;
+        auto slot = [&](int j) { return (int)((kv_it + j) % kStages); };
+        auto sph = [&](int j) { return ((kv_it + j) / kStages) & 1u; };
+        auto need_k = [&](int j) {
+          while (ok && kf_next <= j) {
+            ok = mbar_wait(&bar_kf[slot(kf_next)], sph(kf_next), &abort_sh);
+            ++kf_next;
+          }
+          tc_fence_after();
+        };
+        auto need_v = [&](int j) {
+          while (ok && vf_next <= j) {
+            ok = mbar_wait(&bar_vf[slot(vf_next)], sph(vf_next), &abort_sh);
+            ++vf_next;
+          }
+          tc_fence_after();
+        };
+        // stages are read in order (warpgroup 0 first in each round), so the stage
+        // to release is always the oldest unreleased one
+        auto qk = [&](int t, int k) {
+          const int j = dual ? 2 * k + t : k;
+          need_k(j);
+          if (!ok) return;
+          issue_qk(t, dual ? 0 : t, slot(j));
           mma_commit(&bar_s[t]);
-        }
-        mma_commit(&bar_ke[s0]);
-        if (n_tiles == 1) mma_commit(&bar_qe);
-        for (int j = 0; j < n_tiles && ok; ++j) {
-          const uint32_t k = kv_it + j;
-          const int s = k % kStages;
-          ok = mbar_wait(&bar_vf[s], (k / kStages) & 1u, &abort_sh);
-          const bool has_next = j + 1 < n_tiles;
-          const int s1 = (k + 1) % kStages;
-          if (ok && has_next) ok = mbar_wait(&bar_kf[s1], ((k + 1) / kStages) & 1u, &abort_sh);
-          for (int t = 0; t < item.nt && ok; ++t) {
+          if (++qk_cnt == per_stage) {
+            mma_commit(&bar_ke[slot(qk_rel)]);
+            ++qk_rel;
+            qk_cnt = 0;
+          }
+          if (--qk_left == 0) mma_commit(&bar_qe);  // the item's last QK^T is issued
+        };
+        ok = mbar_wait(&bar_q, n_item & 1u, &abort_sh);
+        if (ok) qk(0, 0);
+        if (ok && nu1 > 0) qk(1, 0);
+        for (int k = 0; k < nu0 && ok; ++k) {
+          for (int t = 0; t < n_wg && ok; ++t) {
+            const int nu = t == 0 ? nu0 : nu1;
+            if (k >= nu) continue;
+            const int j = dual ? 2 * k + t : k;
+            need_v(j);
             // O_t of the previous item must have been read by its epilogue
-            if (j == 0 && uses[t] > 0) ok = mbar_wait(&bar_of[t], (uses[t] - 1) & 1u, &abort_sh);
+            if (ok && k == 0 && uses[t] > 0) ok = mbar_wait(&bar_of[t], (uses[t] - 1) & 1u, &abort_sh);
             ok = ok && mbar_wait(&bar_p[t], ph_p[t], &abort_sh);
             ph_p[t] ^= 1u;
             tc_fence_after();
             if (!ok) break;
-            issue_pv(t, s, j > 0);
-            if (has_next) {
-              issue_qk(t, s1);
-              mma_commit(&bar_s[t]);
-            } else {
-              mma_commit(&bar_o[t]);
+            issue_pv(t, slot(j), k > 0);
+            if (++pv_cnt == per_stage) {
+              mma_commit(&bar_ve[slot(pv_rel)]);
+              ++pv_rel;
+              pv_cnt = 0;
             }
-          }
-          if (!ok) break;
-          mma_commit(&bar_ve[s]);
-          if (has_next) {
-            mma_commit(&bar_ke[s1]);
-            if (j + 2 == n_tiles) mma_commit(&bar_qe);  // the item's last QK^T is issued
+            // S_t of the next stage overwrites P_t after the PV above has read it
+            if (k + 1 < nu) qk(t, k + 1);
+            else mma_commit(&bar_o[t]);
           }
         }
-        for (int t = 0; t < item.nt; ++t) ++uses[t];
+        for (int t = 0; t < n_wg; ++t) ++uses[t];
         kv_it += n_tiles;
         ++n_item;
       }
     }
     __syncwarp();
-  } else if (has_work && warp == 2) {
-    setmaxnreg_dec<kRegsControl>();  // TMEM owner: idle until the exit
   } else if (has_work && warp == 3) {
     // ------------------------------------------------------------ page-table check
     setmaxnreg_dec<kRegsControl>();
@@ -581,39 +618,49 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
     const uint32_t tO = tmem + lane_base + 256 + t * D;
+    const uint32_t tO1 = tmem + lane_base + 256 + D;     // accumulator 1 (read by warpgroup 0 in dual mode)
     const float sl2 = p.scale_log2;
     ItemIter it;
     iter_init(it, pv, cta);
     Item item;
     uint32_t kv_it = 0;
-    uint32_t ph_s = 0, ph_o = 0;
+    uint32_t ph_s = 0, ph_o = 0, ph_ml = 0, ph_wg = 0;
     bool ok = true;
+    // warpgroup-wide barrier with a bounded wait
+    auto wg_sync = [&]() -> bool {
+      mbar_arrive(&bar_wg[t]);
+      const bool k = warp_wait(&bar_wg[t], ph_wg, &abort_sh);
+      ph_wg ^= 1u;
+      return k;
+    };
     while (ok && iter_next(it, pv, cta, item)) {
       const int n_tiles = item.tile_end - item.tile_begin;
-      if (t >= item.nt) {
+      const bool dual = item.nt == 1 && n_tiles >= 2;
+      if (!dual && t >= item.nt) {
         kv_it += n_tiles;
         continue;
       }
+      const int n_units = dual ? (n_tiles - t + 1) / 2 : n_tiles;  // stages of this warpgroup
       if (tid == 128) last_b_sh = item.b;
       const int L = p.prefix_len[item.b];
       const int N = p.n_nodes[item.b];
-      const int mrow = (item.mp * kNT + t) * kBM + r;
+      const int mtile = dual ? 0 : t;                     // M tile whose rows this warpgroup holds
+      const int mrow = (item.mp * kNT + mtile) * kBM + r;
       const int node = mrow / G;
       const int hh = mrow - node * G;
       const bool row_ok = node < N;
       const uint64_t anc = row_ok ? p.anc_mask[(int64_t)item.b * p.n_max + node] : 0ull;
       float m_run = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < n_tiles; ++j) {
+      for (int k = 0; k < n_units; ++k) {
+        const int j = dual ? 2 * k + t : k;                       // stage of this unit
         ok = warp_wait(&bar_s[t], ph_s, &abort_sh);
         ph_s ^= 1u;
         tc_fence_after();
         if (!ok) break;
-        const int key0 = (item.tile_begin + j) * kBN;
-        const bool masked = key0 + kBN > L;
-        // the whole 128-wide S row of this thread in registers (one TMEM load)
+        const int key0 = (item.tile_begin + j) * kBN;             // first key of the stage
         uint32_t v[kBN];
         tmem_ld128(tS, v);
-        if (masked) {
+        if (key0 + kBN > L) {
 #pragma unroll
           for (int c0 = 0; c0 < kBN; c0 += 32) {
             const uint32_t vis = visible32(key0 + c0, L, anc);
@@ -637,8 +684,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
           m_run = m_new;
         }
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        // a tile that runs past the request's data: clear the V rows past it
-        if (t == 0 && key0 + kBN > L + N) {
+        // a stage that runs past the request's data: clear its V rows past the data
+        // (before the first PV that reads this stage)
+        if ((dual || t == 0) && key0 + kBN > L + N) {
           const uint32_t kk = kv_it + j;
           const int s = kk % kStages;
           ok = warp_wait(&bar_vf[s], (kk / kStages) & 1u, &abort_sh);
@@ -663,21 +711,20 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
           const float e0 = ex2_approx(fmaf(__uint_as_float(v[c]), sl2, -m_use));
           const float e1 = ex2_approx(fmaf(__uint_as_float(v[c + 1]), sl2, -m_use));
           ps[(c >> 1) & 3] += e0 + e1;
-          v[c >> 1] = pack_bf16x2(e0, e1);
+          v[c >> 1] = pack_bf16x2_pos(e0, e1);
         }
         tmem_st64(tS, v);
         const float rs = (ps[0] + ps[1]) + (ps[2] + ps[3]);
-        if (__any_sync(0xffffffffu, grow && j > 0)) {
-          // rescale O (the PV of the previous tile completed before S of this tile;
-          // the next PV is issued only after this thread arrives on bar_p)
+        if (__any_sync(0xffffffffu, grow && k > 0)) {
+          // rescale O (the PV of this accumulator's previous stage completed before the
+          // S of this stage became ready; the next PV waits for this thread's arrival)
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t o[32];
             tmem_ld32(tO + c0, o);
 #pragma unroll
             for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st16(tO + c0, o);
-            tmem_st16(tO + c0 + 16, o + 16);
+            tmem_st32(tO + c0, o);
           }
         }
         l_run += rs;
@@ -692,47 +739,78 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
       ph_o ^= 1u;
       tc_fence_after();
       if (!ok) break;
-      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-      const float lse_v = l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+      float m_c = m_run, l_c = l_run, a0 = 1.f, a1 = 0.f;
+      if (dual) {
+        if (t == 1) {
+          // hand the row state to warpgroup 0, which combines both accumulators
+          ml_sh[0][r] = m_run;
+          ml_sh[1][r] = l_run;
+          tc_fence_before();
+          mbar_arrive(&bar_ml);
+          continue;
+        }
+        ok = warp_wait(&bar_ml, ph_ml, &abort_sh);
+        ph_ml ^= 1u;
+        tc_fence_after();
+        if (!ok) break;
+        const float m1 = ml_sh[0][r], l1 = ml_sh[1][r];
+        m_c = fmaxf(m_run, m1);
+        const float mu = (m_c == -INFINITY) ? 0.f : m_c;
+        a0 = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mu);
+        a1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - mu);
+        l_c = l_run * a0 + l1 * a1;
+      }
+      const float inv_l = l_c > 0.f ? 1.f / l_c : 0.f;
+      const float lse_v = l_c > 0.f ? (m_c + __log2f(l_c)) * 0.69314718055994531f : -INFINITY;
       const int h = item.g * G + hh;
       const int64_t orow_idx = ((int64_t)item.b * p.n_max + node) * p.Hq + h;
       const bool direct = item.n_splits == 1;
-      const int prow = t * kBM + r;
+      const int prow = mtile * kBM + r;
       float4* pslot = reinterpret_cast<float4*>(p.part_o) + (int64_t)item.my_slot * (D / 4) * kRowsPerSlot + prow;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t o[32];
         tmem_ld32(tO + c0, o);
+        float y[32];
+        if (dual) {
+          uint32_t o1[32];
+          tmem_ld32(tO1 + c0, o1);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) y[c] = (__uint_as_float(o[c]) * a0 + __uint_as_float(o1[c]) * a1) * inv_l;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) y[c] = __uint_as_float(o[c]) * inv_l;
+        }
         if (row_ok) {
           if (direct) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int c = 0; c < 32; c += 2)
-              pk[c >> 1] = pack_bf16x2(__uint_as_float(o[c]) * inv_l, __uint_as_float(o[c + 1]) * inv_l);
             uint4* dst = reinterpret_cast<uint4*>(p.out + orow_idx * D + c0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pack_bf16x2(y[8 * q], y[8 * q + 1]), pack_bf16x2(y[8 * q + 2], y[8 * q + 3]),
+                                  pack_bf16x2(y[8 * q + 4], y[8 * q + 5]), pack_bf16x2(y[8 * q + 6], y[8 * q + 7]));
           } else {
             float4* dst = pslot + (c0 / 4) * kRowsPerSlot;
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-              dst[q * kRowsPerSlot] = make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
-                                   __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+              dst[q * kRowsPerSlot] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(&bar_of[t]);  // O_t may be overwritten by the next item
+      mbar_arrive(&bar_of[t]);  // the accumulator(s) may be overwritten by the next item
+      if (dual) mbar_arrive(&bar_of[1]);
       if (direct) {
         if (row_ok && p.lse) p.lse[orow_idx] = lse_v;
       } else {
         if (row_ok) p.part_lse[(int64_t)item.my_slot * kRowsPerSlot + prow] = lse_v;
         // ticket: the last split of this (group, M tile) to arrive merges every partial
         __threadfence();
-        named_bar_sync(1 + t, kBM);
-        const int tick_idx = (((item.b * p.Hkv + item.g) * p.mp_max + item.mp) * kNT) + t;
+        ok = wg_sync();
+        if (!ok) break;
+        const int tick_idx = (((item.b * p.Hkv + item.g) * p.mp_max + item.mp) * kNT) + mtile;
         if (r == 0) ticket_sh[t] = atomicAdd(p.ws_tickets + tick_idx, 1);
-        named_bar_sync(1 + t, kBM);
+        ok = wg_sync();
+        if (!ok) break;
         if (ticket_sh[t] == item.n_splits - 1) {
           __threadfence();
           if (row_ok) merge_row<D>(p, item, prow, orow_idx);
