@@ -258,62 +258,97 @@ __device__ __forceinline__ int request_shape_bits(int L, int N, int n_max, int m
 __device__ __forceinline__ int split_slot(const Item& it, int sp) { return sp == 0 ? it.slot0 : 2 * (it.k0 + sp); }
 
 // The last split of a (group, M tile) combines every split's normalised
-// partial row by its log-sum-exp weight: out = sum_s w_s O_s / sum_s w_s,
-// w_s = exp(lse_s - max lse), lse = max lse + ln sum_s w_s.
-template <int D>
-__device__ void merge_row(const AttnParams& p, const Item& it, int prow, int64_t orow_idx) {
-  float m = -INFINITY;
-  for (int sp = 0; sp < it.n_splits; ++sp)
-    m = fmaxf(m, __ldcg(p.part_lse + (int64_t)split_slot(it, sp) * kRowsPerSlot + prow));
-  float wsum = 0.f;
-  for (int sp = 0; sp < it.n_splits; ++sp) {
-    const float ls = __ldcg(p.part_lse + (int64_t)split_slot(it, sp) * kRowsPerSlot + prow);
-    wsum += (ls == -INFINITY) ? 0.f : ex2_approx((ls - m) * kLog2e);
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  uint4* dst = reinterpret_cast<uint4*>(p.out + orow_idx * D);
-#pragma unroll 1
-  for (int c0 = 0; c0 < D; c0 += 32) {
-    float acc[32];
+// partial rows by their log-sum-exp weights: out = sum_s w_s O_s with
+// w_s = exp(lse_s - m) / sum_s' exp(lse_s' - m), m = max_s lse_s, and
+// lse = m + ln sum_s exp(lse_s - m).  The work items are (row, column slice)
+// pairs spread over the whole warpgroup, consecutive threads on consecutive
+// rows so the partial reads coalesce; one item loads the log-sum-exps and the
+// slices of up to kMB splits in a single round trip (kMB * kF float4 per thread
+// in flight), and needs a separate pass for the weights only above kMB splits.
+template <int D, int kMB, int kF>
+__device__ void merge_items(const AttnParams& p, const Item& it, int mtile, int n_rows, int r) {
+  constexpr int kSlices = D / (4 * kF);
+  const int G = p.G;
+  const int ns = it.n_splits;
+  const int n_items = n_rows * kSlices;
+  for (int w = r; w < n_items; w += kBM) {
+    const int row = w % n_rows;
+    const int sl = w / n_rows;
+    const int prow = mtile * kBM + row;
+    const int mrow = (it.mp * kNT + mtile) * kBM + row;
+    const int node = mrow / G;
+    const int64_t orow_idx = ((int64_t)it.b * p.n_max + node) * p.Hq + it.g * G + (mrow - node * G);
+    float m = -INFINITY, wsum = 0.f;
+    if (ns > kMB) {
+      // maximum and weight sum over every split, batch by batch (online)
+      for (int s0 = 0; s0 < ns; s0 += kMB) {
+        float ls[kMB];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) acc[c] = 0.f;
-#pragma unroll 1
-    for (int sp0 = 0; sp0 < it.n_splits; sp0 += 4) {
-      float4 x[4][8];
-      float wv[4];
+        for (int u = 0; u < kMB; ++u)
+          ls[u] = s0 + u < ns ? __ldcg(p.part_lse + (int64_t)split_slot(it, s0 + u) * kRowsPerSlot + prow) : -INFINITY;
+        float mb = m;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        wv[u] = 0.f;
-        if (sp0 + u < it.n_splits) {
-          const int slot = split_slot(it, sp0 + u);
-          const float ls = __ldcg(p.part_lse + (int64_t)slot * kRowsPerSlot + prow);
-          wv[u] = (ls == -INFINITY) ? 0.f : ex2_approx((ls - m) * kLog2e) * inv;
-          const float4* src = reinterpret_cast<const float4*>(p.part_o) +
-                              ((int64_t)slot * (D / 4) + c0 / 4) * kRowsPerSlot + prow;
+        for (int u = 0; u < kMB; ++u) mb = fmaxf(mb, ls[u]);
+        if (mb == -INFINITY) continue;
+        wsum = (m == -INFINITY) ? 0.f : wsum * ex2_approx((m - mb) * kLog2e);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) x[u][q] = __ldcg(src + q * kRowsPerSlot);
+        for (int u = 0; u < kMB; ++u) wsum += (ls[u] == -INFINITY) ? 0.f : ex2_approx((ls[u] - mb) * kLog2e);
+        m = mb;
+      }
+    }
+    float acc[4 * kF];
+#pragma unroll
+    for (int c = 0; c < 4 * kF; ++c) acc[c] = 0.f;
+    for (int s0 = 0; s0 < ns; s0 += kMB) {
+      float ls[kMB];
+      float4 x[kMB][kF];
+#pragma unroll
+      for (int u = 0; u < kMB; ++u) {
+        if (s0 + u < ns) {
+          const int slot = split_slot(it, s0 + u);
+          ls[u] = __ldcg(p.part_lse + (int64_t)slot * kRowsPerSlot + prow);
+          const float4* src =
+              reinterpret_cast<const float4*>(p.part_o) + ((int64_t)slot * (D / 4) + sl * kF) * kRowsPerSlot + prow;
+#pragma unroll
+          for (int q = 0; q < kF; ++q) x[u][q] = __ldcg(src + q * kRowsPerSlot);
         } else {
+          ls[u] = -INFINITY;
 #pragma unroll
-          for (int q = 0; q < 8; ++q) x[u][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int q = 0; q < kF; ++q) x[u][q] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
+      if (ns <= kMB) {  // one batch: the weights come from the values just loaded
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < kMB; ++u) m = fmaxf(m, ls[u]);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          acc[4 * q] += wv[u] * x[u][q].x;
-          acc[4 * q + 1] += wv[u] * x[u][q].y;
-          acc[4 * q + 2] += wv[u] * x[u][q].z;
-          acc[4 * q + 3] += wv[u] * x[u][q].w;
+        for (int u = 0; u < kMB; ++u) wsum += (ls[u] == -INFINITY) ? 0.f : ex2_approx((ls[u] - m) * kLog2e);
+      }
+      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+      for (int u = 0; u < kMB; ++u) {
+        const float wv = (ls[u] == -INFINITY) ? 0.f : ex2_approx((ls[u] - m) * kLog2e) * inv;
+#pragma unroll
+        for (int q = 0; q < kF; ++q) {
+          acc[4 * q] += wv * x[u][q].x;
+          acc[4 * q + 1] += wv * x[u][q].y;
+          acc[4 * q + 2] += wv * x[u][q].z;
+          acc[4 * q + 3] += wv * x[u][q].w;
         }
+      }
     }
+    uint4* dst = reinterpret_cast<uint4*>(p.out + orow_idx * D + sl * (4 * kF));
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      dst[c0 / 8 + q] = make_uint4(pack_bf16x2(acc[8 * q], acc[8 * q + 1]), pack_bf16x2(acc[8 * q + 2], acc[8 * q + 3]),
-                                   pack_bf16x2(acc[8 * q + 4], acc[8 * q + 5]),
-                                   pack_bf16x2(acc[8 * q + 6], acc[8 * q + 7]));
+    for (int q = 0; q < kF / 2; ++q)
+      dst[q] = make_uint4(pack_bf16x2(acc[8 * q], acc[8 * q + 1]), pack_bf16x2(acc[8 * q + 2], acc[8 * q + 3]),
+                          pack_bf16x2(acc[8 * q + 4], acc[8 * q + 5]), pack_bf16x2(acc[8 * q + 6], acc[8 * q + 7]));
+    if (sl == 0 && p.lse) p.lse[orow_idx] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
   }
-  if (p.lse) p.lse[orow_idx] = m + __logf(wsum);
+}
+
+template <int D>
+__device__ __forceinline__ void merge_tile(const AttnParams& p, const Item& it, int mtile, int n_rows, int r) {
+  if (it.n_splits <= 4) merge_items<D, 4, 8>(p, it, mtile, n_rows, r);
+  else merge_items<D, 8, 4>(p, it, mtile, n_rows, r);
 }
 
 template <int D>
@@ -669,12 +704,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
               if (!((vis >> c) & 1u)) v[c0 + c] = __float_as_uint(-INFINITY);
           }
         }
-        // row max as four independent partial maxima
+        // row max as four independent partial maxima of three-input steps
         float pm[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) pm[u] = __uint_as_float(v[u]);
 #pragma unroll
-        for (int c = 4; c < kBN; ++c) pm[c & 3] = fmaxf(pm[c & 3], __uint_as_float(v[c]));
+        for (int c = 4; c < kBN; c += 8)
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            pm[u] = fmax3(pm[u], __uint_as_float(v[c + 2 * u]), __uint_as_float(v[c + 2 * u + 1]));
         const float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
         const float m_new = fmaxf(m_run, mx * sl2);
         const bool grow = m_new > m_run + kRescaleLog2;
@@ -702,18 +740,23 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
           }
           fence_proxy_async_smem();
         }
-        // probabilities 2^(s*scale*log2e - m), packed in place as bf16 pairs
-        float ps[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) ps[u] = 0.f;
+        // probabilities 2^(s*scale*log2e - m), packed in place as bf16 pairs; the
+        // scaling and the row sum run two lanes per instruction
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_use, -m_use);
+        uint64_t ps2[2] = {0ull, 0ull};
 #pragma unroll
         for (int c = 0; c < kBN; c += 2) {
-          const float e0 = ex2_approx(fmaf(__uint_as_float(v[c]), sl2, -m_use));
-          const float e1 = ex2_approx(fmaf(__uint_as_float(v[c + 1]), sl2, -m_use));
-          ps[(c >> 1) & 3] += e0 + e1;
-          v[c >> 1] = pack_bf16x2_pos(e0, e1);
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), sl2x2, negm2), x0, x1);
+          const float e0 = ex2_approx(x0);
+          const float e1 = ex2_approx(x1);
+          ps2[(c >> 1) & 1] = f2_add(ps2[(c >> 1) & 1], f2_pack(e0, e1));
+          v[c >> 1] = pack_bf16x2(e0, e1);
         }
         tmem_st64(tS, v);
+        float ps[4];
+        f2_unpack(ps2[0], ps[0], ps[1]);
+        f2_unpack(ps2[1], ps[2], ps[3]);
         const float rs = (ps[0] + ps[1]) + (ps[2] + ps[3]);
         if (__any_sync(0xffffffffu, grow && k > 0)) {
           // rescale O (the PV of this accumulator's previous stage completed before the
@@ -813,7 +856,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
         if (!ok) break;
         if (ticket_sh[t] == item.n_splits - 1) {
           __threadfence();
-          if (row_ok) merge_row<D>(p, item, prow, orow_idx);
+          const int n_rows = min(kBM, N * G - (item.mp * kNT + mtile) * kBM);  // valid rows of the M tile
+          merge_tile<D>(p, item, mtile, n_rows, r);
           if (r == 0) p.ws_tickets[tick_idx] = 0;  // ready for the next call
         }
       }
