@@ -241,6 +241,7 @@ def main():
             v=v0.unsqueeze(0).repeat(layers, 1, 1, 1, 1).contiguous(),
             q=q0.clone(), target=t0.clone(), draft=d0.clone() if sampling else None,
             ws=tvb.new_attn_workspace(B, n_max, Hq, Hkv, D, dev),
+            aws=tvb.new_accept_workspace(B, n_max, V, dev),
             anc=torch.empty((B, n_max), dtype=torch.int64, device=dev),
             depth=torch.empty((B, n_max), dtype=torch.int32, device=dev),
             status=torch.empty((B,), dtype=torch.int32, device=dev),
@@ -264,7 +265,8 @@ def main():
     def accept_commit_call(cp):
         tvb.tree_accept(cp["target"], cp["draft"], shared["tokens"], shared["parents"], shared["n_nodes"],
                         cp["anc"], cp["depth"], w.temperature, shared["u_accept"] if sampling else None,
-                        shared["u_sample"] if sampling else None, cp["status"], outputs=cp["acc"])
+                        shared["u_sample"] if sampling else None, cp["status"], outputs=cp["acc"],
+                        workspace=cp["aws"])
         tvb.kv_commit_path(cp["k"], cp["v"], shared["page_table"], shared["prefix_len"], shared["n_nodes"],
                            cp["acc"][0], cp["acc"][1], cp["status"], outputs=cp["com"])
 
@@ -360,7 +362,7 @@ def main():
                                  lse=cpk["lse"], workspace=cpk["ws"])
             acc = tvb.tree_accept(dev_in["target"], dev_in.get("draft"), dev_in["tokens"], dev_in["parents"],
                                   dev_in["n_nodes"], anc, depth, w.temperature, dev_in.get("u_accept"),
-                                  dev_in.get("u_sample"), st, outputs=cpk["acc"])
+                                  dev_in.get("u_sample"), st, outputs=cpk["acc"], workspace=cpk["aws"])
             com = tvb.kv_commit_path(cpk["k"], cpk["v"], dev_in["page_table"], dev_in["prefix_len"],
                                      dev_in["n_nodes"], acc[0], acc[1], st, outputs=cpk["com"])
             for hdst, dsrc in zip(res_host, [acc[0], acc[1], acc[2], com[1], com[0]]):

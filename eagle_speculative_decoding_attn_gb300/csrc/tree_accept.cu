@@ -515,9 +515,212 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
   ex.sync();  // no CTA exits while others may still read its shared memory
 }
 
+// ---------------------------------------------------------------- greedy, one pass
+// When the logits of every node are small enough to read outright, the greedy
+// walk needs no sequential row reads: CTA (slice, node, request) reduces one
+// vocabulary slice of one node's row to a partial argmax, and the last CTA of
+// a request to finish (arrival counter) takes every node's argmax and resolves
+// the walk in shared memory.  The result is the same deepest fully hit node as
+// the level walk above; ancestor sets come from pointer jumping over the
+// parent links.
+constexpr int kArgThreads = 256;
+constexpr int kArgPerThread = 32;                        // floats per thread and slice
+constexpr int kArgSlice = kArgThreads * kArgPerThread;   // 8192
+constexpr int64_t kOnePassMaxBytes = 64ll << 20;         // logits read by the one-pass walk
+
+struct OnePassParams {
+  const float* target;
+  const int32_t* tokens;
+  const int32_t* parents;
+  const int32_t* n_nodes;
+  int n_max, V, n_slices;
+  float2* part;        // [B][n_max][n_slices]: (value, index bits) of each slice's argmax
+  int32_t* tickets;    // [B] arrivals of this call (zero between calls)
+  int32_t* accept_len;
+  int32_t* path_nodes;
+  int32_t* out_tokens;
+  int32_t* status;
+};
+
+__device__ void argmax_block256(float& v, int& i, float* wv, int* wi) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+    argmax_take(v, i, v2, i2);
+  }
+  if (lane == 0) {
+    wv[warp] = v;
+    wi[warp] = i;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    for (int w = 1; w < kArgThreads / 32; ++w) argmax_take(v, i, wv[w], wi[w]);
+}
+
+__global__ void __launch_bounds__(kArgThreads) greedy_onepass_kernel(const OnePassParams p) {
+  __shared__ float wv[kArgThreads / 32];
+  __shared__ int wi[kArgThreads / 32];
+  __shared__ int last_sh;
+  __shared__ int par[kMaxNodes], tok[kMaxNodes], am[kMaxNodes], jmp[kMaxNodes];
+  __shared__ unsigned long long anc[kMaxNodes];
+  __shared__ unsigned long long hit_sh[2], key_sh[2];
+  const int sl = blockIdx.x, node = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int n_max = p.n_max, V = p.V;
+  const int N = p.n_nodes[b];
+  const bool req_ok = p.status[b] == 0 && N >= 1 && N <= n_max;
+
+  // ---- this slice's partial argmax (lowest index on ties)
+  float bv = -FLT_MAX;
+  int bi = INT_MAX;
+  if (req_ok && node < N) {
+    const int lo = sl * kArgSlice;
+    const int hi = min(V, lo + kArgSlice);
+    const float* row = p.target + ((int64_t)b * n_max + node) * V;
+    if ((V & 3) == 0) {
+      const float4* r4 = reinterpret_cast<const float4*>(row);
+      float4 x[kArgPerThread / 4];
+#pragma unroll
+      for (int u = 0; u < kArgPerThread / 4; ++u) {
+        const int j = lo / 4 + u * kArgThreads + tid;
+        x[u] = j < hi / 4 ? __ldcs(r4 + j) : make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
+      }
+#pragma unroll
+      for (int u = 0; u < kArgPerThread / 4; ++u) {
+        const int base = 4 * (lo / 4 + u * kArgThreads + tid);
+        argmax_take(bv, bi, x[u].x, base);
+        argmax_take(bv, bi, x[u].y, base + 1);
+        argmax_take(bv, bi, x[u].z, base + 2);
+        argmax_take(bv, bi, x[u].w, base + 3);
+      }
+    } else {
+      for (int j = lo + tid; j < hi; j += kArgThreads) argmax_take(bv, bi, __ldcs(row + j), j);
+    }
+  }
+  argmax_block256(bv, bi, wv, wi);
+  if (tid == 0) {
+    p.part[((int64_t)b * n_max + node) * p.n_slices + sl] = make_float2(bv, __int_as_float(bi));
+    __threadfence();
+    last_sh = atomicAdd(p.tickets + b, 1) == n_max * p.n_slices - 1;
+  }
+  __syncthreads();
+  if (!last_sh) return;
+  __threadfence();
+
+  // ---- the last CTA of request b: validate, then resolve the walk
+  int bad = p.status[b] != 0 ? -1 : 0;
+  if (!bad && (N < 1 || N > n_max)) bad = TV_DEV_BAD_TREE;
+  if (!bad) {
+    bool sbad = false, tbad = false;
+    if (tid < N) {
+      const int pi = p.parents[(int64_t)b * n_max + tid];
+      const int ti = p.tokens[(int64_t)b * n_max + tid];
+      par[tid] = pi;
+      tok[tid] = ti;
+      sbad = tid == 0 ? pi != -1 : (pi < 0 || pi >= tid);
+      tbad = tid >= 1 && (ti < 0 || ti >= V);
+      // this node's argmax over the slices
+      const float2* pp = p.part + ((int64_t)b * n_max + tid) * p.n_slices;
+      float v = -FLT_MAX;
+      int i = INT_MAX;
+      for (int s = 0; s < p.n_slices; ++s) {
+        const float2 x = __ldcg(pp + s);
+        argmax_take(v, i, x.x, __float_as_int(x.y));
+      }
+      am[tid] = i;
+    }
+    const int any_s = __syncthreads_or(sbad);
+    const int any_t = __syncthreads_or(tbad);
+    bad = any_s ? TV_DEV_BAD_TREE : (any_t ? TV_DEV_BAD_TOKEN : 0);
+  }
+  int32_t* pn = p.path_nodes + (int64_t)b * n_max;
+  int32_t* ot = p.out_tokens + (int64_t)b * (n_max + 1);
+  if (bad) {
+    for (int k = tid; k < n_max; k += kArgThreads) pn[k] = -1;
+    for (int k = tid; k <= n_max; k += kArgThreads) ot[k] = -1;
+    if (tid == 0) {
+      p.accept_len[b] = 0;
+      if (bad > 0) atomicOr(p.status + b, bad);
+      p.tickets[b] = 0;
+    }
+    return;
+  }
+  // ancestor-or-self sets by pointer jumping: after round r a set spans 2^(r+1) links
+  if (tid < N) {
+    const int pi = tid == 0 ? 0 : par[tid];
+    anc[tid] = (1ull << tid) | (1ull << pi);
+    jmp[tid] = pi;
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int r = 0; r < 6; ++r) {
+    unsigned long long a = 0;
+    int j = 0;
+    if (tid < N) {
+      a = anc[tid] | anc[jmp[tid]];
+      j = jmp[jmp[tid]];
+    }
+    __syncthreads();
+    if (tid < N) {
+      anc[tid] = a;
+      jmp[tid] = j;
+    }
+    __syncthreads();
+  }
+  // node i hits iff its token is its parent's argmax; accepted iff every
+  // non-root node of its root path hits; the result is the deepest accepted
+  // node, lowest index on ties
+  const bool hit = tid >= 1 && tid < N && tok[tid] == am[par[tid]];
+  const unsigned hb = __ballot_sync(0xffffffffu, hit);
+  if (tid < 64 && (tid & 31) == 0) hit_sh[tid >> 5] = hb;
+  __syncthreads();
+  const unsigned long long hits = hit_sh[0] | (hit_sh[1] << 32) | 1ull;
+  unsigned long long key = 0;
+  if (tid < N && (anc[tid] & ~hits) == 0)
+    key = ((unsigned long long)__popcll(anc[tid]) << 8) | (unsigned long long)(255 - tid);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const unsigned long long k2 = __shfl_xor_sync(0xffffffffu, key, o);
+    key = k2 > key ? k2 : key;
+  }
+  if (tid < 64 && (tid & 31) == 0) key_sh[tid >> 5] = key;
+  __syncthreads();
+  const unsigned long long kb = key_sh[0] > key_sh[1] ? key_sh[0] : key_sh[1];
+  const int best = 255 - (int)(kb & 255);
+  const unsigned long long path = anc[best];
+  const int a = __popcll(path) - 1;
+  // the k-th set bit of the path set is the k-th node of the path (ancestors sort
+  // root-first by index)
+  auto path_node = [&](int k) {
+    unsigned long long m = path;
+    for (int q = 0; q < k; ++q) m &= m - 1;
+    return __ffsll((long long)m) - 1;
+  };
+  for (int k = tid; k < n_max; k += kArgThreads) pn[k] = k <= a ? path_node(k) : -1;
+  for (int k = tid; k <= n_max; k += kArgThreads) ot[k] = k < a ? tok[path_node(k + 1)] : (k == a ? am[best] : -1);
+  if (tid == 0) {
+    p.accept_len[b] = a;
+    p.tickets[b] = 0;  // ready for the next call
+  }
+}
+
 }  // namespace tv
 
-extern "C" size_t tv_tree_accept_workspace(int, int, int) { return 0; }
+namespace {
+int onepass_slices(int V) { return (V + tv::kArgSlice - 1) / tv::kArgSlice; }
+bool onepass_eligible(int B, int n_max, int V) { return (int64_t)B * n_max * V * 4 <= tv::kOnePassMaxBytes; }
+size_t onepass_ws_bytes(int B, int n_max, int V) {
+  const size_t part = (size_t)B * n_max * onepass_slices(V) * sizeof(float2);
+  return ((part + 255) & ~size_t(255)) + (size_t)B * sizeof(int32_t);
+}
+}  // namespace
+
+extern "C" size_t tv_tree_accept_workspace(int B, int n_max, int V) {
+  if (B <= 0 || n_max <= 0 || V <= 0 || !onepass_eligible(B, n_max, V)) return 0;
+  return onepass_ws_bytes(B, n_max, V);
+}
 
 extern "C" int tv_tree_accept(const float* target_logits, const float* draft_logits, const int32_t* tokens,
                               const int32_t* parents, const int32_t* n_nodes, const uint64_t* anc_mask,
@@ -527,8 +730,6 @@ extern "C" int tv_tree_accept(const float* target_logits, const float* draft_log
                               int32_t* status, void* stream) {
   (void)anc_mask;
   (void)depth;
-  (void)ws;
-  (void)ws_bytes;
   tv::clear_error();
   const bool sampling = temperature > 0.f;
   TV_REQUIRE(target_logits && tokens && parents && n_nodes && accept_len && path_nodes && out_tokens && status,
@@ -547,6 +748,30 @@ extern "C" int tv_tree_accept(const float* target_logits, const float* draft_log
   TV_REQUIRE(!sampling || chunk <= tv::kMaxChunk, TV_ERR_UNSUPPORTED,
              "tv_tree_accept: V = %d too large for on-chip sampling (max %d)", V, tv::kMaxChunk * tv::kCL);
   if (B == 0) return TV_OK;
+  if (!sampling && onepass_eligible(B, n_max, V)) {
+    const size_t need = onepass_ws_bytes(B, n_max, V);
+    TV_REQUIRE(ws != nullptr && ws_bytes >= need && tv::aligned16(ws), TV_ERR_INVALID_ARG,
+               "tv_tree_accept: workspace of %zu bytes (16-byte aligned, zero-filled once) required, got %zu",
+               need, ws ? ws_bytes : (size_t)0);
+    TV_REQUIRE(B <= 65535, TV_ERR_UNSUPPORTED, "tv_tree_accept: B = %d above 65535", B);
+    tv::OnePassParams q;
+    q.target = target_logits;
+    q.tokens = tokens;
+    q.parents = parents;
+    q.n_nodes = n_nodes;
+    q.n_max = n_max;
+    q.V = V;
+    q.n_slices = onepass_slices(V);
+    q.part = reinterpret_cast<float2*>(ws);
+    q.tickets = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + (need - (size_t)B * sizeof(int32_t)));
+    q.accept_len = accept_len;
+    q.path_nodes = path_nodes;
+    q.out_tokens = out_tokens;
+    q.status = status;
+    tv::greedy_onepass_kernel<<<dim3(q.n_slices, n_max, B), tv::kArgThreads, 0, tv::as_stream(stream)>>>(q);
+    TV_CUDA_CHECK(cudaGetLastError());
+    return TV_OK;
+  }
   TV_REQUIRE((int64_t)B * tv::kCL < (1ll << 31), TV_ERR_UNSUPPORTED, "tv_tree_accept: B too large");
   tv::AcceptParams p;
   p.target = target_logits;

@@ -163,14 +163,27 @@ def tree_verify_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     return out, lse
 
 
+def tree_accept_workspace_bytes(B, n_max, V) -> int:
+    return int(load_library().tv_tree_accept_workspace(B, n_max, V))
+
+
+def new_accept_workspace(B, n_max, V, device) -> Optional[torch.Tensor]:
+    """A zero-filled workspace for tv_tree_accept (None when the sizes need
+    none), reusable for later calls of the same sizes on the same stream."""
+    nbytes = tree_accept_workspace_bytes(B, n_max, V)
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device) if nbytes > 0 else None
+
+
 def tree_accept(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor], tokens: torch.Tensor,
                 parents: torch.Tensor, n_nodes: torch.Tensor, anc_mask: Optional[torch.Tensor],
                 depth: Optional[torch.Tensor], temperature: float, u_accept: Optional[torch.Tensor],
-                u_sample: Optional[torch.Tensor], status: torch.Tensor, *, outputs=None):
+                u_sample: Optional[torch.Tensor], status: torch.Tensor, *, outputs=None, workspace=None):
     """Greedy (temperature 0) or rejection-sampling acceptance.  Returns
     (accept_len int32 [B], path_nodes int32 [B, n_max], out_tokens int32 [B, n_max+1])."""
     B, n_max, V = target_logits.shape
     dev = target_logits.device
+    if workspace is None:
+        workspace = new_accept_workspace(B, n_max, V, dev)
     if outputs is None:
         accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
         path_nodes = torch.empty((B, n_max), dtype=torch.int32, device=dev)
@@ -180,7 +193,8 @@ def tree_accept(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor
     rc = load_library().tv_tree_accept(
         _ptr(target_logits), _ptr(draft_logits), _ptr(tokens), _ptr(parents), _ptr(n_nodes), _ptr(anc_mask),
         _ptr(depth), B, n_max, V, float(temperature), _ptr(u_accept), _ptr(u_sample), _ptr(accept_len),
-        _ptr(path_nodes), _ptr(out_tokens), None, 0, _ptr(status), _stream(dev))
+        _ptr(path_nodes), _ptr(out_tokens), _ptr(workspace), 0 if workspace is None else workspace.numel(),
+        _ptr(status), _stream(dev))
     _check(rc, "tv_tree_accept")
     return accept_len, path_nodes, out_tokens
 

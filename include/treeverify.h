@@ -152,8 +152,13 @@ int tv_tree_verify_attn_noalloc(const void* q, const void* k_cache, const void* 
                                 int32_t* status, void* stream);
 
 /*
- * Workspace size in bytes that tv_tree_accept needs (currently 0: the
- * acceptance keeps its per-node rows on chip).
+ * Workspace size in bytes that tv_tree_accept needs for these sizes.  It is
+ * non-zero when B * n_max * V * 4 <= 64 MiB: there a greedy call reads every
+ * node's logits in one parallel pass (per-slice partial argmaxes plus one
+ * arrival counter per request) instead of one dependent row read per tree
+ * level.  The workspace (16-byte aligned) must be zero-filled before its first
+ * use; every call leaves the counters at zero again, so one workspace serves
+ * any number of calls issued in order on one stream.  0: none needed.
  */
 size_t tv_tree_accept_workspace(int B, int n_max, int V);
 
@@ -184,6 +189,8 @@ size_t tv_tree_accept_workspace(int B, int n_max, int V);
  *  accept_len  int32 [B]          out: accepted non-root nodes a
  *  path_nodes  int32 [B, n_max]   out: 0, n_1 .. n_a, then -1
  *  out_tokens  int32 [B, n_max+1] out: tokens of n_1..n_a, the bonus, then -1
+ *  ws, ws_bytes  workspace of at least tv_tree_accept_workspace(B, n_max, V)
+ *                bytes (may be NULL when that is 0); TV_ERR_INVALID_ARG if smaller
  *  status      int32 [B]          in/out: TV_DEV_BAD_TOKEN
  */
 int tv_tree_accept(const float* target_logits, const float* draft_logits, const int32_t* tokens,

@@ -95,6 +95,43 @@ def test_greedy_random_trees_with_ties(V, seed):
     assert a.max() >= 2
 
 
+def test_greedy_one_pass_workspace_reuse_and_skips():
+    """The one-pass greedy walk on one workspace three times in a row (its arrival
+    counters must return to zero), with a request whose status is already set
+    (skipped) and one with a malformed tree (BAD_TREE) in the same batch."""
+    dev = require_gpu()
+    rng = np.random.Generator(np.random.PCG64(42))
+    B, V = 6, 5003
+    trees = [W.random_recursive_tree(rng, 40) for _ in range(B)]
+    w = W.make_custom(B=B, Hq=1, Hkv=1, D=64, prefix_len=[0] * B, parents_list=trees, seed=42, V=V, n_max=64)
+    for b in range(B):
+        for c in range(1, int(w.n_nodes[b])):
+            if rng.random() < 0.8:
+                w.tokens[b, c] = int(np.argmax(w.target_logits[b, int(w.parents[b, c])]))
+    w.parents[3, 5] = 7                       # parent after the child: malformed
+    assert tvb.tree_accept_workspace_bytes(B, 64, V) > 0
+    ws = tvb.new_accept_workspace(B, 64, V, dev)
+    dw = DevWorkload(w, dev)
+    ref = oracle.tree_accept_greedy(w.target_logits, w.tokens, w.parents, w.n_nodes)
+    for _ in range(3):
+        st = torch.zeros(B, dtype=torch.int32, device=dev)
+        st[1] = oracle.STATUS_PAGE_OOB        # set by an earlier stage: this request is skipped
+        a, pn, ot = tvb.tree_accept(dw.target, None, dw.tokens, dw.parents, dw.n_nodes, None, None, 0.0, None,
+                                    None, st, workspace=ws)
+        torch.cuda.synchronize()
+        a, pn, ot, st = a.cpu().numpy(), pn.cpu().numpy(), ot.cpu().numpy(), st.cpu().numpy()
+        for b in range(B):
+            if b == 1:
+                assert a[b] == 0 and (pn[b] == -1).all() and (ot[b] == -1).all() and st[b] == oracle.STATUS_PAGE_OOB
+                continue
+            assert st[b] == ref["status"][b]
+            assert a[b] == ref["accept_len"][b]
+            assert np.array_equal(pn[b], ref["path_nodes"][b]) and np.array_equal(ot[b], ref["out_tokens"][b])
+        assert st[3] == oracle.STATUS_BAD_TREE
+        assert a.max() >= 2
+    assert int(ws[-4 * B:].view(torch.int32).abs().sum()) == 0   # arrival counters back at zero
+
+
 def test_sampling_tiny():
     _check_sampling(W.make_workload("tiny"), require_gpu())
 
