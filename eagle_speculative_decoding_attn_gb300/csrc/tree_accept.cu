@@ -51,8 +51,49 @@ struct AcceptParams {
   int32_t* status;
 };
 
+// Double-float numbers: value = hi + lo with |lo| <= ulp(hi) / 2 (about 48
+// significant bits).  The sampling walk accumulates its sums, scans and
+// thresholds in this form on the fp32 pipe; fp64 throughput is far too low on
+// this GPU for a per-thread hot loop.  Sums use Knuth's TwoSum, products an
+// fma-based TwoProduct (Dekker/Knuth error-free transformations).
+struct Df {
+  float hi, lo;
+};
+__device__ __forceinline__ Df df_norm(float s, float e) {
+  const float hi = s + e;
+  return {hi, e - (hi - s)};
+}
+__device__ __forceinline__ Df df_add(Df a, Df b) {
+  const float s = a.hi + b.hi;
+  const float bb = s - a.hi;
+  const float e = (a.hi - (s - bb)) + (b.hi - bb) + (a.lo + b.lo);
+  return df_norm(s, e);
+}
+__device__ __forceinline__ Df df_add1(Df a, float b) {
+  const float s = a.hi + b;
+  const float bb = s - a.hi;
+  const float e = (a.hi - (s - bb)) + (b - bb) + a.lo;
+  return df_norm(s, e);
+}
+__device__ __forceinline__ Df df_mul1(Df a, float u) {
+  const float p = a.hi * u;
+  const float e = fmaf(a.lo, u, fmaf(a.hi, u, -p));
+  return df_norm(p, e);
+}
+__device__ __forceinline__ bool df_gt(Df a, Df b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+__device__ __forceinline__ bool df_pos(Df a) { return a.hi > 0.f; }
+__device__ __forceinline__ Df df_shfl_xor(Df a, int o) {
+  return {__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
+}
+__device__ __forceinline__ Df df_shfl_up(Df a, int o) {
+  return {__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
+}
+__device__ __forceinline__ Df df_shfl(Df a, int src) {
+  return {__shfl_sync(0xffffffffu, a.hi, src), __shfl_sync(0xffffffffu, a.lo, src)};
+}
+
 struct __align__(16) ClSlot {
-  double d[2];
+  Df d[2];
   float f[2];
   int i[2];
 };
@@ -68,12 +109,17 @@ struct AccShared {
   int path[kMaxNodes];
   float wf[kAccWarps];
   int wi[kAccWarps];
-  double wd[kAccWarps][2];
-  double thr_excl[kAccThreads];  // exclusive scan of per-thread sums (inverse CDF)
+  Df wd[kAccWarps][2];
+  Df thr_excl[kAccThreads];  // exclusive scan of per-thread sums (inverse CDF)
   ClSlot slot[2];
+  ClSlot gath[kCL];  // this exchange's slots of every CTA, copied in (rank order)
+  float ua[kMaxNodes];
   float bf;
   int bi;
-  double bd[2];
+  Df bd[2];
+  float cf[2];
+  uint64_t load_bar;
+  int timed_out;
   int bad;
   int cnt;
   int lowest;
@@ -111,41 +157,60 @@ __device__ void block_argmax(float v, int i, AccShared& sh) {
   __syncthreads();
 }
 
-__device__ void block_max(float v, AccShared& sh) {
+// Two block maxima at once; result in sh.cf (after a barrier).
+__device__ void block_max2(float u, float v, AccShared& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if (lane == 0) sh.wf[warp] = v;
+  for (int o = 16; o; o >>= 1) {
+    u = fmaxf(u, __shfl_xor_sync(0xffffffffu, u, o));
+    v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  }
+  if (lane == 0) {
+    sh.wf[warp] = u;
+    sh.wd[warp][0].hi = v;
+  }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float m = sh.wf[0];
-    for (int w = 1; w < kAccWarps; ++w) m = fmaxf(m, sh.wf[w]);
-    sh.bf = m;
+  if (warp == 0) {
+    u = lane < kAccWarps ? sh.wf[lane] : -FLT_MAX;
+    v = lane < kAccWarps ? sh.wd[lane][0].hi : -FLT_MAX;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      u = fmaxf(u, __shfl_xor_sync(0xffffffffu, u, o));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    }
+    if (lane == 0) {
+      sh.cf[0] = u;
+      sh.cf[1] = v;
+    }
   }
   __syncthreads();
 }
 
-// Two sums at once (fp32 inside a warp, fp64 across warps); result in sh.bd.
-__device__ void block_sum2(float a, float b, AccShared& sh) {
+// Two double-float sums over the block; result in sh.bd (after a barrier).
+__device__ void block_sum2(Df a, Df b, AccShared& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
-    a += __shfl_xor_sync(0xffffffffu, a, o);
-    b += __shfl_xor_sync(0xffffffffu, b, o);
+    a = df_add(a, df_shfl_xor(a, o));
+    b = df_add(b, df_shfl_xor(b, o));
   }
   if (lane == 0) {
     sh.wd[warp][0] = a;
     sh.wd[warp][1] = b;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    double x = 0.0, y = 0.0;
-    for (int w = 0; w < kAccWarps; ++w) {
-      x += sh.wd[w][0];
-      y += sh.wd[w][1];
+  if (warp == 0) {
+    Df x = lane < kAccWarps ? sh.wd[lane][0] : Df{0.f, 0.f};
+    Df y = lane < kAccWarps ? sh.wd[lane][1] : Df{0.f, 0.f};
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      x = df_add(x, df_shfl_xor(x, o));
+      y = df_add(y, df_shfl_xor(y, o));
     }
-    sh.bd[0] = x;
-    sh.bd[1] = y;
+    if (lane == 0) {
+      sh.bd[0] = x;
+      sh.bd[1] = y;
+    }
   }
   __syncthreads();
 }
@@ -158,7 +223,14 @@ struct ClusterEx {
   int buf;
   __device__ ClusterEx() : cl(cg::this_cluster()), buf(0) {}
   __device__ ClSlot* publish(AccShared& sh) { return &sh.slot[buf]; }
-  __device__ const ClSlot* remote(AccShared& sh, int r) { return cl.map_shared_rank(&sh.slot[buf], r); }
+  // cluster barrier, then the first kCL threads copy every CTA's slot into this
+  // CTA's shared memory (one remote read per slot instead of one per thread)
+  __device__ void exchange(AccShared& sh) {
+    cl.sync();
+    if (threadIdx.x < kCL) sh.gath[threadIdx.x] = *cl.map_shared_rank(&sh.slot[buf], (int)threadIdx.x);
+    __syncthreads();
+  }
+  __device__ const ClSlot* got(AccShared& sh, int r) { return &sh.gath[r]; }
   __device__ void sync() { cl.sync(); }
   __device__ void flip() { buf ^= 1; }
 };
@@ -179,33 +251,58 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
   float* wt = dyn;             // sampling: current target weights of this slice
   float* wq = dyn + p.chunk;   // sampling: draft weights of this slice
 
-  // ---- tree setup and validation (every CTA redundantly, identical results)
+  // ---- tree setup and validation (every CTA redundantly, identical results):
+  // one node per thread, then thread 0 builds the child lists from shared memory
   const int N = p.n_nodes[b];
+  const int st_in = p.status[b];
+  const bool n_ok = N >= 1 && N <= n_max;
+  bool sbad = false, tbad = false;
+  if (st_in == 0 && n_ok && tid < N) {
+    const int pi = p.parents[(int64_t)b * n_max + tid];
+    const int ti = p.tokens[(int64_t)b * n_max + tid];
+    sh.par[tid] = pi;
+    sh.tok[tid] = ti;
+    sbad = tid == 0 ? pi != -1 : (pi < 0 || pi >= tid);
+    tbad = tid >= 1 && (ti < 0 || ti >= V);
+  }
   if (tid == 0) {
-    int bad = p.status[b] != 0 ? -1 : 0;
-    if (!bad && (N < 1 || N > n_max)) bad = TV_DEV_BAD_TREE;
-    if (!bad) {
-      int cnt[kMaxNodes];
-      for (int i = 0; i < N; ++i) {
-        const int pi = p.parents[(int64_t)b * n_max + i];
-        const int ti = p.tokens[(int64_t)b * n_max + i];
-        sh.par[i] = pi;
-        sh.tok[i] = ti;
-        cnt[i] = 0;
-        if (i == 0 ? pi != -1 : (pi < 0 || pi >= i)) bad = TV_DEV_BAD_TREE;
-      }
-      if (!bad)
-        for (int i = 1; i < N; ++i)
-          if (sh.tok[i] < 0 || sh.tok[i] >= V) bad = TV_DEV_BAD_TOKEN;
-      if (!bad) {
-        for (int i = 1; i < N; ++i) cnt[sh.par[i]]++;
-        sh.kid_off[0] = 0;
-        for (int i = 0; i < N; ++i) sh.kid_off[i + 1] = sh.kid_off[i] + cnt[i];
-        for (int i = 0; i < N; ++i) cnt[i] = sh.kid_off[i];
-        for (int i = 1; i < N; ++i) sh.kids[cnt[sh.par[i]]++] = i;  // ascending per parent
-      }
+    mbar_init(&sh.load_bar, 1);
+    fence_barrier_init();
+    sh.timed_out = 0;
+  }
+  const bool any_s = __syncthreads_or(sbad) != 0;
+  const bool any_t = __syncthreads_or(tbad) != 0;
+  const int bad = st_in != 0 ? -1 : (!n_ok || any_s) ? TV_DEV_BAD_TREE : (any_t ? TV_DEV_BAD_TOKEN : 0);
+  if (bad == 0 && tid < kMaxNodes) {  // warps 0 and 1, whole
+    // children of node tid, then the exclusive scan of the counts over the nodes
+    int cnt = 0;
+    if (tid < N)
+      for (int j = 1; j < N; ++j) cnt += sh.par[j] == tid;
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if ((tid & 31) >= o) incl += y;
     }
-    sh.bad = bad;
+    if (tid == 31) sh.cnt = incl;  // warp 0's total
+    if (tid < N) {
+      sh.kid_off[tid] = incl - cnt;
+      if (p.sampling) sh.ua[tid] = p.u_accept[(int64_t)b * n_max + tid];
+    }
+  }
+  if (tid == 0) sh.bad = bad;
+  __syncthreads();
+  if (bad == 0 && tid < N) {
+    if (tid >= 32) sh.kid_off[tid] += sh.cnt;
+    if (tid == N - 1) sh.kid_off[N] = N - 1;  // every non-root node is somebody's child
+  }
+  __syncthreads();
+  if (bad == 0 && tid >= 1 && tid < N) {
+    // ascending child index within each parent's list
+    const int pj = sh.par[tid];
+    int before = 0;
+    for (int k = 1; k < tid; ++k) before += sh.par[k] == pj;
+    sh.kids[sh.kid_off[pj] + before] = tid;
   }
   __syncthreads();
   if (sh.bad != 0) {
@@ -254,11 +351,11 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
           s->f[0] = sh.bf;
           s->i[0] = sh.bi;
         }
-        ex.sync();
+        ex.exchange(sh);
         float gv = -FLT_MAX;
         int gi = INT_MAX;
         for (int r = 0; r < kCL; ++r) {
-          const ClSlot* s = ex.remote(sh, r);
+          const ClSlot* s = ex.got(sh, r);
           argmax_take(gv, gi, s->f[0], s->i[0]);
         }
         ex.flip();
@@ -291,170 +388,247 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
   } else {
     // ================================================ sampling: walk from the root
     int node = 0;
-    bool first = true;
+    uint32_t load_phase = 0;
     for (;;) {
-      if (!first) ex.sync();  // every CTA finished reading this CTA's slices
-      first = false;
+      // this thread's accesses to the slices precede the next copy into them (the
+      // last exchange was a barrier; no CTA reads another CTA's slices)
+      fence_proxy_async_smem();
       const float* trow = p.target + ((int64_t)b * n_max + node) * V + lo;
       const float* drow = p.draft + ((int64_t)b * n_max + node) * V + lo;
-      float mt = -FLT_MAX, mq = -FLT_MAX;
       if (vec4) {
-        const float4* t4 = reinterpret_cast<const float4*>(trow);
-        const float4* d4 = reinterpret_cast<const float4*>(drow);
-        for (int j = tid; j < (len >> 2); j += kAccThreads) {
-          const float4 x = __ldg(t4 + j);
-          const float4 y = __ldg(d4 + j);
-          reinterpret_cast<float4*>(wt)[j] = x;
-          reinterpret_cast<float4*>(wq)[j] = y;
-          mt = fmaxf(mt, fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
-          mq = fmaxf(mq, fmaxf(fmaxf(y.x, y.y), fmaxf(y.z, y.w)));
+        // 16-byte aligned slices: two bulk copies into shared memory
+        if (tid == 0) {
+          mbar_arrive_expect_tx(&sh.load_bar, 8u * (uint32_t)len);
+          if (len > 0) {
+            bulk_g2s(wt, trow, 4u * (uint32_t)len, &sh.load_bar);
+            bulk_g2s(wq, drow, 4u * (uint32_t)len, &sh.load_bar);
+          }
         }
+        if (!mbar_wait(&sh.load_bar, load_phase, &sh.timed_out)) sh.timed_out = 1;
+        load_phase ^= 1u;
       } else {
         for (int j = tid; j < len; j += kAccThreads) {
-          const float x = __ldg(trow + j), y = __ldg(drow + j);
-          wt[j] = x;
-          wq[j] = y;
-          mt = fmaxf(mt, x);
-          mq = fmaxf(mq, y);
+          wt[j] = __ldg(trow + j);
+          wq[j] = __ldg(drow + j);
         }
+        __syncthreads();
       }
-      block_max(mt, sh);
-      const float bmt = sh.bf;
-      block_max(mq, sh);
-      const float bmq = sh.bf;
+      float mt = -FLT_MAX, mq = -FLT_MAX;
+      for (int j = tid; j < len; j += kAccThreads) {
+        mt = fmaxf(mt, wt[j]);
+        mq = fmaxf(mq, wq[j]);
+      }
+      block_max2(mt, mq, sh);
       if (tid == 0) {
         ClSlot* s = ex.publish(sh);
-        s->f[0] = bmt;
-        s->f[1] = bmq;
+        s->f[0] = sh.cf[0];
+        s->f[1] = sh.cf[1];
       }
-      ex.sync();
+      ex.exchange(sh);
       float Mt = -FLT_MAX, Mq = -FLT_MAX;
       for (int r = 0; r < kCL; ++r) {
-        const ClSlot* s = ex.remote(sh, r);
+        const ClSlot* s = ex.got(sh, r);
         Mt = fmaxf(Mt, s->f[0]);
         Mq = fmaxf(Mq, s->f[1]);
       }
       ex.flip();
-      // exponentiate in place: w = 2^((z - max) * log2(e)/T)
-      float st = 0.f, sq = 0.f;
-      for (int j = tid; j < len; j += kAccThreads) {
-        const float et = exp2f((wt[j] - Mt) * p.k2);
-        const float eq = exp2f((wq[j] - Mq) * p.k2);
-        wt[j] = et;
-        wq[j] = eq;
-        st += et;
-        sq += eq;
+      // exponentiate in place: w = 2^((z - max) * log2(e)/T); sums in double-float
+      // (four terms in fp32, then into the double-float sum)
+      Df st{0.f, 0.f}, sq{0.f, 0.f};
+      for (int j0 = tid; j0 < len; j0 += 4 * kAccThreads) {
+        float gt = 0.f, gq = 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int j = j0 + u * kAccThreads;
+          if (j < len) {
+            const float et = exp2f((wt[j] - Mt) * p.k2);
+            const float eq = exp2f((wq[j] - Mq) * p.k2);
+            wt[j] = et;
+            wq[j] = eq;
+            gt += et;
+            gq += eq;
+          }
+        }
+        st = df_add1(st, gt);
+        sq = df_add1(sq, gq);
       }
       block_sum2(st, sq, sh);
+      const int k_beg = sh.kid_off[node], k_end = sh.kid_off[node + 1];
+      int f_owner = 0, f_off = 0;
+      if (k_beg < k_end) {
+        const int x = sh.tok[sh.kids[k_beg]];
+        f_owner = x / p.chunk;
+        f_off = x - f_owner * p.chunk;
+      }
       if (tid == 0) {
         ClSlot* s = ex.publish(sh);
         s->d[0] = sh.bd[0];
         s->d[1] = sh.bd[1];
+        if (k_beg < k_end && rank == f_owner) {
+          s->f[0] = wt[f_off];
+          s->f[1] = wq[f_off];
+        }
       }
-      ex.sync();
-      double St = 0.0, Sq = 0.0;
-      for (int r = 0; r < kCL; ++r) {
-        const ClSlot* s = ex.remote(sh, r);
-        St += s->d[0];
-        Sq += s->d[1];
+      ex.exchange(sh);
+      Df St{0.f, 0.f}, Sq{0.f, 0.f};
+      for (int r = 0; r < kCL; ++r) {  // rank order: identical in every CTA
+        const ClSlot* s = ex.got(sh, r);
+        St = df_add(St, s->d[0]);
+        Sq = df_add(Sq, s->d[1]);
+      }
+      float pv0 = 0.f, qv0 = 0.f;
+      if (k_beg < k_end) {
+        pv0 = ex.got(sh, f_owner)->f[0];
+        qv0 = ex.got(sh, f_owner)->f[1];
       }
       ex.flip();
-      float Sw = (float)St;            // normaliser of the current target weights wt
-      const float SqF = (float)Sq;     // normaliser of wq
-
+      float Sw = St.hi;         // normaliser of the current target weights wt
+      const float SqF = Sq.hi;  // normaliser of wq
+      const float isq = 1.f / SqF;
+      // the tested child's numerators: the owner CTA published them in the exchange
+      // (no CTA reads another CTA's slices during the walk)
+      float pv = pv0, qv = qv0;
+      // a residual step whose slice update is deferred to the next pass:
+      // wt = max(0, wt * pend_isw - wq * isq), its normaliser already in Sw
+      bool pending = false;
+      float pend_isw = 0.f;
       int accepted = -1;
-      for (int k = sh.kid_off[node]; k < sh.kid_off[node + 1]; ++k) {
+      for (int k = k_beg; k < k_end; ++k) {
         const int c = sh.kids[k];
-        const int x = sh.tok[c];
-        const int owner = x / p.chunk;
-        const int off = x - owner * p.chunk;
-        const float* rwt = ex.cl.map_shared_rank(wt, owner);
-        const float* rwq = ex.cl.map_shared_rank(wq, owner);
-        const float cur_x = rwt[off] / Sw;
-        const float q_x = rwq[off] / SqF;
-        const float u = p.u_accept[(int64_t)b * n_max + c];
-        if (u * q_x < cur_x) {
+        const float u = sh.ua[c];
+        if (u * (qv / SqF) < pv / Sw) {
           accepted = c;
           break;
         }
-        // rejected: residual max(0, cur - q), normalised (kept if it sums to 0)
-        float z = 0.f;
-        for (int j = tid; j < len; j += kAccThreads) z += fmaxf(0.f, wt[j] / Sw - wq[j] / SqF);
-        block_sum2(z, 0.f, sh);
+        // rejected: the residual max(0, p - q), normalised (p kept if it sums to 0).
+        // One pass applies the deferred update and sums the new residual; products
+        // and differences are rounded one by one so every pass agrees.
+        const float cur_isw = 1.f / Sw;
+        Df z{0.f, 0.f};
+        for (int j0 = tid; j0 < len; j0 += 4 * kAccThreads) {
+          float g = 0.f;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = j0 + u * kAccThreads;
+            if (j < len) {
+              float w = wt[j];
+              const float qq = __fmul_rn(wq[j], isq);
+              if (pending) {
+                w = fmaxf(0.f, __fsub_rn(__fmul_rn(w, pend_isw), qq));
+                wt[j] = w;
+              }
+              g += fmaxf(0.f, __fsub_rn(__fmul_rn(w, cur_isw), qq));
+            }
+          }
+          z = df_add1(z, g);
+        }
+        block_sum2(z, Df{0.f, 0.f}, sh);
+        const bool more = k + 1 < k_end;
+        int nx_owner = 0, nx_off = 0;
+        if (more) {
+          const int x = sh.tok[sh.kids[k + 1]];
+          nx_owner = x / p.chunk;
+          nx_off = x - nx_owner * p.chunk;
+        }
         if (tid == 0) {
           ClSlot* s = ex.publish(sh);
           s->d[0] = sh.bd[0];
+          if (more && rank == nx_owner) {
+            const float w = wt[nx_off];
+            const float qq = __fmul_rn(wq[nx_off], isq);
+            s->f[0] = w;                                                  // p numerator if kept
+            s->f[1] = wq[nx_off];                                         // q numerator
+            s->d[1].hi = fmaxf(0.f, __fsub_rn(__fmul_rn(w, cur_isw), qq));  // residual numerator
+          }
         }
-        ex.sync();
-        double Z = 0.0;
-        for (int r = 0; r < kCL; ++r) Z += ex.remote(sh, r)->d[0];
+        ex.exchange(sh);
+        Df Z{0.f, 0.f};
+        for (int r = 0; r < kCL; ++r) Z = df_add(Z, ex.got(sh, r)->d[0]);
+        float nw = 0.f, nq = 0.f, nr = 0.f;
+        if (more) {
+          const ClSlot* o = ex.got(sh, nx_owner);
+          nw = o->f[0];
+          nq = o->f[1];
+          nr = o->d[1].hi;
+        }
         ex.flip();
-        if (Z > 0.0) {
-          for (int j = tid; j < len; j += kAccThreads) wt[j] = fmaxf(0.f, wt[j] / Sw - wq[j] / SqF);
-          Sw = (float)Z;
+        if (df_pos(Z)) {
+          pending = true;
+          pend_isw = cur_isw;
+          Sw = Z.hi;
+          pv = nr;
+        } else {
+          pending = false;
+          pv = nw;
         }
-        ex.sync();  // residual slices complete before anyone reads them
+        qv = nq;
       }
       if (accepted >= 0) {
         node = accepted;
         continue;
       }
-      // ---- bonus token: inverse CDF of wt with u_sample[node]
+      if (pending) {  // the bonus draw reads the current p: apply the deferred update
+        for (int j = tid; j < len; j += kAccThreads)
+          wt[j] = fmaxf(0.f, __fsub_rn(__fmul_rn(wt[j], pend_isw), __fmul_rn(wq[j], isq)));
+        __syncthreads();
+      }
+      // ---- bonus token: inverse CDF of wt with u_sample[node] (double-float prefix sums)
       {
         const int per = (len + kAccThreads - 1) / kAccThreads;
         const int a0 = min(len, tid * per), a1 = min(len, a0 + per);
-        float tsum = 0.f;
-        for (int j = a0; j < a1; ++j) tsum += wt[j];
-        // exclusive scan over threads (fp64), thread 0 sequentially over warps
-        double v = tsum;
+        Df tsum{0.f, 0.f};
+        for (int j = a0; j < a1; ++j) tsum = df_add1(tsum, wt[j]);
+        // exclusive scan over the block's threads
         const int lane = tid & 31, warp = tid >> 5;
-        double incl = v;
+        Df incl = tsum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const double y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
+          const Df y = df_shfl_up(incl, o);
+          if (lane >= o) incl = df_add(incl, y);
         }
+        Df prev = df_shfl_up(incl, 1);
+        if (lane == 0) prev = Df{0.f, 0.f};
         if (lane == 31) sh.wd[warp][0] = incl;
         __syncthreads();
         if (tid == 0) {
-          double run = 0.0;
+          Df run{0.f, 0.f};
           for (int w = 0; w < kAccWarps; ++w) {
-            const double t = sh.wd[w][0];
+            const Df t = sh.wd[w][0];
             sh.wd[w][1] = run;
-            run += t;
+            run = df_add(run, t);
           }
           sh.bd[0] = run;
         }
         __syncthreads();
-        sh.thr_excl[tid] = sh.wd[warp][1] + incl - v;
-        const double s_r = sh.bd[0];
+        sh.thr_excl[tid] = df_add(sh.wd[warp][1], prev);
+        const Df s_r = sh.bd[0];
         if (tid == 0) {
           ClSlot* s = ex.publish(sh);
           s->d[0] = s_r;
         }
-        ex.sync();
-        double pre[kCL];
-        double S = 0.0;
+        ex.exchange(sh);
+        Df pre[kCL], srk[kCL];
+        Df S{0.f, 0.f};
         for (int r = 0; r < kCL; ++r) {
           pre[r] = S;
-          S += ex.remote(sh, r)->d[0];
+          srk[r] = ex.got(sh, r)->d[0];
+          S = df_add(S, srk[r]);
         }
         ex.flip();
-        const double t = (double)p.u_sample[(int64_t)b * n_max + node] * S;
+        const Df t = df_mul1(S, p.u_sample[(int64_t)b * n_max + node]);
         int rstar = -1, rlast = -1;
         for (int r = 0; r < kCL; ++r) {
-          const double sr = (r + 1 < kCL ? pre[r + 1] : S) - pre[r];
-          if (sr > 0.0) rlast = r;
-          if (rstar < 0 && pre[r] + sr > t) rstar = r;
+          if (df_pos(srk[r])) rlast = r;
+          if (rstar < 0 && df_gt(df_add(pre[r], srk[r]), t)) rstar = r;
         }
         const bool fallback_rank = rstar < 0;
         if (fallback_rank) rstar = rlast;
         int found = -1;
         if (rank == rstar) {
           // thread whose range crosses t (or the last non-empty one on fallback)
-          const double base = pre[rank] + sh.thr_excl[tid];
-          const bool crosses = !fallback_rank && tsum > 0.f && base + (double)tsum > t && base <= t;
-          const bool nonempty = tsum > 0.f;
+          const Df base = df_add(pre[rank], sh.thr_excl[tid]);
+          const bool nonempty = tsum.hi > 0.f;
+          const bool crosses = !fallback_rank && nonempty && df_gt(df_add(base, tsum), t) && !df_gt(base, t);
           if (tid == 0) {
             sh.bi = INT_MAX;
             sh.wi[0] = -1;
@@ -467,25 +641,25 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
           const bool fb = (kstar == INT_MAX);
           if (fb) kstar = sh.wi[0];
           if (tid == kstar) {
-            double acc = pre[rank] + sh.thr_excl[tid];
+            Df acc = base;
             int j_found = -1, j_last = -1;
             for (int j = a0; j < a1; ++j) {
               if (wt[j] > 0.f) j_last = j;
-              acc += (double)wt[j];
-              if (!fb && j_found < 0 && acc > t && wt[j] > 0.f) j_found = j;
+              acc = df_add1(acc, wt[j]);
+              if (!fb && j_found < 0 && df_gt(acc, t) && wt[j] > 0.f) j_found = j;
             }
-            sh.bd[1] = (double)(lo + (j_found >= 0 ? j_found : j_last));
+            sh.wi[1] = lo + (j_found >= 0 ? j_found : j_last);
           }
           __syncthreads();
-          found = (int)sh.bd[1];
+          found = sh.wi[1];
         }
         if (tid == 0) {
           ClSlot* s = ex.publish(sh);
           s->i[0] = found;
         }
-        ex.sync();
+        ex.exchange(sh);
         int tokv = -1;
-        for (int r = 0; r < kCL; ++r) tokv = max(tokv, ex.remote(sh, r)->i[0]);
+        for (int r = 0; r < kCL; ++r) tokv = max(tokv, ex.got(sh, r)->i[0]);
         ex.flip();
         bonus = tokv;
       }
@@ -496,6 +670,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
 
   // ---- outputs (rank 0)
   if (rank == 0 && tid == 0) {
+    if (sh.timed_out) atomicOr(p.status + b, TV_DEV_TIMEOUT);
     int len_path = 0;
     for (int j = best; j != 0; j = sh.par[j]) sh.path[len_path++] = j;
     // sh.path holds best .. first child; emit root-first
