@@ -168,6 +168,22 @@ def load_peaks():
 
 
 # ------------------------------------------------------------------ GPU leg
+def reduce_over_ranks(times, work, device):
+    """Whole-job figures of a replicated run: each timing is the maximum over
+    the ranks and each work count the sum (one all-reduce each); unchanged on a
+    single rank.  `device` is where the reduction tensors live (the GPU for
+    NCCL, the CPU for gloo)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(x) for x in times], [float(x) for x in work]
+    t = torch.tensor(times, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor(work, dtype=torch.float64, device=device)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return [float(x) for x in t.tolist()], [float(x) for x in n.tolist()]
+
+
 def profile_attn(args, W, tvb, dev):
     """A small self-contained command for profiler captures: mask once, then
     N eager attention calls on the chosen config."""
@@ -388,19 +404,12 @@ def main():
                        "uniforms copied from pinned host memory each step; results copied back"}
 
     nodes = float(np.sum(w.n_nodes))
-    nodes_total = nodes
-    if world > 1:
-        t = torch.tensor([step_ms, attn_us, ac_us], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, attn_us, ac_us = [float(x) for x in t.tolist()]
-        nn = torch.tensor([nodes], device=dev, dtype=torch.float64)
-        dist.all_reduce(nn)
-        nodes_total = float(nn.item())
-        if e2e is not None:
-            te = torch.tensor([e2e["ms_per_step"]], device=dev, dtype=torch.float64)
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-            e2e["ms_per_step"] = float(te.item())
-            e2e["value"] = nodes_total / (e2e["ms_per_step"] / 1000.0)
+    e2e_in = [e2e["ms_per_step"]] if e2e is not None else []
+    (step_ms, attn_us, ac_us, *e2e_out), (nodes_total,) = reduce_over_ranks(
+        [step_ms, attn_us, ac_us] + e2e_in, [nodes], dev)
+    if e2e is not None:
+        e2e["ms_per_step"] = e2e_out[0]
+        e2e["value"] = nodes_total / (e2e["ms_per_step"] / 1000.0)
 
     hbm, tf_burst, peak_src = load_peaks()
     abytes, aflops = w.attn_bytes(), w.attn_flops()
