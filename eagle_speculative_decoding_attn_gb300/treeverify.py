@@ -46,6 +46,7 @@ _SIGNATURES = {
     "tv_tree_accept_workspace": (_SZ, [_I, _I, _I]),
     "tv_tree_accept": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "tv_kv_commit_path": (_I, [_P, _P, _I, _I64, _I64, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "tv_selftest_wait_timeout": (_I, [_P, _P]),
     "tv_last_error": (ctypes.c_char_p, []),
     "tv_version": (ctypes.c_char_p, []),
 }
@@ -237,3 +238,11 @@ LAUNCHES = {"tree_build_mask": 1, "tree_verify_attn": 1, "tree_accept": 1, "kv_c
 def launches_per_step() -> int:
     """Kernel launches of one verification step (the four calls once each)."""
     return sum(LAUNCHES.values())
+
+
+def selftest_wait_timeout(status: torch.Tensor):
+    """Run the bounded-wait self-test: sets TV_DEV_TIMEOUT (8) in status[0]."""
+    _expect(status, torch.int32, status.shape, "status")
+    rc = load_library().tv_selftest_wait_timeout(_ptr(status), _stream(status.device))
+    _check(rc, "tv_selftest_wait_timeout")
+    return status

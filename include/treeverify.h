@@ -222,6 +222,15 @@ int tv_kv_commit_path(void* k_cache, void* v_cache, int n_layers, int64_t layer_
                       const int32_t* path_nodes, int B, int n_max, int Hkv, int D, int page_size,
                       int64_t* committed_slots, int32_t* new_len, int32_t* status, void* stream);
 
+/*
+ * tv_selftest_wait_timeout — self-test of the bounded waits every kernel uses
+ * (no counterpart in the pages).  One CTA waits on an mbarrier that nothing
+ * ever completes; after the wait limit (1 s) it ORs TV_DEV_TIMEOUT into
+ * *status (int32, device) and returns.  Nothing traps and the context stays
+ * usable.  Asynchronous on `stream`; expect about one second of GPU time.
+ */
+int tv_selftest_wait_timeout(int32_t* status, void* stream);
+
 /* Message for the calling thread's last failed call ("" if none). */
 const char* tv_last_error(void);
 
