@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(kCommitThreads) kv_commit_kernel(const CommitP
   const int b = blockIdx.x / p.ctas_per_req;
   const int c_in = blockIdx.x % p.ctas_per_req;  // this CTA takes pairs c_in, c_in + ctas_per_req, ...
   const bool leader = c_in == 0;
+  griddep_wait();
   const int L = p.prefix_len[b];
   const int N = p.n_nodes[b];
   const int st = p.status[b];
@@ -225,9 +226,9 @@ extern "C" int tv_kv_commit_path(void* k_cache, void* v_cache, int n_layers, int
   p.status = status;
   cudaStream_t s = tv::as_stream(stream);
   if (D == 128)
-    tv::kv_commit_kernel<128><<<(unsigned)grid, tv::kCommitThreads, 0, s>>>(p);
+    TV_CUDA_CHECK(tv::launch_pdl(tv::kv_commit_kernel<128>, dim3((unsigned)grid), dim3(tv::kCommitThreads), 0, s, p));
   else
-    tv::kv_commit_kernel<64><<<(unsigned)grid, tv::kCommitThreads, 0, s>>>(p);
+    TV_CUDA_CHECK(tv::launch_pdl(tv::kv_commit_kernel<64>, dim3((unsigned)grid), dim3(tv::kCommitThreads), 0, s, p));
   TV_CUDA_CHECK(cudaGetLastError());
   return TV_OK;
 }

@@ -251,6 +251,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
   float* wt = dyn;             // sampling: current target weights of this slice
   float* wq = dyn + p.chunk;   // sampling: draft weights of this slice
 
+  griddep_wait();
   // ---- tree setup and validation (every CTA redundantly, identical results):
   // one node per thread, then thread 0 builds the child lists from shared memory
   const int N = p.n_nodes[b];
@@ -744,6 +745,7 @@ __global__ void __launch_bounds__(kArgThreads) greedy_onepass_kernel(const OnePa
   const int sl = blockIdx.x, node = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   const int n_max = p.n_max, V = p.V;
+  griddep_wait();
   const int N = p.n_nodes[b];
   const bool req_ok = p.status[b] == 0 && N >= 1 && N <= n_max;
 
@@ -943,7 +945,8 @@ extern "C" int tv_tree_accept(const float* target_logits, const float* draft_log
     q.path_nodes = path_nodes;
     q.out_tokens = out_tokens;
     q.status = status;
-    tv::greedy_onepass_kernel<<<dim3(q.n_slices, n_max, B), tv::kArgThreads, 0, tv::as_stream(stream)>>>(q);
+    TV_CUDA_CHECK(tv::launch_pdl(tv::greedy_onepass_kernel, dim3(q.n_slices, n_max, B), dim3(tv::kArgThreads), 0,
+                                 tv::as_stream(stream), q));
     TV_CUDA_CHECK(cudaGetLastError());
     return TV_OK;
   }
@@ -967,7 +970,8 @@ extern "C" int tv_tree_accept(const float* target_logits, const float* draft_log
   p.status = status;
   const size_t smem = sampling ? 2ull * chunk * sizeof(float) : 0;
   TV_CUDA_CHECK(tv::ensure_smem_attr((const void*)tv::tree_accept_kernel, 2ull * tv::kMaxChunk * sizeof(float)));
-  tv::tree_accept_kernel<<<B * tv::kCL, tv::kAccThreads, smem, tv::as_stream(stream)>>>(p);
+  TV_CUDA_CHECK(tv::launch_pdl(tv::tree_accept_kernel, dim3(B * tv::kCL), dim3(tv::kAccThreads), smem,
+                               tv::as_stream(stream), p));
   TV_CUDA_CHECK(cudaGetLastError());
   return TV_OK;
 }

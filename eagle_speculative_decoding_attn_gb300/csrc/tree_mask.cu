@@ -17,6 +17,7 @@ __global__ void __launch_bounds__(64) tree_mask_kernel(const int32_t* __restrict
   __shared__ int32_t par[kMaxNodes];
   const int b = blockIdx.x;
   const int i = threadIdx.x;
+  griddep_wait();
   const int n = n_nodes[b];
   const bool n_ok = n >= 1 && n <= n_max;
   const int p = i < n_max ? parents[(int64_t)b * n_max + i] : 0;
@@ -55,8 +56,8 @@ extern "C" int tv_tree_build_mask(const int32_t* parents, const int32_t* n_nodes
   TV_REQUIRE(n_max >= 1 && n_max <= tv::kMaxNodes, TV_ERR_UNSUPPORTED,
              "tv_tree_build_mask: n_max = %d not in [1, 64]", n_max);
   if (B == 0) return TV_OK;
-  tv::tree_mask_kernel<<<B, 64, 0, tv::as_stream(stream)>>>(parents, n_nodes, n_max, anc_mask, depth,
-                                                            status);
+  TV_CUDA_CHECK(tv::launch_pdl(tv::tree_mask_kernel, dim3(B), dim3(64), 0, tv::as_stream(stream), parents, n_nodes,
+                               n_max, anc_mask, depth, status));
   TV_CUDA_CHECK(cudaGetLastError());
   return TV_OK;
 }

@@ -9,6 +9,11 @@
 namespace tv {
 
 // ---------------------------------------------------------------- misc
+// Programmatic dependent launch: wait until the previous kernel of the stream
+// has completed and its writes are visible.  (No kernel triggers its dependents
+// early: a waiting dependent's CTAs would take SM slots from the running grid.)
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

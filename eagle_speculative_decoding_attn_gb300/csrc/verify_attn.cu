@@ -405,6 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
     tmem_alloc(&tmem_sh, 512);
     tmem_relinquish();
   }
+  // everything above is on chip; global memory only after the previous kernel
+  griddep_wait();
   if (warp == 3) {
     // ---- plan: per-request tiles and costs, exclusive scan of the costs
     int64_t carry = 0;
@@ -955,7 +957,7 @@ static bool make_map4(CUtensorMap* m, const void* base, const uint64_t dims[4], 
 template <int D>
 static int launch(const AttnParams& ap, int grid, cudaStream_t st) {
   TV_CUDA_CHECK(ensure_smem_attr((const void*)verify_attn_kernel<D>, Smem<D>::kAlloc));
-  verify_attn_kernel<D><<<grid, kThreads, Smem<D>::kAlloc, st>>>(ap);
+  TV_CUDA_CHECK(launch_pdl(verify_attn_kernel<D>, dim3(grid), dim3(kThreads), (size_t)Smem<D>::kAlloc, st, ap));
   TV_CUDA_CHECK(cudaGetLastError());
   return TV_OK;
 }
