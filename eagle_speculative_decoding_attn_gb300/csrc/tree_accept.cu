@@ -577,8 +577,17 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
       {
         const int per = (len + kAccThreads - 1) / kAccThreads;
         const int a0 = min(len, tid * per), a1 = min(len, a0 + per);
+        // this thread's range sum, starting at an offset rotated by the lane so that
+        // the 32 lanes hit 32 different banks (the ranges are `per` words apart)
         Df tsum{0.f, 0.f};
-        for (int j = a0; j < a1; ++j) tsum = df_add1(tsum, wt[j]);
+        {
+          const int cnt = a1 - a0;
+          int jj = cnt > 0 ? (tid & 31) % cnt : 0;
+          for (int n = 0; n < cnt; ++n) {
+            tsum = df_add1(tsum, wt[a0 + jj]);
+            jj = (jj + 1 == cnt) ? 0 : jj + 1;
+          }
+        }
         // exclusive scan over the block's threads
         const int lane = tid & 31, warp = tid >> 5;
         Df incl = tsum;
