@@ -43,6 +43,7 @@
 #include <cstring>
 #include <mutex>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 #include "tv_common.cuh"
 
 namespace tv {
@@ -77,8 +78,9 @@ struct AttnParams {
   int32_t* ws_bits;     // [B] device-found status bits of this call (zero between calls)
   int32_t* ws_tickets;  // [B * Hkv * mp_max * 2] split arrival counters (zero between calls)
   int32_t* ws_exit;     // CTA exit counter (zero between calls)
-  float* part_o;        // [2 * gridDim][D/4][256] float4: column group major, rows contiguous
-  float* part_lse;      // [2 * gridDim][256]
+  uint4* part_o;        // [2 * gridDim][D/8][256] 8 x fp16: column group major, rows contiguous
+  float* part_lse;      // [2 * gridDim][256] log-sum-exp of each partial row
+  float* part_scale;    // [2 * gridDim][256] max |O| of each partial row (its fp16 values are O / max)
   int64_t num_pages;
   int B, max_pages, n_max, Hq, Hkv, G, q_box_nodes, mp_max;
   float scale_log2;
@@ -168,9 +170,11 @@ __device__ void iter_init(ItemIter& it, const PlanView& pv, int cta) {
     const int64_t per_g = (int64_t)T * (MT + MP);
     const int64_t off = it.lo - pv.start[b];
     if (off > 0) {
-      const int g = (int)imin64(pv.Hkv - 1, off / per_g);
+      // 32-bit divisions when every cost position fits in 32 bits
+      const int g = (int)imin64(pv.Hkv - 1, pv.narrow ? (int64_t)((uint32_t)off / (uint32_t)per_g) : off / per_g);
       const int64_t off2 = off - g * per_g;
-      const int mp = (int)imin64(MP - 1, off2 / (3ll * T));
+      const int mp = (int)imin64(MP - 1, pv.narrow ? (int64_t)((uint32_t)off2 / (uint32_t)(3 * T))
+                                                   : off2 / (3ll * T));
       it.j = g * MP + mp;
       it.gstart = pv.start[b] + g * per_g + (int64_t)mp * 3 * T;
     }
@@ -260,14 +264,16 @@ __device__ __forceinline__ int split_slot(const Item& it, int sp) { return sp ==
 // The last split of a (group, M tile) combines every split's normalised
 // partial rows by their log-sum-exp weights: out = sum_s w_s O_s with
 // w_s = exp(lse_s - m) / sum_s' exp(lse_s' - m), m = max_s lse_s, and
-// lse = m + ln sum_s exp(lse_s - m).  The work items are (row, column slice)
-// pairs spread over the whole warpgroup, consecutive threads on consecutive
-// rows so the partial reads coalesce; one item loads the log-sum-exps and the
-// slices of up to kMB splits in a single round trip (kMB * kF float4 per thread
-// in flight), and needs a separate pass for the weights only above kMB splits.
+// lse = m + ln sum_s exp(lse_s - m).  A partial row is stored as fp16 values
+// of O_s / c_s with c_s = max |O_s| (kept in fp32), so w_s c_s multiplies them.
+// The work items are (row, column slice) pairs spread over the whole
+// warpgroup, consecutive threads on consecutive rows so the partial reads
+// coalesce; one item loads the log-sum-exps, scales and slices of up to kMB
+// splits in a single round trip (kMB * kF 16-byte loads per thread in flight),
+// and needs a separate pass for the weights only above kMB splits.
 template <int D, int kMB, int kF>
 __device__ void merge_items(const AttnParams& p, const Item& it, int mtile, int n_rows, int r) {
-  constexpr int kSlices = D / (4 * kF);
+  constexpr int kSlices = D / (8 * kF);
   const int G = p.G;
   const int ns = it.n_splits;
   const int n_items = n_rows * kSlices;
@@ -296,25 +302,26 @@ __device__ void merge_items(const AttnParams& p, const Item& it, int mtile, int 
         m = mb;
       }
     }
-    float acc[4 * kF];
+    float acc[8 * kF];
 #pragma unroll
-    for (int c = 0; c < 4 * kF; ++c) acc[c] = 0.f;
+    for (int c = 0; c < 8 * kF; ++c) acc[c] = 0.f;
     for (int s0 = 0; s0 < ns; s0 += kMB) {
-      float ls[kMB];
-      float4 x[kMB][kF];
+      float ls[kMB], sc[kMB];
+      uint4 x[kMB][kF];
 #pragma unroll
       for (int u = 0; u < kMB; ++u) {
         if (s0 + u < ns) {
           const int slot = split_slot(it, s0 + u);
           ls[u] = __ldcg(p.part_lse + (int64_t)slot * kRowsPerSlot + prow);
-          const float4* src =
-              reinterpret_cast<const float4*>(p.part_o) + ((int64_t)slot * (D / 4) + sl * kF) * kRowsPerSlot + prow;
+          sc[u] = __ldcg(p.part_scale + (int64_t)slot * kRowsPerSlot + prow);
+          const uint4* src = p.part_o + ((int64_t)slot * (D / 8) + sl * kF) * kRowsPerSlot + prow;
 #pragma unroll
           for (int q = 0; q < kF; ++q) x[u][q] = __ldcg(src + q * kRowsPerSlot);
         } else {
           ls[u] = -INFINITY;
+          sc[u] = 0.f;
 #pragma unroll
-          for (int q = 0; q < kF; ++q) x[u][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int q = 0; q < kF; ++q) x[u][q] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
       if (ns <= kMB) {  // one batch: the weights come from the values just loaded
@@ -326,19 +333,22 @@ __device__ void merge_items(const AttnParams& p, const Item& it, int mtile, int 
       const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
       for (int u = 0; u < kMB; ++u) {
-        const float wv = (ls[u] == -INFINITY) ? 0.f : ex2_approx((ls[u] - m) * kLog2e) * inv;
+        const float wv = (ls[u] == -INFINITY) ? 0.f : ex2_approx((ls[u] - m) * kLog2e) * inv * sc[u];
 #pragma unroll
         for (int q = 0; q < kF; ++q) {
-          acc[4 * q] += wv * x[u][q].x;
-          acc[4 * q + 1] += wv * x[u][q].y;
-          acc[4 * q + 2] += wv * x[u][q].z;
-          acc[4 * q + 3] += wv * x[u][q].w;
+          const uint32_t hw[4] = {x[u][q].x, x[u][q].y, x[u][q].z, x[u][q].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hw[e]));
+            acc[8 * q + 2 * e] += wv * f.x;
+            acc[8 * q + 2 * e + 1] += wv * f.y;
+          }
         }
       }
     }
-    uint4* dst = reinterpret_cast<uint4*>(p.out + orow_idx * D + sl * (4 * kF));
+    uint4* dst = reinterpret_cast<uint4*>(p.out + orow_idx * D + sl * (8 * kF));
 #pragma unroll
-    for (int q = 0; q < kF / 2; ++q)
+    for (int q = 0; q < kF; ++q)
       dst[q] = make_uint4(pack_bf16x2(acc[8 * q], acc[8 * q + 1]), pack_bf16x2(acc[8 * q + 2], acc[8 * q + 3]),
                           pack_bf16x2(acc[8 * q + 4], acc[8 * q + 5]), pack_bf16x2(acc[8 * q + 6], acc[8 * q + 7]));
     if (sl == 0 && p.lse) p.lse[orow_idx] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
@@ -347,8 +357,12 @@ __device__ void merge_items(const AttnParams& p, const Item& it, int mtile, int 
 
 template <int D>
 __device__ __forceinline__ void merge_tile(const AttnParams& p, const Item& it, int mtile, int n_rows, int r) {
-  if (it.n_splits <= 4) merge_items<D, 4, 8>(p, it, mtile, n_rows, r);
-  else merge_items<D, 8, 4>(p, it, mtile, n_rows, r);
+  // (splits per round trip, 16-byte loads per split): about 128 registers of loads
+  // and accumulators either way
+  if (it.n_splits <= 2) merge_items<D, 2, (D >= 128 ? 8 : 4)>(p, it, mtile, n_rows, r);
+  else if (it.n_splits <= 4) merge_items<D, 4, 4>(p, it, mtile, n_rows, r);
+  else if (it.n_splits <= 6) merge_items<D, 6, 4>(p, it, mtile, n_rows, r);
+  else merge_items<D, 8, 2>(p, it, mtile, n_rows, r);
 }
 
 template <int D>
@@ -811,12 +825,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
       const int64_t orow_idx = ((int64_t)item.b * p.n_max + node) * p.Hq + h;
       const bool direct = item.n_splits == 1;
       const int prow = mtile * kBM + r;
-      float4* pslot = reinterpret_cast<float4*>(p.part_o) + (int64_t)item.my_slot * (D / 4) * kRowsPerSlot + prow;
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      // the normalised row (both accumulators in dual mode), in chunks of 32 columns
+      auto row_chunk = [&](int c0, float* y) {
         uint32_t o[32];
         tmem_ld32(tO + c0, o);
-        float y[32];
         if (dual) {
           uint32_t o1[32];
           tmem_ld32(tO1 + c0, o1);
@@ -826,6 +838,24 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
 #pragma unroll
           for (int c = 0; c < 32; ++c) y[c] = __uint_as_float(o[c]) * inv_l;
         }
+      };
+      float row_scale = 0.f;
+      if (!direct) {
+        // a partial row is stored as fp16 values of O / max |O|
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float y[32];
+          row_chunk(c0, y);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) row_scale = fmaxf(row_scale, fabsf(y[c]));
+        }
+      }
+      const float to_half = row_scale > 0.f ? 1.f / row_scale : 0.f;
+      uint4* pslot = p.part_o + (int64_t)item.my_slot * (D / 8) * kRowsPerSlot + prow;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float y[32];
+        row_chunk(c0, y);
         if (row_ok) {
           if (direct) {
             uint4* dst = reinterpret_cast<uint4*>(p.out + orow_idx * D + c0);
@@ -834,10 +864,17 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
               dst[q] = make_uint4(pack_bf16x2(y[8 * q], y[8 * q + 1]), pack_bf16x2(y[8 * q + 2], y[8 * q + 3]),
                                   pack_bf16x2(y[8 * q + 4], y[8 * q + 5]), pack_bf16x2(y[8 * q + 6], y[8 * q + 7]));
           } else {
-            float4* dst = pslot + (c0 / 4) * kRowsPerSlot;
+            uint4* dst = pslot + (c0 / 8) * kRowsPerSlot;
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q * kRowsPerSlot] = make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+            for (int q = 0; q < 4; ++q) {
+              uint32_t hw[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __half2 h = __floats2half2_rn(y[8 * q + 2 * e] * to_half, y[8 * q + 2 * e + 1] * to_half);
+                hw[e] = *reinterpret_cast<const uint32_t*>(&h);
+              }
+              dst[q * kRowsPerSlot] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            }
           }
         }
       }
@@ -847,7 +884,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
       if (direct) {
         if (row_ok && p.lse) p.lse[orow_idx] = lse_v;
       } else {
-        if (row_ok) p.part_lse[(int64_t)item.my_slot * kRowsPerSlot + prow] = lse_v;
+        if (row_ok) {
+          p.part_lse[(int64_t)item.my_slot * kRowsPerSlot + prow] = lse_v;
+          p.part_scale[(int64_t)item.my_slot * kRowsPerSlot + prow] = row_scale;
+        }
         // ticket: the last split of this (group, M tile) to arrive merges every partial
         __threadfence();
         ok = wg_sync();
@@ -911,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
 
 // ---------------------------------------------------------------- host side
 struct WsLayout {
-  size_t bits, tickets, exit, part_lse, part_o, total;
+  size_t bits, tickets, exit, part_lse, part_scale, part_o, total;
   int mp_max;
 };
 
@@ -926,8 +966,9 @@ static WsLayout ws_layout(int B, int n_max, int Hq, int Hkv, int D, int grid) {
   w.bits = 256;
   w.tickets = align256(w.bits + sizeof(int32_t) * (size_t)std::max(B, 1));
   w.part_lse = align256(w.tickets + sizeof(int32_t) * (size_t)std::max(B, 1) * Hkv * w.mp_max * kNT);
-  w.part_o = align256(w.part_lse + sizeof(float) * (size_t)2 * grid * kRowsPerSlot);
-  w.total = align256(w.part_o + sizeof(float) * (size_t)2 * grid * kRowsPerSlot * D);
+  w.part_scale = align256(w.part_lse + sizeof(float) * (size_t)2 * grid * kRowsPerSlot);
+  w.part_o = align256(w.part_scale + sizeof(float) * (size_t)2 * grid * kRowsPerSlot);
+  w.total = align256(w.part_o + sizeof(uint16_t) * (size_t)2 * grid * kRowsPerSlot * D);
   return w;
 }
 
@@ -1025,7 +1066,8 @@ static void bind_workspace(AttnParams* ap, const WsLayout& wl, uint8_t* wsb) {
   ap->ws_bits = reinterpret_cast<int32_t*>(wsb + wl.bits);
   ap->ws_tickets = reinterpret_cast<int32_t*>(wsb + wl.tickets);
   ap->part_lse = reinterpret_cast<float*>(wsb + wl.part_lse);
-  ap->part_o = reinterpret_cast<float*>(wsb + wl.part_o);
+  ap->part_scale = reinterpret_cast<float*>(wsb + wl.part_scale);
+  ap->part_o = reinterpret_cast<uint4*>(wsb + wl.part_o);
   ap->mp_max = wl.mp_max;
 }
 
