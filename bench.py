@@ -278,13 +278,19 @@ def main():
                              shared["n_nodes"], cp["anc"], w.scale, cp["status"], out=cp["out"], lse=cp["lse"],
                              workspace=cp["ws"])
 
-    def accept_commit_call(cp):
+    def accept_call(cp):
         tvb.tree_accept(cp["target"], cp["draft"], shared["tokens"], shared["parents"], shared["n_nodes"],
                         cp["anc"], cp["depth"], w.temperature, shared["u_accept"] if sampling else None,
                         shared["u_sample"] if sampling else None, cp["status"], outputs=cp["acc"],
                         workspace=cp["aws"])
+
+    def commit_call(cp):
         tvb.kv_commit_path(cp["k"], cp["v"], shared["page_table"], shared["prefix_len"], shared["n_nodes"],
                            cp["acc"][0], cp["acc"][1], cp["status"], outputs=cp["com"])
+
+    def accept_commit_call(cp):
+        accept_call(cp)
+        commit_call(cp)
 
     def step_call(cp):
         mask_call(cp)
@@ -298,6 +304,7 @@ def main():
 
     side = torch.cuda.Stream(dev)
     graphs, attn_graph, ac_graph = [], torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    acc_graph, com_graph = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.stream(side):
         for cp in copies:
             gph = torch.cuda.CUDAGraph()
@@ -310,6 +317,12 @@ def main():
         with torch.cuda.graph(ac_graph, stream=side):
             for cp in copies:
                 accept_commit_call(cp)
+        with torch.cuda.graph(acc_graph, stream=side):
+            for cp in copies:
+                accept_call(cp)
+        with torch.cuda.graph(com_graph, stream=side):
+            for cp in copies:
+                commit_call(cp)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream(dev)
 
@@ -347,10 +360,34 @@ def main():
     for _ in range(reps):
         ac_graph.replay()
     c1.record(stream)
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    acc_graph.replay()
+    x0.record(stream)
+    for _ in range(reps):
+        acc_graph.replay()
+    x1.record(stream)
+    y0, y1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    com_graph.replay()
+    y0.record(stream)
+    for _ in range(reps):
+        com_graph.replay()
+    y1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     attn_us = a0.elapsed_time(a1) * 1000.0 / (reps * R)
     ac_us = c0.elapsed_time(c1) * 1000.0 / (reps * R)
+    accept_us = x0.elapsed_time(x1) * 1000.0 / (reps * R)
+    commit_us = y0.elapsed_time(y1) * 1000.0 / (reps * R)
+    # bytes of the accept and commit rooflines: logits rows (all nodes; the accepted
+    # path's nodes only, the lower bound) and the moved K/V rows of every layer
+    acc_len = copies[0]["acc"][0].cpu().numpy().astype(np.int64)
+    path_nodes = copies[0]["acc"][1].cpu().numpy()
+    rows_factor = (2 if sampling else 1) * V * 4
+    accept_bytes_all = int(np.sum(w.n_nodes)) * rows_factor
+    accept_bytes_path = int(np.sum(acc_len + 1)) * rows_factor
+    moved = sum(int(np.sum(path_nodes[b, 1:acc_len[b] + 1] != np.arange(1, acc_len[b] + 1)))
+                for b in range(B))
+    commit_bytes = moved * 2 * Hkv * D * 2 * 2 * layers  # K and V rows, read and written
 
     # end to end through the public binding with host buffers
     e2e = None
@@ -405,8 +442,8 @@ def main():
 
     nodes = float(np.sum(w.n_nodes))
     e2e_in = [e2e["ms_per_step"]] if e2e is not None else []
-    (step_ms, attn_us, ac_us, *e2e_out), (nodes_total,) = reduce_over_ranks(
-        [step_ms, attn_us, ac_us] + e2e_in, [nodes], dev)
+    (step_ms, attn_us, ac_us, accept_us, commit_us, *e2e_out), (nodes_total,) = reduce_over_ranks(
+        [step_ms, attn_us, ac_us, accept_us, commit_us] + e2e_in, [nodes], dev)
     if e2e is not None:
         e2e["ms_per_step"] = e2e_out[0]
         e2e["value"] = nodes_total / (e2e["ms_per_step"] / 1000.0)
@@ -449,6 +486,13 @@ def main():
         "attn_roofline_frac": max(t_hbm, t_tc) / attn_s,
         "attn_nodes_per_s": nodes_total / attn_s,
         "accept_commit_us": ac_us,
+        "accept": {"us": accept_us, "mode": "sampling" if sampling else "greedy",
+                   "bytes_all_rows": accept_bytes_all, "bytes_path_rows": accept_bytes_path,
+                   "hbm_us_all_rows": accept_bytes_all / (hbm * 1e3),
+                   "hbm_us_path_rows": accept_bytes_path / (hbm * 1e3)},
+        "commit": {"us": commit_us, "layers": layers, "moved_rows_per_layer_head": moved,
+                   "bytes": commit_bytes, "hbm_us": commit_bytes / (hbm * 1e3)},
+        "nodes_per_s_attn_accept_commit": nodes_total / ((attn_us + accept_us + commit_us) * 1e-6),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json)",
                      "algorithmic": {"bytes": abytes, "flops": aflops}},
