@@ -426,3 +426,62 @@ def make_custom(*, B, Hq, Hkv, D, prefix_len, parents_list, seed=0, V=16, temper
                     target_logits=target, draft_logits=draft if temperature > 0 else None,
                     u_accept=rng.random((B, n_max), dtype=np.float32),
                     u_sample=rng.random((B, n_max), dtype=np.float32))
+
+
+# --------------------------------------------------------------------------
+# dynamic tree construction inputs
+# --------------------------------------------------------------------------
+ROW_PEAKED, ROW_FEW, ROW_FLAT = 0, 1, 2
+
+
+@dataclasses.dataclass
+class ExpandWorkload:
+    B: int
+    n_max: int
+    V: int
+    draft_logits: np.ndarray    # fp32 [B, n_max, V]: the drafter's row for every node id
+    kinds: np.ndarray           # int8 [B, n_max]: ROW_PEAKED / ROW_FEW / ROW_FLAT
+    root_tokens: np.ndarray     # int32 [B]
+    n_levels: int
+    top_k: int
+    max_new: int
+    budget: int
+
+    def level_bytes(self, frontier_rows: int) -> int:
+        """Logit bytes one level reads for this many frontier rows in total."""
+        return int(frontier_rows) * self.V * 4
+
+
+def make_expand_workload(B: int, n_max: int, V: int, *, seed: int, n_levels: int = 6, top_k: int = 8,
+                         max_new: int = 16, budget: Optional[int] = None, p_kinds=(0.35, 0.35, 0.30),
+                         sigma_flat: float = 3.0, spike: float = 25.0) -> ExpandWorkload:
+    """Synthetic drafter rows for dynamic tree construction.
+
+    Every row is one of three kinds, drawn with probabilities ``p_kinds``:
+      peaked: N(0,1) logits plus ``spike`` on one random token (a
+              deterministic context: entropy near 0, a single branch);
+      few:    N(0,1) logits plus spike + N(0, 0.7) on 2..6 random tokens (a
+              handful of plausible continuations: perplexity between 1 and 6);
+      flat:   sigma_flat * N(0,1) logits (an open context: high entropy, the
+              widest branching).
+    Rows exist for every node id the tree may reach; a row is read only when
+    its node is on a frontier.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    kinds = rng.choice(3, size=(B, n_max), p=list(p_kinds)).astype(np.int8)
+    logits = rng.standard_normal((B, n_max, V), dtype=np.float32)
+    for b in range(B):
+        for f in range(n_max):
+            k = int(kinds[b, f])
+            if k == ROW_FLAT:
+                logits[b, f] *= np.float32(sigma_flat)
+            elif k == ROW_PEAKED:
+                logits[b, f, int(rng.integers(0, V))] += np.float32(spike)
+            else:
+                cnt = int(rng.integers(2, 7))
+                toks = rng.choice(V, size=cnt, replace=False)
+                logits[b, f, toks] += (spike + 0.7 * rng.standard_normal(cnt)).astype(np.float32)
+    root_tokens = rng.integers(0, V, size=B).astype(np.int32)
+    return ExpandWorkload(B=B, n_max=n_max, V=V, draft_logits=logits, kinds=kinds, root_tokens=root_tokens,
+                          n_levels=n_levels, top_k=top_k, max_new=max_new,
+                          budget=n_max if budget is None else budget)

@@ -23,6 +23,10 @@ Sources (the three pages on EAGLE speculative decoding):
   * "EAGLE" study note (estelledc.github.io), case 3: accept a candidate the
     target finds likely, otherwise reject with the difference probability and
     resample; case 1: k drafted hits advance k+1 tokens.
+  * Tech Radar section 2 again for the drafting loop before verification
+    (step 0): per depth (4-6) the entropy H = -sum P log P of the draft
+    distribution is scored, then beam search prunes the low branches; low
+    entropy extends one branch, high entropy widens up to 8 nodes.
 
 Readings where the pages are silent (each one is listed in the design notes):
   * multi-child rule: children are tried in ascending node index with the
@@ -34,6 +38,11 @@ Readings where the pages are silent (each one is listed in the design notes):
   * GQA: query head h reads KV head h // (Hq / Hkv);
   * scale is given by the caller (1/sqrt(D) in every workload); the
     log-sum-exp is in natural log.
+  * tree expansion: a frontier node gets round(e^H) children (natural log,
+    clamped to [1, top_k]); candidates are its most probable tokens scored by
+    cumulative log-probability; per level the best min(max_new, budget -
+    n_nodes) are kept (equal scores: lower parent, then lower rank) and
+    appended in (parent, rank) order.
 
 Every function here is pinned by tests in ``tests/test_oracle_*.py`` against
 facts that do not come from this file (library routines, closed forms,
@@ -425,3 +434,174 @@ def kv_commit_path(k_layers, v_layers, page_table, prefix_len, n_nodes, accept_l
             slots[b, k] = int(page_table[b, pos // page_size]) * page_size + pos % page_size
         new_len[b] = L + a + 1
     return k_new, v_new, slots, new_len, status
+
+
+# --------------------------------------------------------------------------
+# step 0: dynamic tree expansion (the drafting loop before verification)
+# --------------------------------------------------------------------------
+NEAR_EXPAND = 1e-4
+
+
+def draft_entropy(z):
+    """H = -sum_i P(x_i) log P(x_i) with P = softmax(z), natural log (Tech
+    Radar section 2, "Dynamic Tree-Attention Masking", the entropy of the
+    draft distribution).  Terms with P = 0 contribute 0."""
+    x = np.asarray(z, dtype=np.float64)
+    x = x - np.max(x)
+    log_p = x - np.log(np.sum(np.exp(x)))
+    p = np.exp(log_p)
+    return float(-np.sum(np.where(p > 0.0, p * log_p, 0.0)))
+
+
+def branch_width(H, top_k):
+    """Children a frontier node gets: round(e^H) clamped to [1, top_k].
+
+    Reading of the same passage: low entropy extends a single branch, high
+    entropy widens the tree up to 8 nodes.  e^H is the perplexity, the number
+    of equally likely tokens with the same entropy, so the plainest continuous
+    rule is its nearest integer.  The step from w to w + 1 children sits at
+    H = ln(w + 1/2); the width is 1 plus the number of those thresholds
+    (w = 1 .. top_k - 1) that H reaches.
+    """
+    w = 1
+    for j in range(1, top_k):
+        if H >= np.log(j + 0.5):
+            w = j + 1
+    return w
+
+
+def top_tokens(z, w):
+    """The w most probable tokens of a draft row, most probable first; equal
+    logits in ascending token id (top-k expansion of the drafter): w rounds
+    of taking the first maximum among the tokens not yet taken."""
+    z = np.array(z, dtype=np.float64, copy=True)
+    picked = []
+    for _ in range(min(w, len(z))):
+        t = int(np.argmax(z))                 # first index of the maximum
+        picked.append(t)
+        z[t] = -np.inf
+    return picked
+
+
+def log_softmax_at(z, t):
+    """log P(t) for P = softmax(z), in fp64."""
+    x = np.asarray(z, dtype=np.float64)
+    m = np.max(x)
+    return float(x[t] - m - np.log(np.sum(np.exp(x - m))))
+
+
+def tree_expand_level(draft_logits, parents, tokens, scores, n_nodes, level_start, top_k, max_new,
+                      budget):
+    """One level of the dynamic expansion loop (Tech Radar section 2, sequence
+    diagram: per depth, the drafter scores entropy, then beam search prunes
+    the low branches; the tree holds at most 64 nodes).
+
+    State per request b: nodes [0, n_nodes[b]) with parents, tokens and
+    cumulative log-probabilities ``scores``; the frontier is the last level
+    added, nodes [level_start[b], n_nodes[b]).  Draft row f of
+    ``draft_logits[b]`` is the drafter's distribution over the children of
+    node f (the same row later serves as the q row of verification).
+
+    For each frontier node f (ascending): P = softmax(draft row f),
+    H_f = draft_entropy, w_f = branch_width(H_f, top_k); its top w_f tokens
+    are candidates (f, r, token, score_f + log P(token)).  Beam step: of all
+    candidates the best  keep = min(max_new, budget - n_nodes, count)  by
+    score are kept (equal scores: lower f, then lower rank r) and appended as
+    nodes n_nodes, n_nodes + 1, ... in (f, r) order, so parents precede
+    children and siblings are contiguous, most probable first.  Afterwards
+    level_start = old n_nodes and n_nodes grows by ``keep``.
+
+    An invalid state (not 1 <= n_nodes <= n_max, or not 0 <= level_start <=
+    n_nodes) leaves the request unchanged with STATUS_BAD_TREE.
+
+    Returns dict(parents, tokens, scores, n_nodes, level_start: the new state
+    (copies), entropy / width: per frontier node (NaN / 0 elsewhere), status,
+    near_boundary: some entropy lies within NEAR_EXPAND of a width threshold
+    or the last kept and first dropped scores are within NEAR_EXPAND, where a
+    rounding difference may legitimately change the result).
+    """
+    parents = np.array(parents, dtype=np.int32, copy=True)
+    tokens = np.array(tokens, dtype=np.int32, copy=True)
+    scores = np.array(scores, dtype=np.float64, copy=True)
+    n_nodes = np.array(n_nodes, dtype=np.int32, copy=True)
+    level_start = np.array(level_start, dtype=np.int32, copy=True)
+    B, n_max = parents.shape
+    entropy = np.full((B, n_max), np.nan)
+    width = np.zeros((B, n_max), dtype=np.int32)
+    status = np.zeros(B, dtype=np.int32)
+    near = np.zeros(B, dtype=bool)
+    for b in range(B):
+        n, ls = int(n_nodes[b]), int(level_start[b])
+        if not (1 <= n <= n_max and 0 <= ls <= n):
+            status[b] = STATUS_BAD_TREE
+            continue
+        cands = []                                   # (score, f, r, token)
+        for f in range(ls, n):
+            row = draft_logits[b, f]
+            H = draft_entropy(row)
+            w = branch_width(H, top_k)
+            entropy[b, f], width[b, f] = H, w
+            for j in range(1, top_k):
+                if abs(H - np.log(j + 0.5)) < NEAR_EXPAND:
+                    near[b] = True
+            for r, t in enumerate(top_tokens(row, w)):
+                cands.append((float(scores[b, f]) + log_softmax_at(row, t), f, r, t))
+        keep = max(0, min(max_new, budget - n, len(cands)))
+        # beam: repeatedly take the best remaining candidate
+        remaining = list(cands)
+        chosen = []
+        for _ in range(keep):
+            best = 0
+            for k in range(1, len(remaining)):
+                s, f, r, _t = remaining[k]
+                sb, fb, rb, _tb = remaining[best]
+                if s > sb or (s == sb and (f, r) < (fb, rb)):
+                    best = k
+            chosen.append(remaining.pop(best))
+        if chosen and remaining:
+            first_out = max(c[0] for c in remaining)
+            if abs(chosen[-1][0] - first_out) < NEAR_EXPAND * max(1.0, abs(first_out)):
+                near[b] = True
+        chosen.sort(key=lambda c: (c[1], c[2]))
+        for k, (s, f, _r, t) in enumerate(chosen):
+            parents[b, n + k] = f
+            tokens[b, n + k] = t
+            scores[b, n + k] = s
+        level_start[b] = n
+        n_nodes[b] = n + keep
+    return dict(parents=parents, tokens=tokens, scores=scores, n_nodes=n_nodes,
+                level_start=level_start, entropy=entropy, width=width, status=status,
+                near_boundary=near)
+
+
+def tree_build_dynamic(draft_logits, root_tokens, n_levels, top_k, max_new, budget):
+    """The whole expansion loop: a root per request (token root_tokens[b],
+    score 0), then ``n_levels`` calls of tree_expand_level (depth 4-6 in the
+    pages).  draft_logits [B, n_max, V] holds the drafter's row for every node
+    id that may be created.  Returns the final state of tree_expand_level
+    with near_boundary OR-ed over the levels and entropy / width of every
+    expanded node."""
+    B, n_max, _V = draft_logits.shape
+    parents = np.full((B, n_max), -1, dtype=np.int32)
+    tokens = np.zeros((B, n_max), dtype=np.int32)
+    tokens[:, 0] = np.asarray(root_tokens, dtype=np.int32)
+    scores = np.zeros((B, n_max), dtype=np.float64)
+    n_nodes = np.ones(B, dtype=np.int32)
+    level_start = np.zeros(B, dtype=np.int32)
+    entropy = np.full((B, n_max), np.nan)
+    width = np.zeros((B, n_max), dtype=np.int32)
+    near = np.zeros(B, dtype=bool)
+    status = np.zeros(B, dtype=np.int32)
+    for _ in range(n_levels):
+        out = tree_expand_level(draft_logits, parents, tokens, scores, n_nodes, level_start, top_k,
+                                max_new, budget)
+        parents, tokens, scores = out["parents"], out["tokens"], out["scores"]
+        n_nodes, level_start = out["n_nodes"], out["level_start"]
+        got = ~np.isnan(out["entropy"])
+        entropy[got] = out["entropy"][got]
+        width[got] = out["width"][got]
+        near |= out["near_boundary"]
+        status |= out["status"]
+    return dict(parents=parents, tokens=tokens, scores=scores, n_nodes=n_nodes,
+                level_start=level_start, entropy=entropy, width=width, status=status,
+                near_boundary=near)
