@@ -204,6 +204,76 @@ def profile_attn(args, W, tvb, dev):
                       "status": status.cpu().numpy().tolist(), "kv_bytes": int(w.k_bits.nbytes * 2)}))
 
 
+def time_expand(args, W, tvb, torch, np, dev, stream, B, n_max, V, cfg):
+    """Dynamic tree construction on its own: `levels` launches of
+    tv_tree_expand per tree over seeded drafter rows of the workload's batch and
+    vocabulary, each tree from a fresh root; rotated logits copies keep the
+    rows out of L2.  The state reset (one device copy per tree) is timed
+    separately and subtracted."""
+    levels, top_k, max_new = 6, 8, 16
+    ew = W.make_expand_workload(B, n_max, V, seed=cfg.seed, n_levels=levels, top_k=top_k, max_new=max_new,
+                                sigma_flat=cfg.sigma)
+    Bn = B * n_max
+    init = torch.zeros(4 * Bn + 3 * B, dtype=torch.int32)
+    init[0:Bn] = -1                                                  # parents
+    init[Bn:2 * Bn].view(B, n_max)[:, 0] = torch.from_numpy(ew.root_tokens)
+    init[4 * Bn:4 * Bn + B] = 1                                      # n_nodes
+    init = init.to(dev)
+    RE = min(64, max(1, math.ceil(3 * L2_BYTES / ew.draft_logits.nbytes)))
+    logits0 = torch.from_numpy(ew.draft_logits).to(dev)
+    copies = []
+    for _ in range(RE):
+        st = init.clone()
+        copies.append(dict(logits=logits0.clone(), state=st, parents=st[0:Bn].view(B, n_max),
+                           tokens=st[Bn:2 * Bn].view(B, n_max), scores=st[2 * Bn:3 * Bn].view(torch.float32).view(B, n_max),
+                           width=st[3 * Bn:4 * Bn].view(B, n_max), n_nodes=st[4 * Bn:4 * Bn + B],
+                           level_start=st[4 * Bn + B:4 * Bn + 2 * B], status=st[4 * Bn + 2 * B:],
+                           ws=tvb.new_expand_workspace(B, max_new, V, dev)))
+    del logits0
+
+    def build(ec):
+        for _ in range(levels):
+            tvb.tree_expand(ec["logits"], ec["parents"], ec["tokens"], ec["scores"], ec["n_nodes"], ec["level_start"],
+                            ec["status"], top_k=top_k, max_new=max_new, budget=n_max, max_frontier=max_new,
+                            width=ec["width"], workspace=ec["ws"])
+
+    for ec in copies:
+        ec["state"].copy_(init)
+        build(ec)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(dev)
+    g_all, g_rst = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g_all, stream=side):
+            for ec in copies:
+                ec["state"].copy_(init)
+                build(ec)
+        with torch.cuda.graph(g_rst, stream=side):
+            for ec in copies:
+                ec["state"].copy_(init)
+    torch.cuda.synchronize()
+    reps = max(3, min(50, args.steps // RE + 1))
+    times = []
+    for gph in (g_all, g_rst):
+        gph.replay()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(reps):
+            gph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        times.append(t0.elapsed_time(t1) * 1000.0 / (reps * RE))
+    g_all.replay()                      # leave every copy holding a finished tree
+    torch.cuda.synchronize()
+    ec = copies[0]
+    rows_read = int((ec["width"] > 0).sum().item())
+    return {"us_per_tree": times[0] - times[1], "reset_us": times[1], "levels": levels, "top_k": top_k,
+            "max_new_per_level": max_new, "budget": n_max, "rows_read": rows_read,
+            "nodes": int(ec["n_nodes"].sum().item()), "bytes": rows_read * V * 4,
+            "status_ok": bool((ec["status"] == 0).all().item()),
+            "l2": f"{RE} rotated logits copies ({RE * ew.draft_logits.nbytes / 1e6:.0f} MB)"}
+
+
 def main():
     args = parse_args()
     if args.oracle_sample:
@@ -373,6 +443,7 @@ def main():
         com_graph.replay()
     y1.record(stream)
     torch.cuda.synchronize()
+    expand = time_expand(args, W, tvb, torch, np, dev, stream, B, n_max, V, cfg)
     clk = clocks.stop()
     attn_us = a0.elapsed_time(a1) * 1000.0 / (reps * R)
     ac_us = c0.elapsed_time(c1) * 1000.0 / (reps * R)
@@ -442,8 +513,9 @@ def main():
 
     nodes = float(np.sum(w.n_nodes))
     e2e_in = [e2e["ms_per_step"]] if e2e is not None else []
-    (step_ms, attn_us, ac_us, accept_us, commit_us, *e2e_out), (nodes_total,) = reduce_over_ranks(
-        [step_ms, attn_us, ac_us, accept_us, commit_us] + e2e_in, [nodes], dev)
+    (step_ms, attn_us, ac_us, accept_us, commit_us, expand_us, *e2e_out), (nodes_total,) = reduce_over_ranks(
+        [step_ms, attn_us, ac_us, accept_us, commit_us, expand["us_per_tree"]] + e2e_in, [nodes], dev)
+    expand["us_per_tree"] = expand_us
     if e2e is not None:
         e2e["ms_per_step"] = e2e_out[0]
         e2e["value"] = nodes_total / (e2e["ms_per_step"] / 1000.0)
@@ -493,6 +565,8 @@ def main():
         "commit": {"us": commit_us, "layers": layers, "moved_rows_per_layer_head": moved,
                    "bytes": commit_bytes, "hbm_us": commit_bytes / (hbm * 1e3)},
         "nodes_per_s_attn_accept_commit": nodes_total / ((attn_us + accept_us + commit_us) * 1e-6),
+        "expand": dict(expand, us_per_level=expand_us / expand["levels"],
+                       hbm_us=expand["bytes"] / (hbm * 1e3), hbm_frac=expand["bytes"] / (hbm * 1e3) / expand_us),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json)",
                      "algorithmic": {"bytes": abytes, "flops": aflops}},

@@ -46,6 +46,8 @@ _SIGNATURES = {
     "tv_tree_accept_workspace": (_SZ, [_I, _I, _I]),
     "tv_tree_accept": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "tv_kv_commit_path": (_I, [_P, _P, _I, _I64, _I64, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "tv_tree_expand_workspace": (_SZ, [_I, _I, _I]),
+    "tv_tree_expand": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _P]),
     "tv_selftest_wait_timeout": (_I, [_P, _P]),
     "tv_last_error": (ctypes.c_char_p, []),
     "tv_version": (ctypes.c_char_p, []),
@@ -225,6 +227,42 @@ def kv_commit_path(k_cache: torch.Tensor, v_cache: torch.Tensor, page_table: tor
         _ptr(new_len), _ptr(status), _stream(dev))
     _check(rc, "tv_kv_commit_path")
     return slots, new_len
+
+
+def tree_expand_workspace_bytes(B, max_frontier, V) -> int:
+    return int(load_library().tv_tree_expand_workspace(B, max_frontier, V))
+
+
+def new_expand_workspace(B, max_frontier, V, device) -> torch.Tensor:
+    """A zero-filled workspace for tv_tree_expand, reusable for later calls of
+    the same sizes on the same stream."""
+    return torch.zeros(tree_expand_workspace_bytes(B, max_frontier, V), dtype=torch.uint8, device=device)
+
+
+def tree_expand(draft_logits: torch.Tensor, parents: torch.Tensor, tokens: torch.Tensor, scores: torch.Tensor,
+                n_nodes: torch.Tensor, level_start: torch.Tensor, status: torch.Tensor, *, top_k: int,
+                max_new: int, budget: int, max_frontier: Optional[int] = None, entropy=None, width=None,
+                workspace=None):
+    """One level of dynamic tree construction; updates parents, tokens,
+    scores, n_nodes and level_start in place.  Returns (entropy, width) of the
+    frontier rows (tensors the caller passed, else None)."""
+    B, n_max, V = draft_logits.shape
+    _expect(draft_logits, torch.float32, (B, n_max, V), "draft_logits")
+    _expect(parents, torch.int32, (B, n_max), "parents")
+    _expect(tokens, torch.int32, (B, n_max), "tokens")
+    _expect(scores, torch.float32, (B, n_max), "scores")
+    _expect(n_nodes, torch.int32, (B,), "n_nodes")
+    _expect(level_start, torch.int32, (B,), "level_start")
+    if max_frontier is None:
+        max_frontier = max(1, min(max_new, n_max))
+    if workspace is None:
+        workspace = new_expand_workspace(B, max_frontier, V, draft_logits.device)
+    rc = load_library().tv_tree_expand(
+        _ptr(draft_logits), _ptr(parents), _ptr(tokens), _ptr(scores), _ptr(n_nodes), _ptr(level_start),
+        _ptr(entropy), _ptr(width), B, n_max, V, int(top_k), int(max_new), int(budget), int(max_frontier),
+        _ptr(workspace), workspace.numel(), _ptr(status), _stream(draft_logits.device))
+    _check(rc, "tv_tree_expand")
+    return entropy, width
 
 
 def version() -> str:

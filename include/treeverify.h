@@ -65,6 +65,65 @@ extern "C" {
 #define TV_DEV_BAD_TOKEN 16   /* a drafted token id is outside [0, V)                              */
 
 /*
+ * Workspace size in bytes that tv_tree_expand needs for B requests, frontiers
+ * of at most max_frontier nodes and vocabulary V: per-slice partials of every
+ * frontier row (80 bytes per 8192-logit slice) plus one arrival counter per
+ * request.  The workspace (16-byte aligned) must be zero-filled before its
+ * first use; every call leaves the counters at zero again, so one workspace
+ * serves any number of calls issued in order on one stream.
+ */
+size_t tv_tree_expand_workspace(int B, int max_frontier, int V);
+
+/*
+ * tv_tree_expand — one level of dynamic draft-tree construction, the drafting
+ * loop that builds the tree the other calls verify ("SGLang EAGLE-2
+ * Speculative Decoding" (Tech Radar), section 2: per expansion depth the
+ * drafter's distribution is scored by its entropy H = -sum P log P, natural
+ * log ("Dynamic Tree-Attention Masking"); low entropy extends one branch,
+ * high entropy widens the tree up to 8 children; beam search prunes the low
+ * branches (sequence diagram); the tree holds at most 64 nodes).
+ *
+ * State per request b (updated in place): nodes [0, n_nodes[b]) with parents,
+ * tokens and cumulative log-probabilities `scores`; the frontier is the last
+ * level added, nodes [level_start[b], n_nodes[b]).  Start a tree with
+ * n_nodes = 1, level_start = 0, parents[0] = -1, tokens[0] = the last verified
+ * token, scores[0] = 0, then call once per depth (4-6 in the pages).
+ *
+ * For each frontier node f: P = softmax(draft_logits[b][f]);
+ * w_f = round(e^H) clamped to [1, top_k] (H at or above ln(j + 1/2) gives more
+ * than j children); candidates are f's w_f most probable tokens (equal logits:
+ * lower token id first) with score scores[f] + log P(token).  The best
+ * keep = min(max_new, budget - n_nodes[b], candidates) by score (equal scores:
+ * lower f, then lower rank) become nodes n_nodes[b] .. n_nodes[b] + keep - 1,
+ * in (f, rank) order: parents precede children, siblings are contiguous, most
+ * probable first.  Then level_start[b] = old n_nodes[b] and n_nodes[b] += keep
+ * (keep = 0 leaves an empty frontier).  Entries past the old n_nodes[b] are
+ * written only up to the new n_nodes[b].
+ *
+ *  draft_logits float [B, n_max, V]  row f = the drafter's logits for the
+ *    children of node f (finite values; only frontier rows are read).  The
+ *    same rows are the q rows tv_tree_accept takes when sampling.
+ *  parents, tokens  int32 [B, n_max]  in/out
+ *  scores   float [B, n_max]  in/out, cumulative natural-log probability
+ *  n_nodes, level_start  int32 [B]  in/out
+ *  entropy  float [B, n_max]  out (may be NULL): H of each frontier row
+ *  width    int32 [B, n_max]  out (may be NULL): w_f of each frontier row
+ *  top_k    1..8 (largest branching); max_new >= 1 (nodes one level may add);
+ *  budget   1..n_max (node cap of the tree); max_frontier 1..n_max: an upper
+ *    bound on every request's frontier (max_new, or 1 for the first level)
+ *  ws, ws_bytes  workspace of at least tv_tree_expand_workspace(B,
+ *    max_frontier, V) bytes
+ *  status   int32 [B]  in/out: requests with non-zero status are skipped;
+ *    an invalid state (n_nodes not in [1, n_max] or level_start not in
+ *    [0, n_nodes]) ORs TV_DEV_BAD_TREE and a frontier larger than
+ *    max_frontier ORs TV_DEV_CAPACITY; the state is then left unchanged.
+ */
+int tv_tree_expand(const float* draft_logits, int32_t* parents, int32_t* tokens, float* scores, int32_t* n_nodes,
+                   int32_t* level_start, float* entropy, int32_t* width, int B, int n_max, int V, int top_k,
+                   int max_new, int budget, int max_frontier, void* ws, size_t ws_bytes, int32_t* status,
+                   void* stream);
+
+/*
  * tv_tree_build_mask — the tree-attention mask (Tech Radar section 2, the mask
  * M: bit j of anc_mask[b][i] is set iff node j is an ancestor of node i or i
  * itself) and each node's depth (root = 0; RoPE positions are L + depth).
