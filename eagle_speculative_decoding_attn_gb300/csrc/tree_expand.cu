@@ -14,12 +14,19 @@
 // candidates by score (equal scores: lower f, then lower rank) are appended in
 // (f, rank) order, so parents precede children and siblings are contiguous.
 //
-// One launch per level.  CTA (slice, frontier row, request) reduces an
-// 8192-logit slice of one draft row to (max, sum e^(x-max), sum e^(x-max)(x-max))
-// and its 8 largest logits; the last CTA of a request (arrival counter) merges
-// the slices of every frontier row, takes the widths and the beam selection
-// in shared memory and appends the nodes.  The logits are read once, in
-// coalesced 16-byte loads: the kernel is bound by HBM.
+// One launch per level.  A work item is one 8192-logit slice of one frontier
+// row; it is reduced to (max, sum e^(x-max), sum e^(x-max)(x-max)) and its 8
+// largest logits.  The last item of a request to finish (arrival counter)
+// merges the slices of every frontier row, takes the widths and the beam
+// selection in shared memory and appends the nodes.  The logits are read once:
+// the kernel is bound by HBM.
+//
+// One CTA per potential item (slice, frontier row, request) loads its slice
+// straight into registers (16-byte loads when V is a multiple of 4); four CTAs
+// share an SM so that the loads of some overlap the reductions of others.
+// (A persistent form that staged slices through a shared-memory ring with the
+// bulk-copy engine measured slower: its per-slice reduction, barriers and
+// arrival are a serial latency chain that two resident CTAs did not hide.)
 #include <cfloat>
 #include <climits>
 
@@ -32,6 +39,7 @@ constexpr int kExpPerThread = 32;                        // logits per thread an
 constexpr int kExpSlice = kExpThreads * kExpPerThread;   // 8192
 constexpr int kExpTop = 8;                               // widest branching (width <= 8)
 constexpr int kSliceCand = 256;                          // threshold candidates of a slice
+constexpr int kExpWarps = kExpThreads / 32;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct __align__(16) ExpPart {  // one slice of one draft row
@@ -53,6 +61,26 @@ struct ExpandParams {
   ExpPart* part;      // [B][max_frontier][n_slices]
   int32_t* tickets;   // [B] arrivals of this call (zero between calls)
   int32_t* status;
+};
+
+struct ExpShared {
+  float red_m[kExpWarps], red_s[kExpWarps], red_t[kExpWarps], wmax[kExpWarps];
+  float wtop_v[kExpWarps][kExpTop];
+  int wtop_i[kExpWarps][kExpTop];
+  float top_v[kExpTop];
+  int top_i[kExpTop];
+  float cand_v[kSliceCand];
+  int cand_i[kSliceCand];
+  int cand_n;
+  int last;
+  // merge of a request
+  float row_c[kMaxNodes][kExpTop];
+  int row_tok[kMaxNodes][kExpTop];
+  int row_w[kMaxNodes];
+  int row_off[kMaxNodes + 1];
+  float mc[kMaxNodes * kExpTop];
+  int mkey[kMaxNodes * kExpTop];
+  int sel_cnt[2][kExpWarps];
 };
 
 // (v1, i1) ranks before (v2, i2): larger logit, then lower token id.
@@ -146,130 +174,93 @@ __device__ __forceinline__ void warp_mst(float& m, float& s, float& t) {
   }
 }
 
-__global__ void __launch_bounds__(kExpThreads) tree_expand_kernel(const ExpandParams p) {
-  constexpr int kWarps = kExpThreads / 32;
-  constexpr int kCand = kMaxNodes * kExpTop;  // 512 candidates at most
-  __shared__ float red_m[kWarps], red_s[kWarps], red_t[kWarps];
-  __shared__ float wtop_v[kWarps][kExpTop];
-  __shared__ int wtop_i[kWarps][kExpTop];
-  __shared__ int last_sh;
-  __shared__ float row_c[kMaxNodes][kExpTop];
-  __shared__ int row_tok[kMaxNodes][kExpTop];
-  __shared__ int row_w[kMaxNodes];
-  __shared__ int row_off[kMaxNodes + 1];
-  __shared__ float cand_c[kCand];
-  __shared__ int cand_key[kCand];
-  __shared__ int sel_cnt[2][kWarps];
-  __shared__ float cand_v[kSliceCand];
-  __shared__ int cand_i[kSliceCand];
-  __shared__ int cand_n;
-  __shared__ float wmax_sh[kWarps];
-  __shared__ float top_v_sh[kExpTop];
-  __shared__ int top_i_sh[kExpTop];
+// Thread's 32 logits of a slice: element (u, c) is logit lo + 4 * (u * 256 +
+// tid) + c, so token ids rise along u and c and equal logits keep the lower id
+// first; entries past hi are -inf.
+__device__ __forceinline__ int slice_j(int lo, int u, int c) { return lo + 4 * (u * kExpThreads + threadIdx.x) + c; }
 
-  const int sl = blockIdx.x, y = blockIdx.y, b = blockIdx.z;
+// Reduce one slice (x in registers) to its part and store it at dst (thread 0
+// writes it; it publishes the part with a fence before arriving).
+__device__ __forceinline__ void slice_reduce(ExpShared& sh, const float (&x)[kExpPerThread], bool work, int lo,
+                                             int hi, ExpPart* dst) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n_max = p.n_max, V = p.V;
-  griddep_wait();
-  const int st = p.status[b];
-  const int n = p.n_nodes[b], ls = p.level_start[b];
-  const bool ok = st == 0 && n >= 1 && n <= n_max && ls >= 0 && ls <= n;
-  const int F = ok ? n - ls : 0;
-  const bool work = ok && y < F && F <= p.max_frontier && n < p.budget;
-
-  // ---- this CTA's slice of draft row ls + y
   float m = -INFINITY, s = 0.f, t = 0.f;
-  float x[kExpPerThread];
-  int lo = 0, hi = 0;
-  if (tid == 0) cand_n = 0;
   if (work) {
-    const float* row = p.logits + ((int64_t)b * n_max + ls + y) * V;
-    lo = sl * kExpSlice;
-    hi = min(V, lo + kExpSlice);
-    // element (u, c) of a thread is logit lo + 4 * (u * 256 + tid) + c: token
-    // ids rise along u and c, so equal logits keep the lower id first
-    if ((V & 3) == 0) {
-      const float4* r4 = reinterpret_cast<const float4*>(row + lo);
+    // four independent chains for the maximum and the two sums
+    float m4[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-      for (int u = 0; u < kExpPerThread / 4; ++u) {
-        const int e = 4 * (u * kExpThreads + tid);
-        const float4 q = lo + e < hi ? __ldcs(r4 + u * kExpThreads + tid)
-                                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        x[4 * u] = q.x;
-        x[4 * u + 1] = q.y;
-        x[4 * u + 2] = q.z;
-        x[4 * u + 3] = q.w;
-      }
-    } else {
-#pragma unroll
-      for (int u = 0; u < kExpPerThread / 4; ++u)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int j = lo + 4 * (u * kExpThreads + tid) + c;
-          x[4 * u + c] = j < hi ? __ldcs(row + j) : -INFINITY;
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < kExpPerThread; ++k) m = fmaxf(m, x[k]);
+    for (int k = 4; k < kExpPerThread; ++k) m4[k & 3] = fmaxf(m4[k & 3], x[k]);
+    m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+    float s4[4] = {0.f, 0.f, 0.f, 0.f}, t4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < kExpPerThread; ++k) {
       // d >= -200 keeps e * d finite: e is then 0 (also when the thread saw
       // no logit and m = -inf, where x - m is NaN and fmaxf takes -200)
       const float d = fmaxf(x[k] - m, -200.f);
       const float e = ex2_approx(d * kLog2e);
-      s += e;
-      t = fmaf(e, d, t);
+      s4[k & 3] += e;
+      t4[k & 3] = fmaf(e, d, t4[k & 3]);
     }
+    s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    t = (t4[0] + t4[1]) + (t4[2] + t4[3]);
     if (s == 0.f) m = -INFINITY;
   }
   // Each warp's largest logit is a distinct logit, so with 8 warps the
   // slice's 8 best are all >= tau, the smallest warp maximum: only logits
-  // >= tau are candidates (a warp without logits makes tau = -inf).
-  float wm = m;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+  // >= tau are candidates (a warp without logits makes tau = -inf).  After
+  // the warp's (m, s, t) merge, m is that maximum.
   warp_mst(m, s, t);
   if (lane == 0) {
-    red_m[warp] = m;
-    red_s[warp] = s;
-    red_t[warp] = t;
-    wmax_sh[warp] = wm;
+    sh.red_m[warp] = m;
+    sh.red_s[warp] = s;
+    sh.red_t[warp] = t;
+    sh.wmax[warp] = m;
   }
-  if (tid < kExpTop) {
-    top_v_sh[tid] = -INFINITY;
-    top_i_sh[tid] = INT_MAX;
+  if (tid == 0) {  // the thread that reads the previous slice's list
+#pragma unroll
+    for (int k = 0; k < kExpTop; ++k) {
+      sh.top_v[k] = -INFINITY;
+      sh.top_i[k] = INT_MAX;
+    }
   }
   __syncthreads();
+  if (warp == 0) {  // the slice's (m, s, t)
+    m = lane < kExpWarps ? sh.red_m[lane] : -INFINITY;
+    s = lane < kExpWarps ? sh.red_s[lane] : 0.f;
+    t = lane < kExpWarps ? sh.red_t[lane] : 0.f;
+    warp_mst(m, s, t);
+  }
   float tau = INFINITY;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) tau = fminf(tau, wmax_sh[w]);
+  for (int w = 0; w < kExpWarps; ++w) tau = fminf(tau, sh.wmax[w]);
   if (work) {
 #pragma unroll
     for (int u = 0; u < kExpPerThread / 4; ++u)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int j = lo + 4 * (u * kExpThreads + tid) + c;
+        const int j = slice_j(lo, u, c);
         if (j < hi && x[4 * u + c] >= tau) {
-          const int slot = atomicAdd(&cand_n, 1);
+          const int slot = atomicAdd(&sh.cand_n, 1);
           if (slot < kSliceCand) {
-            cand_v[slot] = x[4 * u + c];
-            cand_i[slot] = j;
+            sh.cand_v[slot] = x[4 * u + c];
+            sh.cand_i[slot] = j;
           }
         }
       }
   }
   __syncthreads();
-  const int nc = cand_n;
+  const int nc = sh.cand_n;
   if (nc <= kSliceCand) {
     // a candidate's rank among the candidates; ranks 0..7 are the slice's 8 best
     if (tid < nc) {
-      const float v = cand_v[tid];
-      const int i = cand_i[tid];
+      const float v = sh.cand_v[tid];
+      const int i = sh.cand_i[tid];
       int rank = 0;
-      for (int c = 0; c < nc; ++c) rank += top_before(cand_v[c], cand_i[c], v, i);
+#pragma unroll 4
+      for (int c = 0; c < nc; ++c) rank += top_before(sh.cand_v[c], sh.cand_i[c], v, i);
       if (rank < kExpTop) {
-        top_v_sh[rank] = v;
-        top_i_sh[rank] = i;
+        sh.top_v[rank] = v;
+        sh.top_i[rank] = i;
       }
     }
   } else {
@@ -282,7 +273,7 @@ __global__ void __launch_bounds__(kExpThreads) tree_expand_kernel(const ExpandPa
       for (int u = 0; u < kExpPerThread / 4; ++u)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int j = lo + 4 * (u * kExpThreads + tid) + c;
+          const int j = slice_j(lo, u, c);
           if (j < hi) top_insert(tv_, ti_, x[4 * u + c], j);
         }
     }
@@ -290,35 +281,30 @@ __global__ void __launch_bounds__(kExpThreads) tree_expand_kernel(const ExpandPa
     if (lane == 0) {
 #pragma unroll
       for (int k = 0; k < kExpTop; ++k) {
-        wtop_v[warp][k] = ov[k];
-        wtop_i[warp][k] = oi[k];
+        sh.wtop_v[warp][k] = ov[k];
+        sh.wtop_i[warp][k] = oi[k];
       }
     }
     __syncthreads();
     if (warp == 0) {
 #pragma unroll
       for (int k = 0; k < kExpTop; ++k) {
-        tv_[k] = lane < kWarps ? wtop_v[lane][k] : -INFINITY;
-        ti_[k] = lane < kWarps ? wtop_i[lane][k] : INT_MAX;
+        tv_[k] = lane < kExpWarps ? sh.wtop_v[lane][k] : -INFINITY;
+        ti_[k] = lane < kExpWarps ? sh.wtop_i[lane][k] : INT_MAX;
       }
       warp_top8(tv_, ti_, ov, oi);
       if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < kExpTop; ++k) {
-          top_v_sh[k] = ov[k];
-          top_i_sh[k] = oi[k];
+          sh.top_v[k] = ov[k];
+          sh.top_i[k] = oi[k];
         }
       }
     }
   }
   __syncthreads();
   if (warp == 0) {
-    m = lane < kWarps ? red_m[lane] : -INFINITY;
-    s = lane < kWarps ? red_s[lane] : 0.f;
-    t = lane < kWarps ? red_t[lane] : 0.f;
-    warp_mst(m, s, t);
     if (lane == 0) {
-      ExpPart* dst = p.part + ((int64_t)b * p.max_frontier + y) * p.n_slices + sl;
       ExpPart r;
       r.m = m;
       r.s = s;
@@ -326,41 +312,41 @@ __global__ void __launch_bounds__(kExpThreads) tree_expand_kernel(const ExpandPa
       r.pad = 0.f;
 #pragma unroll
       for (int k = 0; k < kExpTop; ++k) {
-        r.v[k] = top_v_sh[k];
-        r.i[k] = top_i_sh[k];
+        r.v[k] = sh.top_v[k];
+        r.i[k] = sh.top_i[k];
       }
       *dst = r;
-      __threadfence();
-      last_sh = atomicAdd(p.tickets + b, 1) == p.max_frontier * p.n_slices - 1;
     }
+  } else if (tid == 32) {
+    sh.cand_n = 0;  // every thread has read it; the next slice appends after its first barrier
+  }
+}
+
+// Thread 0 (the writer of this CTA's parts) publishes them and arrives `cnt`
+// times on request b's counter; returns (block-uniform) whether the request's
+// parts are now complete.
+__device__ __forceinline__ bool arrive(ExpShared& sh, int32_t* ticket, int cnt, int expected) {
+  if (threadIdx.x == 0) {
+    __threadfence();
+    sh.last = atomicAdd(ticket, cnt) + cnt == expected;
   }
   __syncthreads();
-  if (!last_sh) return;
-  __threadfence();
+  const bool last = sh.last;
+  if (last) __threadfence();
+  return last;
+}
 
-  // ---- the last CTA of request b
-  if (!ok || F > p.max_frontier) {
-    if (tid == 0) {
-      if (st == 0) atomicOr(p.status + b, ok ? TV_DEV_CAPACITY : TV_DEV_BAD_TREE);
-      p.tickets[b] = 0;
-    }
-    return;
-  }
-  const int room = p.budget - n;
-  if (F == 0 || room <= 0) {
-    if (tid == 0) {
-      p.level_start[b] = n;
-      p.tickets[b] = 0;
-    }
-    return;
-  }
-  // merge the slices of each frontier row: warp w takes rows w, w + 8, ...
+// The last arrival of request b: merge the parts of its F frontier rows
+// (state n, ls), take the widths and the beam cut, append the kept nodes at
+// n, n + 1, ...  Returns how many were appended.
+__device__ int request_merge(ExpShared& sh, const ExpandParams& p, int b, int n, int ls, int F) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_max = p.n_max;
   float tv_[kExpTop], ov[kExpTop];
   int ti_[kExpTop], oi[kExpTop];
-  for (int r = warp; r < F; r += kWarps) {
-    m = -INFINITY;
-    s = 0.f;
-    t = 0.f;
+  // warp w takes rows w, w + 8, ...
+  for (int r = warp; r < F; r += kExpWarps) {
+    float m = -INFINITY, s = 0.f, t = 0.f;
     top_clear(tv_, ti_);
     const ExpPart* src = p.part + ((int64_t)b * p.max_frontier + r) * p.n_slices;
     for (int q = lane; q < p.n_slices; q += 32) {
@@ -400,12 +386,12 @@ __global__ void __launch_bounds__(kExpThreads) tree_expand_kernel(const ExpandPa
       w = min(w, real);
       if (p.entropy) p.entropy[(int64_t)b * n_max + f] = H;
       if (p.width) p.width[(int64_t)b * n_max + f] = w;
-      row_w[r] = w;
+      sh.row_w[r] = w;
       const float sf = p.scores[(int64_t)b * n_max + f];
 #pragma unroll
       for (int k = 0; k < kExpTop; ++k) {
-        row_c[r][k] = sf + ((ov[k] - m) - lz);
-        row_tok[r][k] = oi[k];
+        sh.row_c[r][k] = sf + ((ov[k] - m) - lz);
+        sh.row_tok[r][k] = oi[k];
       }
     }
   }
@@ -413,22 +399,22 @@ __global__ void __launch_bounds__(kExpThreads) tree_expand_kernel(const ExpandPa
   if (tid == 0) {
     int acc = 0;
     for (int r = 0; r < F; ++r) {
-      row_off[r] = acc;
-      acc += row_w[r];
+      sh.row_off[r] = acc;
+      acc += sh.row_w[r];
     }
-    row_off[F] = acc;
+    sh.row_off[F] = acc;
   }
   __syncthreads();
-  const int C = row_off[F];
+  const int C = sh.row_off[F];
   for (int a = tid; a < F * kExpTop; a += kExpThreads) {
     const int r = a / kExpTop, k = a % kExpTop;
-    if (k < row_w[r]) {
-      cand_c[row_off[r] + k] = row_c[r][k];
-      cand_key[row_off[r] + k] = a;  // dense order = (row, rank) order
+    if (k < sh.row_w[r]) {
+      sh.mc[sh.row_off[r] + k] = sh.row_c[r][k];
+      sh.mkey[sh.row_off[r] + k] = a;  // dense order = (row, rank) order
     }
   }
   __syncthreads();
-  const int keep = min(min(p.max_new, room), C);
+  const int keep = min(min(p.max_new, p.budget - n), C);
   // rank of each candidate by score (equal scores: earlier in (row, rank)
   // order first); the best `keep` are appended in (row, rank) order
 #pragma unroll
@@ -436,30 +422,97 @@ __global__ void __launch_bounds__(kExpThreads) tree_expand_kernel(const ExpandPa
     const int d = h * kExpThreads + tid;
     bool sel = false;
     if (d < C) {
-      const float c = cand_c[d];
+      const float c = sh.mc[d];
       int rank = 0;
       for (int e = 0; e < C; ++e) {
-        const float ce = cand_c[e];
+        const float ce = sh.mc[e];
         rank += (ce > c) || (ce == c && e < d);
       }
       sel = rank < keep;
     }
     const unsigned bal = __ballot_sync(0xffffffffu, sel);
-    if (lane == 0) sel_cnt[h][warp] = __popc(bal);
+    if (lane == 0) sh.sel_cnt[h][warp] = __popc(bal);
     __syncthreads();
     if (sel) {
       int pos = __popc(bal & ((1u << lane) - 1u));
       for (int hh = 0; hh < h; ++hh)
-        for (int w = 0; w < kWarps; ++w) pos += sel_cnt[hh][w];
-      for (int w = 0; w < warp; ++w) pos += sel_cnt[h][w];
-      const int key = cand_key[d];
+        for (int w = 0; w < kExpWarps; ++w) pos += sh.sel_cnt[hh][w];
+      for (int w = 0; w < warp; ++w) pos += sh.sel_cnt[h][w];
+      const int key = sh.mkey[d];
       const int r = key / kExpTop, k = key % kExpTop;
       const int64_t o = (int64_t)b * n_max + n + pos;
       p.parents[o] = ls + r;
-      p.tokens[o] = row_tok[r][k];
-      p.scores[o] = row_c[r][k];
+      p.tokens[o] = sh.row_tok[r][k];
+      p.scores[o] = sh.row_c[r][k];
     }
   }
+  __syncthreads();  // the merge arrays may be reused by the next request
+  return keep;
+}
+
+// CTA (slice, frontier row, request).  Every CTA of a request arrives, live or
+// not, so the last one runs after every read of that request's state.
+__global__ void __launch_bounds__(kExpThreads, 4) tree_expand_kernel(const ExpandParams p) {
+  __shared__ ExpShared sh;
+  const int sl = blockIdx.x, y = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int n_max = p.n_max, V = p.V;
+  griddep_wait();
+  const int st = p.status[b];
+  const int n = p.n_nodes[b], ls = p.level_start[b];
+  const bool ok = st == 0 && n >= 1 && n <= n_max && ls >= 0 && ls <= n;
+  const int F = ok ? n - ls : 0;
+  const bool work = ok && y < F && F <= p.max_frontier && n < p.budget;
+  if (tid == 0) sh.cand_n = 0;
+
+  float x[kExpPerThread];
+  int lo = 0, hi = 0;
+  if (work) {
+    const float* row = p.logits + ((int64_t)b * n_max + ls + y) * V;
+    lo = sl * kExpSlice;
+    hi = min(V, lo + kExpSlice);
+    if ((V & 3) == 0) {
+      const float4* r4 = reinterpret_cast<const float4*>(row + lo);
+#pragma unroll
+      for (int u = 0; u < kExpPerThread / 4; ++u) {
+        const int e = 4 * (u * kExpThreads + tid);
+        const float4 q = lo + e < hi ? __ldcs(r4 + u * kExpThreads + tid)
+                                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        x[4 * u] = q.x;
+        x[4 * u + 1] = q.y;
+        x[4 * u + 2] = q.z;
+        x[4 * u + 3] = q.w;
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kExpPerThread / 4; ++u)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int j = slice_j(lo, u, c);
+          x[4 * u + c] = j < hi ? __ldcs(row + j) : -INFINITY;
+        }
+    }
+  }
+  ExpPart* dst = p.part + ((int64_t)b * p.max_frontier + y) * p.n_slices + sl;
+  slice_reduce(sh, x, work, lo, hi, dst);
+  if (!arrive(sh, p.tickets + b, 1, p.max_frontier * p.n_slices)) return;
+
+  // ---- the last CTA of request b
+  if (!ok || F > p.max_frontier) {
+    if (tid == 0) {
+      if (st == 0) atomicOr(p.status + b, ok ? TV_DEV_CAPACITY : TV_DEV_BAD_TREE);
+      p.tickets[b] = 0;
+    }
+    return;
+  }
+  if (F == 0 || n >= p.budget) {
+    if (tid == 0) {
+      p.level_start[b] = n;
+      p.tickets[b] = 0;
+    }
+    return;
+  }
+  const int keep = request_merge(sh, p, b, n, ls, F);
   if (tid == 0) {
     p.n_nodes[b] = n + keep;
     p.level_start[b] = n;

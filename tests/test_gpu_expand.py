@@ -245,3 +245,12 @@ def test_rows_with_many_equal_logits():
     st, near, rows_read = _grow_and_compare(wl, dev)
     assert np.all(st["status"] == 0)
     assert st["tokens"][0, 1:9].tolist() == list(range(8))     # uniform root row: the 8 lowest ids
+
+
+def test_large_batch():
+    """520 requests (grid z beyond a few hundred) on a small vocabulary."""
+    dev = require_gpu()
+    wl = W.make_expand_workload(520, 16, 2048, seed=21, n_levels=3, top_k=4, max_new=6)
+    st, near, rows = _grow_and_compare(wl, dev)
+    assert np.all(st["status"] == 0)
+    assert near <= 520 * 3 // 20
