@@ -47,6 +47,11 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-attn", type=int, default=0,
                     help="only run this many eager tv_tree_verify_attn calls (for profiler captures)")
+    ap.add_argument("--profile-expand", type=int, default=0,
+                    help="profiler capture mode: build N trees (6 levels each) with tv_tree_expand and exit")
+    ap.add_argument("--breakdown", action="store_true",
+                    help="print per-call times of every kernel on each verification workload (CUDA graphs of ten "
+                         "calls, L2-warm) and the 6-level expansion time, one JSON line per workload, and exit")
     ap.add_argument("--oracle-sample", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -274,6 +279,146 @@ def time_expand(args, W, tvb, torch, np, dev, stream, B, n_max, V, cfg):
             "l2": f"{RE} rotated logits copies ({RE * ew.draft_logits.nbytes / 1e6:.0f} MB)"}
 
 
+def profile_expand(args, W, tvb, dev):
+    """A small self-contained command for profiler captures: N eager tree
+    builds of 6 levels of dynamic expansion on the chosen config's batch and
+    vocabulary."""
+    import numpy as np
+    import torch
+    cfg = W.CONFIG_BY_NAME[args.config]
+    B, V, n_max = cfg.B, cfg.V, 64
+    ew = W.make_expand_workload(B, n_max, V, seed=cfg.seed, n_levels=6, sigma_flat=cfg.sigma)
+    logits = torch.from_numpy(ew.draft_logits).to(dev)
+    ws = tvb.new_expand_workspace(B, 16, V, dev)
+    for _ in range(args.profile_expand):
+        par = torch.full((B, n_max), -1, dtype=torch.int32, device=dev)
+        tok = torch.zeros((B, n_max), dtype=torch.int32, device=dev)
+        tok[:, 0] = torch.from_numpy(ew.root_tokens).to(dev)
+        sc = torch.zeros((B, n_max), dtype=torch.float32, device=dev)
+        n = torch.ones(B, dtype=torch.int32, device=dev)
+        ls = torch.zeros(B, dtype=torch.int32, device=dev)
+        st = torch.zeros(B, dtype=torch.int32, device=dev)
+        for _ in range(6):
+            tvb.tree_expand(logits, par, tok, sc, n, ls, st, top_k=8, max_new=16, budget=n_max, max_frontier=16,
+                            workspace=ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_expand": args.config, "trees": args.profile_expand,
+                      "n_nodes": n.cpu().numpy().tolist(), "status": st.cpu().numpy().tolist()}))
+
+
+def breakdown(args, W, tvb, dev):
+    """Per-call cost of each kernel inside CUDA graphs of ten calls (inputs
+    L2-warm) on the four Llama-shaped workloads, and six levels of tree
+    expansion on each workload's batch and vocabulary."""
+    import numpy as np
+    import torch
+    g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    bf = lambda b: g(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16)
+
+    def gtime(fn, n=10, reps=200):
+        fn()
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream(dev)
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(gr, stream=s):
+                for _ in range(n):
+                    fn()
+        torch.cuda.synchronize()
+        for _ in range(3):
+            gr.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            gr.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1000 / (reps * n)
+
+    hbm, tf_burst, _ = load_peaks()
+    for name in ("llama2_7b", "llama3_70b", "serving", "long"):
+        w = W.make_workload(name)
+        cfg = W.CONFIG_BY_NAME[name]
+        sampling = w.temperature > 0
+        parents, n_nodes, L, pt, tokens = g(w.parents), g(w.n_nodes), g(w.prefix_len), g(w.page_table), g(w.tokens)
+        target = g(w.target_logits)
+        draft = g(w.draft_logits) if sampling else None
+        ua = g(w.u_accept) if sampling else None
+        us = g(w.u_sample) if sampling else None
+        layers = cfg.n_layers_commit
+        k = bf(w.k_bits).unsqueeze(0).repeat(layers, 1, 1, 1, 1).contiguous()
+        v = bf(w.v_bits).unsqueeze(0).repeat(layers, 1, 1, 1, 1).contiguous()
+        q = bf(w.q_bits)
+        anc, depth, status = tvb.tree_build_mask(parents, n_nodes)
+        ws = tvb.new_attn_workspace(w.B, w.n_max, w.Hq, w.Hkv, w.D, dev)
+        aws = tvb.new_accept_workspace(w.B, w.n_max, w.V, dev)
+        out = torch.empty_like(q)
+        lse = torch.empty((w.B, w.n_max, w.Hq), dtype=torch.float32, device=dev)
+        t_mask = gtime(lambda: tvb.tree_build_mask(parents, n_nodes, anc_mask=anc, depth=depth, status=status))
+        t_attn = gtime(lambda: tvb.tree_verify_attn(q, k[0], v[0], pt, L, n_nodes, anc, w.scale, status, out=out,
+                                                    lse=lse, workspace=ws))
+        acc = tvb.tree_accept(target, draft, tokens, parents, n_nodes, anc, depth, w.temperature, ua, us, status,
+                              workspace=aws)
+        t_acc = gtime(lambda: tvb.tree_accept(target, draft, tokens, parents, n_nodes, anc, depth, w.temperature, ua,
+                                              us, status, outputs=acc, workspace=aws))
+        com = tvb.kv_commit_path(k, v, pt, L, n_nodes, acc[0], acc[1], status)
+        t_com = gtime(lambda: tvb.kv_commit_path(k, v, pt, L, n_nodes, acc[0], acc[1], status, outputs=com))
+        ok = bool((status == 0).all().item())
+        del k, v, target, draft
+        torch.cuda.empty_cache()
+        # six levels of expansion from a fresh root, the reset outside the graph
+        ew = W.make_expand_workload(w.B, 64, w.V, seed=cfg.seed, n_levels=6, sigma_flat=cfg.sigma)
+        logits = g(ew.draft_logits)
+        st = [torch.full((w.B, 64), -1, dtype=torch.int32, device=dev),
+              torch.zeros((w.B, 64), dtype=torch.int32, device=dev),
+              torch.zeros((w.B, 64), dtype=torch.float32, device=dev), torch.ones(w.B, dtype=torch.int32, device=dev),
+              torch.zeros(w.B, dtype=torch.int32, device=dev), torch.zeros(w.B, dtype=torch.int32, device=dev)]
+        st[1][:, 0] = g(ew.root_tokens)
+        wd = torch.zeros((w.B, 64), dtype=torch.int32, device=dev)
+        init = [x.clone() for x in st]
+        xws = tvb.new_expand_workspace(w.B, 16, w.V, dev)
+
+        def levels():
+            for _ in range(6):
+                tvb.tree_expand(logits, *st[:5], st[5], top_k=8, max_new=16, budget=64, max_frontier=16, width=wd,
+                                workspace=xws)
+        levels()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        sx = torch.cuda.Stream(dev)
+        with torch.cuda.stream(sx):
+            with torch.cuda.graph(gr, stream=sx):
+                levels()
+        ts = []
+        for _ in range(12):
+            for a, b in zip(st, init):
+                a.copy_(b)
+            wd.zero_()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            gr.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1000)
+        t_exp = float(np.median(ts[2:]))
+        rows = int((wd > 0).sum().item())
+        ok = ok and bool((st[5] == 0).all().item())
+        del logits
+        torch.cuda.empty_cache()
+        abytes, aflops = w.attn_bytes(), w.attn_flops()
+        t_roof = max(abytes / (hbm * 1e3), aflops / (tf_burst * 1e6))
+        print(json.dumps({
+            "workload": name, "status_ok": ok, "us_per_call": {
+                "mask": t_mask, "attn": t_attn, "accept": t_acc, "commit": t_com},
+            "attn_roofline_us": t_roof, "attn_bound": "hbm" if abytes / hbm >= aflops / tf_burst / 1e3 else "tensor",
+            "attn_roofline_frac": t_roof / t_attn, "accept_mode": "sampling" if sampling else "greedy",
+            "commit_layers": layers,
+            "expand_6_levels": {"us": t_exp, "rows_read": rows, "bytes": rows * w.V * 4,
+                                "tbps": rows * w.V * 4 / t_exp / 1e6}}), flush=True)
+
+
 def main():
     args = parse_args()
     if args.oracle_sample:
@@ -303,6 +448,10 @@ def main():
     tvb.load_library()
     if args.profile_attn:
         return profile_attn(args, W, tvb, dev)
+    if args.profile_expand:
+        return profile_expand(args, W, tvb, dev)
+    if args.breakdown:
+        return breakdown(args, W, tvb, dev)
 
     cfg = W.CONFIG_BY_NAME[args.config]
     w = W.make_workload(cfg)
