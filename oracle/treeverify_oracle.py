@@ -32,6 +32,9 @@ Readings where the pages are silent (each one is listed in the design notes):
   * multi-child rule: children are tried in ascending node index with the
     draft distribution q fixed; after a rejected child the target
     distribution is replaced by the normalised residual max(0, p - q);
+    for siblings drafted without replacement (distinct tokens, top-k trees)
+    the selectable variant also removes each rejected token from q and
+    renormalises it before the next sibling;
   * ties: argmax -> lowest vocab index; deepest accepted node -> lowest node
     index; inverse CDF -> first index j with u*S < C_j (strict);
   * temperature: softmax(z / T); T = 0 means greedy;
@@ -295,6 +298,38 @@ def node_plan(p, q, child_tokens):
     return cur_list, cur
 
 
+def node_plan_wor(p, q, child_tokens):
+    """The acceptance plan at one tree node for siblings drafted without
+    replacement (top-k style trees whose siblings are distinct tokens): as
+    ``node_plan``, but after child k with token x is rejected the draft is
+    also updated, q_{k+1} = q_k with x removed and renormalised (all zero if
+    nothing is left).  The target side is unchanged: cur_{k+1} = max(0,
+    cur_k - q_k) normalised, with q_k the draft child k was tested against.
+
+    Sequential rejection with q renormalised after each removal is the
+    standard recursive rejection sampling for draws without replacement: the
+    k-th sibling is a draw from q_k, so each step is an ordinary
+    speculative-sampling step against the current residual.
+
+    Returns (plans, final): plans[k] = (cur_k, q_k) for the k-th child and
+    ``final`` the distribution the bonus token is drawn from when every child
+    is rejected.
+    """
+    cur = np.asarray(p, dtype=np.float64)
+    qk = np.asarray(q, dtype=np.float64)
+    plans = []
+    for x in child_tokens:
+        plans.append((cur, qk))
+        r = np.maximum(0.0, cur - qk)
+        s = np.sum(r)
+        cur = r / s if s > 0 else cur
+        q_next = qk.copy()
+        q_next[int(x)] = 0.0
+        sq = np.sum(q_next)
+        qk = q_next / sq if sq > 0 else q_next
+    return plans, cur
+
+
 def accept_test(u, cur_x, q_x):
     """Accept iff u * q(x) < cur(x), i.e. u < min(1, cur(x)/q(x)) without a
     division; with q(x) = 0 this accepts iff cur(x) > 0."""
@@ -317,7 +352,7 @@ def inverse_cdf(w, u):
 
 
 def tree_accept_sampling(target_logits, draft_logits, tokens, parents, n_nodes, temperature,
-                         u_accept, u_sample, V=None):
+                         u_accept, u_sample, V=None, without_replacement=False):
     """Rejection-sampling acceptance at temperature T > 0 (lossless
     verification: troisinh.com "Why it works"; study note case 3).
 
@@ -328,6 +363,10 @@ def tree_accept_sampling(target_logits, draft_logits, tokens, parents, n_nodes, 
     child is accepted (or n is a leaf) the bonus token is drawn from the
     current distribution (the residual after the rejections, or p at a leaf)
     by inverse CDF with u = u_sample[n], and the walk ends.
+
+    ``without_replacement`` selects the sibling rule of ``node_plan_wor`` (the
+    draft renormalised without each rejected sibling's token) instead of
+    ``node_plan`` (draft fixed).
 
     Returns dict like ``tree_accept_greedy`` plus ``near_boundary`` bool [B]:
     some decision of the walk had |u - cur(x)/q(x)| < 1e-6 or an inverse-CDF
@@ -358,13 +397,17 @@ def tree_accept_sampling(target_logits, draft_logits, tokens, parents, n_nodes, 
             p = softmax_t(target_logits[b, node], T)
             q = softmax_t(draft_logits[b, node], T)
             child_tokens = [int(tokens[b, c]) for c in kids[node]]
-            cur_list, final = node_plan(p, q, child_tokens)
+            if without_replacement:
+                plans, final = node_plan_wor(p, q, child_tokens)
+            else:
+                cur_list, final = node_plan(p, q, child_tokens)
+                plans = [(cur, q) for cur in cur_list]
             nxt = None
-            for c, x, cur in zip(kids[node], child_tokens, cur_list):
+            for c, x, (cur, qk) in zip(kids[node], child_tokens, plans):
                 u = float(u_accept[b, c])
-                if q[x] > 0 and abs(u - cur[x] / q[x]) < NEAR_BOUNDARY:
+                if qk[x] > 0 and abs(u - cur[x] / qk[x]) < NEAR_BOUNDARY:
                     near[b] = True
-                if accept_test(u, cur[x], q[x]):
+                if accept_test(u, cur[x], qk[x]):
                     nxt = c
                     break
             if nxt is not None:

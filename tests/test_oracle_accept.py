@@ -289,3 +289,188 @@ def test_workload_sampling_configs_run():
     assert 0 <= a <= 3
     g = oracle.tree_accept_greedy(w.target_logits, w.tokens, w.parents, w.n_nodes)
     assert g["status"][0] == 0
+
+
+# --------------------------------------------------------------------------
+# siblings drafted without replacement
+# --------------------------------------------------------------------------
+def test_wor_hand_worked_example():
+    fx = read_fixture("sampling_wor_example.txt")
+    p = np.array([float(v) for v in fx["p"]])
+    q = np.array([float(v) for v in fx["q"]])
+    kids = [int(v) for v in fx["children"]]
+    plans, final = oracle.node_plan_wor(p, q, kids)
+    acc = [min(1.0, cur[x] / qk[x]) for x, (cur, qk) in zip(kids, plans)]
+    np.testing.assert_allclose(acc, [float(v) for v in fx["accept_prob"]], atol=1e-15)
+    np.testing.assert_allclose(plans[1][0], [float(v) for v in fx["cur_after_first"]], atol=1e-15)
+    np.testing.assert_allclose(plans[1][1], [float(v) for v in fx["q_after_first"]], atol=1e-15)
+    np.testing.assert_allclose(final, [float(v) for v in fx["final"]], atol=1e-15)
+    parents = np.array([[-1, 0, 0]], dtype=np.int32)
+    tokens = np.array([[0] + kids], dtype=np.int32)
+    T = np.log(np.stack([p, p, p]))[None].astype(np.float32)
+    D = np.log(np.stack([q, q, q]))[None].astype(np.float32)
+    for case in fx["case"]:
+        ua = np.array([[0.0, float(case["u1"]), float(case["u2"])]], dtype=np.float32)
+        us = np.full((1, 3), 0.5, dtype=np.float32)
+        r = oracle.tree_accept_sampling(T, D, tokens, parents, np.array([3]), 1.0, ua, us, without_replacement=True)
+        acc_node = int(case["accepted"])
+        assert r["accept_len"][0] == (1 if acc_node else 0)
+        if acc_node:
+            assert r["path_nodes"][0, 1] == acc_node
+        else:
+            assert r["out_tokens"][0, 0] == int(case["bonus"])
+
+
+def _wor_sequences(q, width):
+    """Every ordered draw of `width` distinct tokens without replacement from
+    q, with its probability (written out from the definition of the draw)."""
+    V = len(q)
+    for toks in itertools.permutations(range(V), width):
+        prob, left = 1.0, 1.0
+        for t in toks:
+            prob *= q[t] / left if left > 0 else 0.0
+            left -= q[t]
+        yield toks, prob
+
+
+def _exact_first_token_dist_rule(p, q, draws, plan):
+    dist = np.zeros(len(p))
+    for toks, w_draw in draws:
+        if w_draw == 0.0:
+            continue
+        plans, final = plan(p, q, list(toks))
+        reach = 1.0
+        for x, (cur, qk) in zip(toks, plans):
+            a = min(1.0, cur[x] / qk[x]) if qk[x] > 0 else (1.0 if cur[x] > 0 else 0.0)
+            dist[x] += w_draw * reach * a
+            reach *= 1.0 - a
+        dist += w_draw * reach * final
+    return dist
+
+
+def _plan_fixed_q(p, q, toks):
+    cur_list, final = oracle.node_plan(p, q, toks)
+    return [(c, np.asarray(q, dtype=np.float64)) for c in cur_list], final
+
+
+@pytest.mark.parametrize("V,width,seed", [(2, 1, 0), (2, 2, 1), (3, 2, 2), (3, 3, 3), (4, 2, 4), (4, 4, 5),
+                                          (5, 3, 6)])
+def test_wor_first_token_is_exactly_target(V, width, seed):
+    """Siblings drawn without replacement from q and tested with the
+    renormalised draft: the first emitted token is distributed exactly as p."""
+    rng = np.random.Generator(np.random.PCG64(100 + seed))
+    for _ in range(5):
+        p = oracle.softmax_t(rng.normal(0, 2, V), 1.0)
+        q = oracle.softmax_t(rng.normal(0, 2, V), 1.0)
+        dist = _exact_first_token_dist_rule(p, q, list(_wor_sequences(q, width)), oracle.node_plan_wor)
+        np.testing.assert_allclose(dist, p, rtol=0, atol=1e-12)
+
+
+def test_wor_with_zero_probabilities_and_whole_vocabulary():
+    p = np.array([0.0, 0.6, 0.4, 0.0])
+    q = np.array([0.5, 0.0, 0.3, 0.2])
+    for width in (1, 2, 3):  # up to the draft's support: a draw without replacement ends there
+        dist = _exact_first_token_dist_rule(p, q, list(_wor_sequences(q, width)), oracle.node_plan_wor)
+        np.testing.assert_allclose(dist, p, atol=1e-12)
+
+
+def test_sibling_rules_are_not_interchangeable():
+    """Negative controls: the fixed-draft rule is biased under draws without
+    replacement, and the renormalised rule is biased under i.i.d. draws."""
+    p = np.array([0.3, 0.5, 0.2])    # the hand-worked case: a two-point residual after a rejection
+    q = np.array([0.1, 0.3, 0.6])
+    wor = list(_wor_sequences(q, 2))
+    iid = [(toks, float(np.prod([q[t] for t in toks]))) for toks in itertools.product(range(3), repeat=2)]
+    d_fixed_wor = _exact_first_token_dist_rule(p, q, wor, _plan_fixed_q)
+    d_wor_iid = _exact_first_token_dist_rule(p, q, iid, oracle.node_plan_wor)
+    assert np.max(np.abs(d_fixed_wor - p)) > 1e-3
+    assert np.max(np.abs(d_wor_iid - p)) > 1e-3
+    np.testing.assert_allclose(_exact_first_token_dist_rule(p, q, iid, _plan_fixed_q), p, atol=1e-12)
+
+
+def test_wor_drafts_are_renormalised_without_rejected_tokens():
+    rng = np.random.Generator(np.random.PCG64(10))
+    p = oracle.softmax_t(rng.normal(0, 2, 6), 1.0)
+    q = oracle.softmax_t(rng.normal(0, 2, 6), 1.0)
+    kids = [4, 1, 3, 0]
+    plans, _ = oracle.node_plan_wor(p, q, kids)
+    for k, (_cur, qk) in enumerate(plans):
+        assert qk.sum() == pytest.approx(1.0, abs=1e-12)
+        assert all(qk[x] == 0.0 for x in kids[:k])
+        keep = [t for t in range(6) if t not in kids[:k]]
+        np.testing.assert_allclose(qk[keep], q[keep] / q[keep].sum(), atol=1e-15)
+
+
+def test_wor_second_token_given_accepted_child_is_child_target():
+    """Depth-2 trees drawn without replacement at every node: conditional on
+    the first emitted token being an accepted draft x, the next emitted token
+    is distributed as the target at context (x,)."""
+    V, width, seed = 4, 2, 78
+    p0 = oracle.softmax_t(_lm_rows((), V, seed, "t"), 1.0)
+    q0 = oracle.softmax_t(_lm_rows((), V, seed, "d"), 1.0)
+    joint = np.zeros((V, V))
+    acc_mass = np.zeros(V)
+    for toks, w0 in _wor_sequences(q0, width):
+        plans, _ = oracle.node_plan_wor(p0, q0, list(toks))
+        reach = 1.0
+        for x, (cur, qk) in zip(toks, plans):
+            a = min(1.0, cur[x] / qk[x])
+            m = w0 * reach * a
+            acc_mass[x] += m
+            p1 = oracle.softmax_t(_lm_rows((x,), V, seed, "t"), 1.0)
+            q1 = oracle.softmax_t(_lm_rows((x,), V, seed, "d"), 1.0)
+            joint[x] += m * _exact_first_token_dist_rule(p1, q1, list(_wor_sequences(q1, width)),
+                                                         oracle.node_plan_wor)
+            reach *= 1.0 - a
+    for x in range(V):
+        if acc_mass[x] > 0:
+            p1 = oracle.softmax_t(_lm_rows((x,), V, seed, "t"), 1.0)
+            np.testing.assert_allclose(joint[x] / acc_mass[x], p1, atol=1e-12)
+
+
+def test_wor_walker_chi_square():
+    """The walker on trees whose siblings are Gumbel top-k draws (without
+    replacement) emits a first token distributed as the target at the root."""
+    V, T, seed, width = 5, 0.8, 6, 3
+    rng = np.random.Generator(np.random.PCG64(54321))
+    counts = np.zeros(V)
+    n_draws = 6000
+    for _ in range(n_draws):
+        parents, tokens, ctx = [-1], [0], [()]
+        frontier = [0]
+        for _ in range(2):
+            nxt = []
+            for n in frontier:
+                z = _lm_rows(ctx[n], V, seed, "d") / T + rng.gumbel(size=V)
+                for x in np.argsort(-z, kind="stable")[:width]:
+                    parents.append(n)
+                    tokens.append(int(x))
+                    ctx.append(ctx[n] + (int(x),))
+                    nxt.append(len(parents) - 1)
+            frontier = nxt
+        n = len(parents)
+        tl = np.stack([_lm_rows(c, V, seed, "t") for c in ctx]).astype(np.float32)
+        dl = np.stack([_lm_rows(c, V, seed, "d") for c in ctx]).astype(np.float32)
+        ua = rng.random((1, n), dtype=np.float32)
+        us = rng.random((1, n), dtype=np.float32)
+        r = oracle.tree_accept_sampling(tl[None], dl[None], np.array([tokens], np.int32),
+                                        np.array([parents], np.int32), np.array([n]), T, ua, us,
+                                        without_replacement=True)
+        counts[r["out_tokens"][0, 0]] += 1
+    p_root = oracle.softmax_t(_lm_rows((), V, seed, "t").astype(np.float32), T)
+    chi2, pval = stats.chisquare(counts, n_draws * p_root)
+    assert pval > 1e-4, (counts, n_draws * p_root, pval)
+
+
+def test_wor_equals_fixed_rule_on_chains():
+    """With one child per node the two sibling rules coincide."""
+    w = W.make_workload("tiny")
+    parents = np.arange(-1, 7, dtype=np.int32)[None]
+    rng = np.random.Generator(np.random.PCG64(3))
+    tokens = rng.integers(0, w.V, size=(1, 8)).astype(np.int32)
+    a = oracle.tree_accept_sampling(w.target_logits, w.draft_logits, tokens, parents, np.array([8]), 1.0,
+                                    w.u_accept, w.u_sample)
+    b = oracle.tree_accept_sampling(w.target_logits, w.draft_logits, tokens, parents, np.array([8]), 1.0,
+                                    w.u_accept, w.u_sample, without_replacement=True)
+    for k in ("accept_len", "path_nodes", "out_tokens"):
+        assert np.array_equal(a[k], b[k])
