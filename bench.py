@@ -362,6 +362,13 @@ def breakdown(args, W, tvb, dev):
                               workspace=aws)
         t_acc = gtime(lambda: tvb.tree_accept(target, draft, tokens, parents, n_nodes, anc, depth, w.temperature, ua,
                                               us, status, outputs=acc, workspace=aws))
+        t_acc_wor = None
+        if sampling:  # the sibling rule for trees drafted without replacement, same inputs
+            t_acc_wor = gtime(lambda: tvb.tree_accept(target, draft, tokens, parents, n_nodes, anc, depth,
+                                                      w.temperature, ua, us, status, outputs=acc, workspace=aws,
+                                                      without_replacement=True))
+            tvb.tree_accept(target, draft, tokens, parents, n_nodes, anc, depth, w.temperature, ua, us, status,
+                            outputs=acc, workspace=aws)
         com = tvb.kv_commit_path(k, v, pt, L, n_nodes, acc[0], acc[1], status)
         t_com = gtime(lambda: tvb.kv_commit_path(k, v, pt, L, n_nodes, acc[0], acc[1], status, outputs=com))
         ok = bool((status == 0).all().item())
@@ -411,7 +418,8 @@ def breakdown(args, W, tvb, dev):
         t_roof = max(abytes / (hbm * 1e3), aflops / (tf_burst * 1e6))
         print(json.dumps({
             "workload": name, "status_ok": ok, "us_per_call": {
-                "mask": t_mask, "attn": t_attn, "accept": t_acc, "commit": t_com},
+                "mask": t_mask, "attn": t_attn, "accept": t_acc, "accept_siblings_without_replacement": t_acc_wor,
+                "commit": t_com},
             "attn_roofline_us": t_roof, "attn_bound": "hbm" if abytes / hbm >= aflops / tf_burst / 1e3 else "tensor",
             "attn_roofline_frac": t_roof / t_attn, "accept_mode": "sampling" if sampling else "greedy",
             "commit_layers": layers,

@@ -45,6 +45,7 @@ struct AcceptParams {
   int n_max, V, chunk;
   float k2;          // log2(e) / T   (sampling)
   int sampling;
+  int wor;           // siblings drafted without replacement: q renormalised without each rejected token
   int32_t* accept_len;
   int32_t* path_nodes;
   int32_t* out_tokens;
@@ -483,84 +484,107 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
         qv0 = ex.got(sh, f_owner)->f[1];
       }
       ex.flip();
-      float Sw = St.hi;         // normaliser of the current target weights wt
-      const float SqF = Sq.hi;  // normaliser of wq
-      const float isq = 1.f / SqF;
+      float Sw = St.hi;   // normaliser of the current target weights wt
+      float SqF = Sq.hi;  // normaliser of the current draft weights wq
       // the tested child's numerators: the owner CTA published them in the exchange
       // (no CTA reads another CTA's slices during the walk)
       float pv = pv0, qv = qv0;
       // a residual step whose slice update is deferred to the next pass:
-      // wt = max(0, wt * pend_isw - wq * isq), its normaliser already in Sw
+      // wt = max(0, wt * pend_isw - wq * pend_isq), its normaliser already in Sw
       bool pending = false;
-      float pend_isw = 0.f;
+      float pend_isw = 0.f, pend_isq = 0.f;
+      // without replacement: the rejected token whose draft weight is zeroed in the
+      // next pass, after that pass's deferred update has used it (slice offset, or -1)
+      int pend_zero = -1;
       int accepted = -1;
       for (int k = k_beg; k < k_end; ++k) {
         const int c = sh.kids[k];
         const float u = sh.ua[c];
-        if (u * (qv / SqF) < pv / Sw) {
+        if (u * (SqF > 0.f ? qv / SqF : 0.f) < pv / Sw) {
           accepted = c;
           break;
         }
-        // rejected: the residual max(0, p - q), normalised (p kept if it sums to 0).
-        // One pass applies the deferred update and sums the new residual; products
-        // and differences are rounded one by one so every pass agrees.
+        // rejected: the residual max(0, p - q), normalised (p kept if it sums to 0);
+        // without replacement also q without the rejected token, renormalised.  One
+        // pass applies the deferred update and sums the new residual (and the
+        // remaining draft weights); products and differences are rounded one by one
+        // so every pass agrees.
         const float cur_isw = 1.f / Sw;
-        Df z{0.f, 0.f};
+        const float cur_isq = SqF > 0.f ? 1.f / SqF : 0.f;
+        const int xk = sh.tok[c];
+        const int xk_off = (p.wor && xk >= lo && xk < hi) ? xk - lo : -1;
+        Df z{0.f, 0.f}, zq{0.f, 0.f};
         for (int j0 = tid; j0 < len; j0 += 4 * kAccThreads) {
-          float g = 0.f;
+          float g = 0.f, gq = 0.f;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int j = j0 + u * kAccThreads;
             if (j < len) {
               float w = wt[j];
-              const float qq = __fmul_rn(wq[j], isq);
+              float qw = wq[j];
               if (pending) {
-                w = fmaxf(0.f, __fsub_rn(__fmul_rn(w, pend_isw), qq));
+                w = fmaxf(0.f, __fsub_rn(__fmul_rn(w, pend_isw), __fmul_rn(qw, pend_isq)));
                 wt[j] = w;
               }
-              g += fmaxf(0.f, __fsub_rn(__fmul_rn(w, cur_isw), qq));
+              if (j == pend_zero) {
+                qw = 0.f;
+                wq[j] = 0.f;
+              }
+              g += fmaxf(0.f, __fsub_rn(__fmul_rn(w, cur_isw), __fmul_rn(qw, cur_isq)));
+              if (j != xk_off) gq += qw;
             }
           }
           z = df_add1(z, g);
+          zq = df_add1(zq, gq);
         }
-        block_sum2(z, Df{0.f, 0.f}, sh);
+        block_sum2(z, zq, sh);
         const bool more = k + 1 < k_end;
-        int nx_owner = 0, nx_off = 0;
+        int nx_owner = 0, nx_off = 0, nx_tok = -1;
         if (more) {
-          const int x = sh.tok[sh.kids[k + 1]];
-          nx_owner = x / p.chunk;
-          nx_off = x - nx_owner * p.chunk;
+          nx_tok = sh.tok[sh.kids[k + 1]];
+          nx_owner = nx_tok / p.chunk;
+          nx_off = nx_tok - nx_owner * p.chunk;
         }
         if (tid == 0) {
           ClSlot* s = ex.publish(sh);
           s->d[0] = sh.bd[0];
+          s->d[1] = sh.bd[1];
           if (more && rank == nx_owner) {
             const float w = wt[nx_off];
-            const float qq = __fmul_rn(wq[nx_off], isq);
-            s->f[0] = w;                                                  // p numerator if kept
-            s->f[1] = wq[nx_off];                                         // q numerator
-            s->d[1].hi = fmaxf(0.f, __fsub_rn(__fmul_rn(w, cur_isw), qq));  // residual numerator
+            const float qw = wq[nx_off];
+            s->f[0] = w;                                                   // p numerator if kept
+            s->f[1] = (p.wor && nx_tok == xk) ? 0.f : qw;                  // next child's q numerator
+            s->i[0] = __float_as_int(
+                fmaxf(0.f, __fsub_rn(__fmul_rn(w, cur_isw), __fmul_rn(qw, cur_isq))));  // residual numerator
           }
         }
         ex.exchange(sh);
-        Df Z{0.f, 0.f};
-        for (int r = 0; r < kCL; ++r) Z = df_add(Z, ex.got(sh, r)->d[0]);
+        Df Z{0.f, 0.f}, Zq{0.f, 0.f};
+        for (int r = 0; r < kCL; ++r) {
+          Z = df_add(Z, ex.got(sh, r)->d[0]);
+          Zq = df_add(Zq, ex.got(sh, r)->d[1]);
+        }
         float nw = 0.f, nq = 0.f, nr = 0.f;
         if (more) {
           const ClSlot* o = ex.got(sh, nx_owner);
           nw = o->f[0];
           nq = o->f[1];
-          nr = o->d[1].hi;
+          nr = __int_as_float(o->i[0]);
         }
         ex.flip();
         if (df_pos(Z)) {
           pending = true;
           pend_isw = cur_isw;
+          pend_isq = cur_isq;
           Sw = Z.hi;
           pv = nr;
         } else {
           pending = false;
           pv = nw;
+        }
+        if (p.wor) {
+          pend_zero = xk_off;
+          SqF = Zq.hi;
         }
         qv = nq;
       }
@@ -570,7 +594,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
       }
       if (pending) {  // the bonus draw reads the current p: apply the deferred update
         for (int j = tid; j < len; j += kAccThreads)
-          wt[j] = fmaxf(0.f, __fsub_rn(__fmul_rn(wt[j], pend_isw), __fmul_rn(wq[j], isq)));
+          wt[j] = fmaxf(0.f, __fsub_rn(__fmul_rn(wt[j], pend_isw), __fmul_rn(wq[j], pend_isq)));
         __syncthreads();
       }
       // ---- bonus token: inverse CDF of wt with u_sample[node] (double-float prefix sums)
@@ -910,7 +934,7 @@ extern "C" size_t tv_tree_accept_workspace(int B, int n_max, int V) {
 
 extern "C" int tv_tree_accept(const float* target_logits, const float* draft_logits, const int32_t* tokens,
                               const int32_t* parents, const int32_t* n_nodes, const uint64_t* anc_mask,
-                              const int32_t* depth, int B, int n_max, int V, float temperature,
+                              const int32_t* depth, int B, int n_max, int V, float temperature, int flags,
                               const float* u_accept, const float* u_sample, int32_t* accept_len,
                               int32_t* path_nodes, int32_t* out_tokens, void* ws, size_t ws_bytes,
                               int32_t* status, void* stream) {
@@ -924,6 +948,8 @@ extern "C" int tv_tree_accept(const float* target_logits, const float* draft_log
              "tv_tree_accept: sampling needs draft_logits, u_accept and u_sample");
   TV_REQUIRE(temperature >= 0.f && temperature == temperature, TV_ERR_INVALID_ARG,
              "tv_tree_accept: temperature must be >= 0");
+  TV_REQUIRE((flags & ~TV_ACCEPT_SIBLINGS_WITHOUT_REPLACEMENT) == 0, TV_ERR_INVALID_ARG,
+             "tv_tree_accept: unknown flags 0x%x", flags);
   TV_REQUIRE(B >= 0 && V >= 1, TV_ERR_INVALID_ARG, "tv_tree_accept: bad sizes B=%d V=%d", B, V);
   TV_REQUIRE(n_max >= 1 && n_max <= tv::kMaxNodes, TV_ERR_UNSUPPORTED,
              "tv_tree_accept: n_max = %d not in [1, 64]", n_max);
@@ -973,6 +999,7 @@ extern "C" int tv_tree_accept(const float* target_logits, const float* draft_log
   p.chunk = chunk;
   p.k2 = sampling ? (float)(1.4426950408889634 / (double)temperature) : 0.f;
   p.sampling = sampling ? 1 : 0;
+  p.wor = (flags & TV_ACCEPT_SIBLINGS_WITHOUT_REPLACEMENT) ? 1 : 0;
   p.accept_len = accept_len;
   p.path_nodes = path_nodes;
   p.out_tokens = out_tokens;

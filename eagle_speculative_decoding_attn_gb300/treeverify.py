@@ -24,6 +24,8 @@ TV_ERR_UNSUPPORTED = -2
 TV_ERR_WORKSPACE = -3
 TV_ERR_CUDA = -4
 
+TV_ACCEPT_SIBLINGS_WITHOUT_REPLACEMENT = 1
+
 TV_DEV_BAD_TREE = 1
 TV_DEV_PAGE_OOB = 2
 TV_DEV_CAPACITY = 4
@@ -44,7 +46,7 @@ _SIGNATURES = {
     "tv_tree_verify_attn_noalloc": (_I, [_P, _P, _P, _I64, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                                          _P, _P]),
     "tv_tree_accept_workspace": (_SZ, [_I, _I, _I]),
-    "tv_tree_accept": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "tv_tree_accept": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "tv_kv_commit_path": (_I, [_P, _P, _I, _I64, _I64, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "tv_tree_expand_workspace": (_SZ, [_I, _I, _I]),
     "tv_tree_expand": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _P]),
@@ -180,9 +182,12 @@ def new_accept_workspace(B, n_max, V, device) -> Optional[torch.Tensor]:
 def tree_accept(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor], tokens: torch.Tensor,
                 parents: torch.Tensor, n_nodes: torch.Tensor, anc_mask: Optional[torch.Tensor],
                 depth: Optional[torch.Tensor], temperature: float, u_accept: Optional[torch.Tensor],
-                u_sample: Optional[torch.Tensor], status: torch.Tensor, *, outputs=None, workspace=None):
-    """Greedy (temperature 0) or rejection-sampling acceptance.  Returns
-    (accept_len int32 [B], path_nodes int32 [B, n_max], out_tokens int32 [B, n_max+1])."""
+                u_sample: Optional[torch.Tensor], status: torch.Tensor, *, outputs=None, workspace=None,
+                without_replacement: bool = False):
+    """Greedy (temperature 0) or rejection-sampling acceptance; with
+    ``without_replacement`` the sampling walk renormalises the draft without
+    each rejected sibling's token.  Returns (accept_len int32 [B], path_nodes
+    int32 [B, n_max], out_tokens int32 [B, n_max+1])."""
     B, n_max, V = target_logits.shape
     dev = target_logits.device
     if workspace is None:
@@ -195,7 +200,8 @@ def tree_accept(target_logits: torch.Tensor, draft_logits: Optional[torch.Tensor
         accept_len, path_nodes, out_tokens = outputs
     rc = load_library().tv_tree_accept(
         _ptr(target_logits), _ptr(draft_logits), _ptr(tokens), _ptr(parents), _ptr(n_nodes), _ptr(anc_mask),
-        _ptr(depth), B, n_max, V, float(temperature), _ptr(u_accept), _ptr(u_sample), _ptr(accept_len),
+        _ptr(depth), B, n_max, V, float(temperature), TV_ACCEPT_SIBLINGS_WITHOUT_REPLACEMENT if without_replacement else 0,
+        _ptr(u_accept), _ptr(u_sample), _ptr(accept_len),
         _ptr(path_nodes), _ptr(out_tokens), _ptr(workspace), 0 if workspace is None else workspace.numel(),
         _ptr(status), _stream(dev))
     _check(rc, "tv_tree_accept")

@@ -295,6 +295,16 @@ def _gumbel_argmax(rng, logits_row: np.ndarray, temperature: float, count: int) 
     return out
 
 
+def _gumbel_top_k(rng, logits_row: np.ndarray, temperature: float, count: int) -> List[int]:
+    """``count`` distinct tokens drawn without replacement from the categorical
+    with logits ``row / T``: the ``count`` largest of row / T + Gumbel noise,
+    largest first (Gumbel top-k; the drafter's sampling)."""
+    g = rng.gumbel(size=logits_row.shape[0]).astype(np.float64)
+    z = logits_row.astype(np.float64) / temperature + g
+    order = np.argsort(-z, kind="stable")[:count]
+    return [int(x) for x in order]
+
+
 def _top_k(logits_row: np.ndarray, k: int) -> List[int]:
     """The drafter's top-k expansion: the k largest draft logits, largest first
     (equal values by ascending token id)."""
@@ -306,11 +316,14 @@ def _top_k(logits_row: np.ndarray, k: int) -> List[int]:
 
 
 def make_workload(cfg, seed: Optional[int] = None, *, with_logits: bool = True,
-                  B: Optional[int] = None) -> Workload:
+                  B: Optional[int] = None, siblings: str = "iid") -> Workload:
     """Draw the full synthetic input of a config.
 
     ``B`` overrides the batch (a prefix of the same request stream), used for
-    bounded samples of a workload.
+    bounded samples of a workload.  ``siblings`` selects how a sampled
+    (T > 0) node's children are drafted from q: "iid" (independent draws,
+    repeats possible) or "wor" (without replacement: distinct tokens, Gumbel
+    top-k).
     """
     if isinstance(cfg, str):
         cfg = CONFIG_BY_NAME[cfg]
@@ -371,7 +384,9 @@ def make_workload(cfg, seed: Optional[int] = None, *, with_logits: bool = True,
             for node in range(n):
                 if not kids[node]:
                     continue
-                if T > 0:
+                if T > 0 and siblings == "wor":
+                    toks = _gumbel_top_k(rng, draft[b, node], T, len(kids[node]))
+                elif T > 0:
                     toks = _gumbel_argmax(rng, draft[b, node], T, len(kids[node]))
                 else:
                     toks = _top_k(draft[b, node], len(kids[node]))

@@ -57,6 +57,9 @@ extern "C" {
 #define TV_ERR_WORKSPACE    (-3)  /* workspace smaller than the *_workspace() query        */
 #define TV_ERR_CUDA         (-4)  /* a CUDA runtime call or launch failed                  */
 
+/* tv_tree_accept flags */
+#define TV_ACCEPT_SIBLINGS_WITHOUT_REPLACEMENT 1  /* renormalise q without each rejected sibling's token */
+
 /* device status bits (per request, OR-ed) */
 #define TV_DEV_BAD_TREE   1   /* parent[0] != -1, parent[i] not in [0, i), n_nodes not in [1, n_max] */
 #define TV_DEV_PAGE_OOB   2   /* a needed page id is outside [0, num_pages)                        */
@@ -240,10 +243,20 @@ size_t tv_tree_accept_workspace(int B, int n_max, int V);
  * running sum C of the current p (troisinh.com "Why it works"; study note
  * case 3).
  *
+ * TV_ACCEPT_SIBLINGS_WITHOUT_REPLACEMENT: for trees whose siblings were drafted
+ * without replacement (distinct tokens, e.g. Gumbel top-k): after child c with
+ * token x is rejected, q also loses x and is renormalised before the next
+ * sibling (q(x) <- 0, q <- q / sum q; all zero when nothing is left); the
+ * residual step itself uses the q that c was tested against.  Sequential
+ * rejection against the renormalised draft keeps the output distribution
+ * exactly the target's under such drafting, as the fixed-q rule does under
+ * i.i.d. drafting.
+ *
  *  target_logits float [B, n_max, V]; draft_logits float [B, n_max, V] (row n =
  *    the distribution n's children were drawn from; may be NULL when greedy)
  *  tokens   int32 [B, n_max]  drafted token of each node (root entry ignored)
  *  parents, n_nodes, anc_mask, depth: as produced by tv_tree_build_mask
+ *  flags    0, or TV_ACCEPT_SIBLINGS_WITHOUT_REPLACEMENT (sampling only; see below)
  *  u_accept, u_sample  float [B, n_max] uniforms in [0, 1) (unused when greedy)
  *  accept_len  int32 [B]          out: accepted non-root nodes a
  *  path_nodes  int32 [B, n_max]   out: 0, n_1 .. n_a, then -1
@@ -254,7 +267,7 @@ size_t tv_tree_accept_workspace(int B, int n_max, int V);
  */
 int tv_tree_accept(const float* target_logits, const float* draft_logits, const int32_t* tokens,
                    const int32_t* parents, const int32_t* n_nodes, const uint64_t* anc_mask,
-                   const int32_t* depth, int B, int n_max, int V, float temperature,
+                   const int32_t* depth, int B, int n_max, int V, float temperature, int flags,
                    const float* u_accept, const float* u_sample, int32_t* accept_len,
                    int32_t* path_nodes, int32_t* out_tokens, void* ws, size_t ws_bytes,
                    int32_t* status, void* stream);

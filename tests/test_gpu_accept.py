@@ -15,18 +15,19 @@ from scipy import stats
 import oracle
 from eagle_speculative_decoding_attn_gb300 import treeverify as tvb
 from eagle_speculative_decoding_attn_gb300 import workloads as W
+from golden_io import read_fixture
 from gpu_helpers import DevWorkload, require_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
 
-def _run(dw, temperature, status=None):
+def _run(dw, temperature, status=None, wor=False):
     anc, depth, st = dw.mask()
     if status is not None:
         st = status
     if temperature > 0:
         res = tvb.tree_accept(dw.target, dw.draft, dw.tokens, dw.parents, dw.n_nodes, anc, depth, temperature,
-                              dw.u_accept, dw.u_sample, st)
+                              dw.u_accept, dw.u_sample, st, without_replacement=wor)
     else:
         res = tvb.tree_accept(dw.target, None, dw.tokens, dw.parents, dw.n_nodes, anc, depth, 0.0, None, None, st)
     torch.cuda.synchronize()
@@ -43,11 +44,11 @@ def _check_greedy(w, dev):
     return a
 
 
-def _check_sampling(w, dev, T=None):
+def _check_sampling(w, dev, T=None, wor=False):
     T = w.temperature if T is None else T
-    a, pn, ot, st = _run(DevWorkload(w, dev), T)
+    a, pn, ot, st = _run(DevWorkload(w, dev), T, wor=wor)
     ref = oracle.tree_accept_sampling(w.target_logits, w.draft_logits, w.tokens, w.parents, w.n_nodes, T,
-                                      w.u_accept, w.u_sample)
+                                      w.u_accept, w.u_sample, without_replacement=wor)
     assert np.array_equal(st, ref["status"])
     near = ref["near_boundary"]
     same = (a == ref["accept_len"]) & (pn == ref["path_nodes"]).all(1) & (ot == ref["out_tokens"]).all(1)
@@ -221,3 +222,114 @@ def test_accept_errors():
                         torch.ones(1, dtype=torch.int32, device=dev), None, None, 1.0,
                         dw.u_accept[:, :2].contiguous(), dw.u_sample[:, :2].contiguous(),
                         torch.zeros(1, dtype=torch.int32, device=dev))
+
+
+# --------------------------------------------------------------------------
+# siblings drafted without replacement (renormalised draft after each rejection)
+# --------------------------------------------------------------------------
+def test_sampling_wor_hand_worked_example():
+    dev = require_gpu()
+    fx = read_fixture("sampling_wor_example.txt")
+    p = np.array([float(v) for v in fx["p"]])
+    q = np.array([float(v) for v in fx["q"]])
+    kids = [int(v) for v in fx["children"]]
+    cases = fx["case"]
+    B = len(cases)
+    parents = np.tile(np.array([-1, 0, 0], np.int32), (B, 1))
+    tokens = np.tile(np.array([0] + kids, np.int32), (B, 1))
+    tl = np.broadcast_to(np.log(p).astype(np.float32), (B, 3, 3)).copy()
+    dl = np.broadcast_to(np.log(q).astype(np.float32), (B, 3, 3)).copy()
+    ua = np.array([[0.0, float(c["u1"]), float(c["u2"])] for c in cases], np.float32)
+    us = np.full((B, 3), 0.5, np.float32)
+    pd, nd = to_dev(parents, dev), to_dev(np.full(B, 3, np.int32), dev)
+    anc, depth, st = tvb.tree_build_mask(pd, nd)
+    a, pn, ot = tvb.tree_accept(to_dev(tl, dev), to_dev(dl, dev), to_dev(tokens, dev), pd, nd, anc, depth, 1.0,
+                                to_dev(ua, dev), to_dev(us, dev), st, without_replacement=True)
+    torch.cuda.synchronize()
+    a, pn, ot = a.cpu().numpy(), pn.cpu().numpy(), ot.cpu().numpy()
+    for b, c in enumerate(cases):
+        acc = int(c["accepted"])
+        assert a[b] == (1 if acc else 0)
+        if acc:
+            assert pn[b, 1] == acc
+        else:
+            assert ot[b, 0] == int(c["bonus"])
+
+
+def test_sampling_wor_tiny():
+    _check_sampling(W.make_workload("tiny", siblings="wor"), require_gpu(), wor=True)
+
+
+def test_sampling_wor_llama3_70b():
+    a = _check_sampling(W.make_workload("llama3_70b", siblings="wor"), require_gpu(), wor=True)
+    print("70B (siblings without replacement) accept_len", a.tolist())
+
+
+def test_sampling_wor_long():
+    _check_sampling(W.make_workload("long", siblings="wor"), require_gpu(), wor=True)
+
+
+@pytest.mark.parametrize("V,T,seed,dup", [(5, 1.0, 0, False), (50, 0.5, 1, False), (4096, 1.3, 2, False),
+                                          (32003, 0.9, 3, False), (7, 1.0, 4, True)])
+def test_sampling_wor_random(V, T, seed, dup):
+    """Children by Gumbel top-k of the draft at T (distinct siblings), or,
+    with dup, i.i.d. draws so that the rule also meets repeated tokens."""
+    dev = require_gpu()
+    rng = np.random.Generator(np.random.PCG64(170 + seed))
+    B = 48
+    trees = [W.random_recursive_tree(rng, int(rng.integers(1, 65))) for _ in range(B)]
+    w = W.make_custom(B=B, Hq=1, Hkv=1, D=64, prefix_len=[0] * B, parents_list=trees, seed=seed, V=V,
+                      temperature=T, n_max=64)
+    w.target_logits[:] = (w.draft_logits + 0.7 * rng.standard_normal(w.draft_logits.shape)).astype(np.float32)
+    for b in range(B):
+        n = int(w.n_nodes[b])
+        kids = W.children_lists(w.parents[b], n)
+        for node in range(n):
+            if not kids[node]:
+                continue
+            z = w.draft_logits[b, node].astype(np.float64) / T
+            if dup:
+                toks = [int(np.argmax(z + rng.gumbel(size=V))) for _ in kids[node]]
+            else:
+                toks = np.argsort(-(z + rng.gumbel(size=V)), kind="stable")[:len(kids[node])].tolist()
+            for c, t in zip(kids[node], toks):
+                w.tokens[b, c] = t
+    a = _check_sampling(w, dev, wor=True)
+    print(f"V={V} accept lengths mean {a.mean():.2f} max {a.max()}")
+
+
+def test_sampling_wor_chi_square_million_draws():
+    """Root with 3 children drawn without replacement from q (Gumbel top-3,
+    fresh per request); the first emitted token over 10^6 GPU draws against
+    p_root (V - 1 dof)."""
+    dev = require_gpu()
+    V, T = 6, 1.0
+    rng = np.random.Generator(np.random.PCG64(2025))
+    tl = (1.5 * rng.standard_normal(V)).astype(np.float32)
+    dl = (1.5 * rng.standard_normal(V)).astype(np.float32)
+    p_root = oracle.softmax_t(tl, T)
+    B, n = 125000, 4
+    parents = np.tile(np.array([-1, 0, 0, 0], np.int32), (B, 1))
+    target = np.broadcast_to(np.tile(tl, (n, 1)), (B, n, V)).astype(np.float32)
+    draft = np.broadcast_to(np.tile(dl, (n, 1)), (B, n, V)).astype(np.float32)
+    pd, dd = to_dev(parents, dev), to_dev(np.full(B, n, np.int32), dev)
+    td, drd = to_dev(target, dev), to_dev(draft, dev)
+    anc, depth, st0 = tvb.tree_build_mask(pd, dd)
+    counts = np.zeros(V)
+    for rep in range(8):
+        z = dl.astype(np.float64)[None, :] / T + rng.gumbel(size=(B, V))
+        toks = np.zeros((B, n), np.int32)
+        toks[:, 1:] = np.argsort(-z, axis=1, kind="stable")[:, : n - 1]
+        ua = rng.random((B, n), dtype=np.float32)
+        us = rng.random((B, n), dtype=np.float32)
+        st = st0.clone()
+        a, pn, ot = tvb.tree_accept(td, drd, to_dev(toks, dev), pd, dd, anc, depth, T, to_dev(ua, dev),
+                                    to_dev(us, dev), st, without_replacement=True)
+        first = ot[:, 0].cpu().numpy()
+        assert (st.cpu().numpy() == 0).all()
+        counts += np.bincount(first, minlength=V)
+    total = counts.sum()
+    assert total == 10 ** 6
+    chi2, pval = stats.chisquare(counts, total * p_root)
+    print(f"chi2 {chi2:.2f} p {pval:.3f}")
+    assert pval > 1e-4
