@@ -236,6 +236,51 @@ struct ClusterEx {
   __device__ void flip() { buf ^= 1; }
 };
 
+// One pass over this CTA's slices after a rejected child: apply the deferred
+// residual update of the previous rejection (pending), and sum the new
+// residual max(0, w / Sw - q / Sq) into z.  Without replacement (kWor) the
+// previously rejected token's draft weight is zeroed once the deferred update
+// has used it, and the draft weights left after removing this child's token
+// are summed into zq.  Products and differences are rounded one by one so
+// every pass and every CTA agrees.
+template <bool kWor>
+__device__ __forceinline__ void residual_pass(float* wt, float* wq, int len, bool pending, float pend_isw,
+                                              float pend_isq, int pend_zero, float cur_isw, float cur_isq,
+                                              int xk_off, Df& z, Df& zq) {
+  for (int j0 = threadIdx.x; j0 < len; j0 += 4 * kAccThreads) {
+    float g = 0.f, gq = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u * kAccThreads;
+      if (j < len) {
+        float w = wt[j];
+        float qw = wq[j];
+        if (kWor) {
+          if (pending) {
+            w = fmaxf(0.f, __fsub_rn(__fmul_rn(w, pend_isw), __fmul_rn(qw, pend_isq)));
+            wt[j] = w;
+          }
+          if (j == pend_zero) {
+            qw = 0.f;
+            wq[j] = 0.f;
+          }
+          g += fmaxf(0.f, __fsub_rn(__fmul_rn(w, cur_isw), __fmul_rn(qw, cur_isq)));
+          if (j != xk_off) gq += qw;
+        } else {  // the draft and its normaliser never change
+          const float qq = __fmul_rn(qw, cur_isq);
+          if (pending) {
+            w = fmaxf(0.f, __fsub_rn(__fmul_rn(w, pend_isw), qq));
+            wt[j] = w;
+          }
+          g += fmaxf(0.f, __fsub_rn(__fmul_rn(w, cur_isw), qq));
+        }
+      }
+    }
+    z = df_add1(z, g);
+    if (kWor) zq = df_add1(zq, gq);
+  }
+}
+
 // ---------------------------------------------------------------- the kernel
 __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
     tree_accept_kernel(const AcceptParams p) {
@@ -514,29 +559,10 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
         const int xk = sh.tok[c];
         const int xk_off = (p.wor && xk >= lo && xk < hi) ? xk - lo : -1;
         Df z{0.f, 0.f}, zq{0.f, 0.f};
-        for (int j0 = tid; j0 < len; j0 += 4 * kAccThreads) {
-          float g = 0.f, gq = 0.f;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int j = j0 + u * kAccThreads;
-            if (j < len) {
-              float w = wt[j];
-              float qw = wq[j];
-              if (pending) {
-                w = fmaxf(0.f, __fsub_rn(__fmul_rn(w, pend_isw), __fmul_rn(qw, pend_isq)));
-                wt[j] = w;
-              }
-              if (j == pend_zero) {
-                qw = 0.f;
-                wq[j] = 0.f;
-              }
-              g += fmaxf(0.f, __fsub_rn(__fmul_rn(w, cur_isw), __fmul_rn(qw, cur_isq)));
-              if (j != xk_off) gq += qw;
-            }
-          }
-          z = df_add1(z, g);
-          zq = df_add1(zq, gq);
-        }
+        if (p.wor)
+          residual_pass<true>(wt, wq, len, pending, pend_isw, pend_isq, pend_zero, cur_isw, cur_isq, xk_off, z, zq);
+        else
+          residual_pass<false>(wt, wq, len, pending, pend_isw, pend_isq, pend_zero, cur_isw, cur_isq, xk_off, z, zq);
         block_sum2(z, zq, sh);
         const bool more = k + 1 < k_end;
         int nx_owner = 0, nx_off = 0, nx_tok = -1;
