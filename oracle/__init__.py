@@ -8,4 +8,5 @@ from .treeverify_oracle import (tree_build_mask, tree_verify_attn, tree_accept_g
                                 tree_accept_sampling, kv_commit_path, node_plan, node_plan_wor, softmax_t,
                                 inverse_cdf, accept_test, ancestors_or_self, bf16_to_f64,
                                 tree_is_valid, draft_entropy, branch_width, top_tokens,
-                                log_softmax_at, tree_expand_level, tree_build_dynamic)
+                                log_softmax_at, tree_expand_level, tree_build_dynamic,
+                                kv_prune_pages)

@@ -62,6 +62,7 @@ STATUS_PAGE_OOB = 2
 STATUS_CAPACITY = 4
 STATUS_TIMEOUT = 8
 STATUS_BAD_TOKEN = 16
+STATUS_BAD_REFCOUNT = 32
 
 MAX_NODES = 64
 NEAR_BOUNDARY = 1e-6
@@ -648,3 +649,66 @@ def tree_build_dynamic(draft_logits, root_tokens, n_levels, top_k, max_new, budg
     return dict(parents=parents, tokens=tokens, scores=scores, n_nodes=n_nodes,
                 level_start=level_start, entropy=entropy, width=width, status=status,
                 near_boundary=near)
+
+
+# --------------------------------------------------------------------------
+# step 5: zero-copy pruning of the rejected branches' pages
+# --------------------------------------------------------------------------
+def kv_prune_pages(page_table, refcount, prefix_len, n_nodes, new_len, status_in=None, page_size=16):
+    """Release, without copying anything, the pages that after the commit
+    hold only rejected tree rows (Tech Radar, failure mode 2: rejected
+    branches leave garbage blocks in the page table; managing the branches as
+    a prefix tree frees them at once, with no copy).
+
+    After the commit request b keeps positions [0, new_len); positions
+    [new_len, L + N) held the tree and are garbage.  Page-table slots
+    s = ceil(new_len / P) .. ceil((L + N) / P) - 1 contain no kept position,
+    so the request lets go of them: the slot becomes -1 and the physical
+    page's reference count drops by one; a page whose count reaches zero is
+    free (pages shared with other sequences, counts above one, stay in use).
+    The slot holding position new_len - 1 and everything before it are kept.
+
+    Requests are handled in index order; the final counts and the set of
+    freed pages do not depend on that order for valid inputs.  A request is
+    skipped when its incoming status is non-zero; BAD_TREE when new_len is
+    not in [L + 1, L + N]; CAPACITY when L + N does not fit the row (or
+    L < 0); PAGE_OOB when a released slot's id is outside [0, num_pages)
+    (nothing released); BAD_REFCOUNT when a released page's count is already
+    zero (that slot is cleared, the count stays zero).
+
+    Returns (page_table copy, refcount copy, freed: sorted list of page ids,
+    status int32 [B]).
+    """
+    pt = np.array(page_table, dtype=np.int32, copy=True)
+    rc = np.array(refcount, dtype=np.int32, copy=True)
+    B, max_pages = pt.shape
+    num_pages = rc.shape[0]
+    status = np.zeros(B, dtype=np.int32)
+    freed = []
+    for b in range(B):
+        if status_in is not None and int(status_in[b]) != 0:
+            status[b] = int(status_in[b])
+            continue
+        L, N, nl = int(prefix_len[b]), int(n_nodes[b]), int(new_len[b])
+        if L < 0 or N < 1 or (L + N + page_size - 1) // page_size > max_pages:
+            status[b] = STATUS_CAPACITY
+            continue
+        if not (L + 1 <= nl <= L + N):
+            status[b] = STATUS_BAD_TREE
+            continue
+        first = (nl + page_size - 1) // page_size
+        last = (L + N + page_size - 1) // page_size
+        slots = list(range(first, last))
+        if any(not (0 <= int(pt[b, s]) < num_pages) for s in slots):
+            status[b] = STATUS_PAGE_OOB
+            continue
+        for s in slots:
+            pid = int(pt[b, s])
+            pt[b, s] = -1
+            if rc[pid] <= 0:
+                status[b] |= STATUS_BAD_REFCOUNT
+                continue
+            rc[pid] -= 1
+            if rc[pid] == 0:
+                freed.append(pid)
+    return pt, rc, sorted(freed), status
