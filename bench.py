@@ -371,6 +371,21 @@ def breakdown(args, W, tvb, dev):
                             outputs=acc, workspace=aws)
         com = tvb.kv_commit_path(k, v, pt, L, n_nodes, acc[0], acc[1], status)
         t_com = gtime(lambda: tvb.kv_commit_path(k, v, pt, L, n_nodes, acc[0], acc[1], status, outputs=com))
+        # release of the rejected pages: page table and counts restored by a device copy before
+        # each call; the copies alone are timed too and subtracted
+        pt0, rc0 = pt.clone(), torch.ones(w.num_pages, dtype=torch.int32, device=dev)
+        ptw, rcw = pt.clone(), rc0.clone()
+        fl = torch.empty(w.B * 8, dtype=torch.int32, device=dev)
+        fc = torch.zeros(1, dtype=torch.int32, device=dev)
+        pst = torch.zeros_like(status)
+
+        def restore():
+            ptw.copy_(pt0)
+            rcw.copy_(rc0)
+            fc.zero_()
+        t_prune = gtime(lambda: (restore(), tvb.kv_prune_pages(ptw, rcw, L, n_nodes, com[1], pst, free_list=fl,
+                                                                 free_count=fc))) - gtime(restore)
+        freed = int(fc.item())
         ok = bool((status == 0).all().item())
         del k, v, target, draft
         torch.cuda.empty_cache()
@@ -419,7 +434,8 @@ def breakdown(args, W, tvb, dev):
         print(json.dumps({
             "workload": name, "status_ok": ok, "us_per_call": {
                 "mask": t_mask, "attn": t_attn, "accept": t_acc, "accept_siblings_without_replacement": t_acc_wor,
-                "commit": t_com},
+                "commit": t_com, "prune_pages": t_prune},
+            "pages_freed": freed,
             "attn_roofline_us": t_roof, "attn_bound": "hbm" if abytes / hbm >= aflops / tf_burst / 1e3 else "tensor",
             "attn_roofline_frac": t_roof / t_attn, "accept_mode": "sampling" if sampling else "greedy",
             "commit_layers": layers,

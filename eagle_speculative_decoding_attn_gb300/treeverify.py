@@ -31,6 +31,7 @@ TV_DEV_PAGE_OOB = 2
 TV_DEV_CAPACITY = 4
 TV_DEV_TIMEOUT = 8
 TV_DEV_BAD_TOKEN = 16
+TV_DEV_BAD_REFCOUNT = 32
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -50,6 +51,7 @@ _SIGNATURES = {
     "tv_kv_commit_path": (_I, [_P, _P, _I, _I64, _I64, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "tv_tree_expand_workspace": (_SZ, [_I, _I, _I]),
     "tv_tree_expand": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _P]),
+    "tv_kv_prune_pages": (_I, [_P, _I, _P, _I64, _P, _P, _P, _I, _I, _P, _I64, _P, _P, _P]),
     "tv_selftest_wait_timeout": (_I, [_P, _P]),
     "tv_last_error": (ctypes.c_char_p, []),
     "tv_version": (ctypes.c_char_p, []),
@@ -269,6 +271,28 @@ def tree_expand(draft_logits: torch.Tensor, parents: torch.Tensor, tokens: torch
         _ptr(workspace), workspace.numel(), _ptr(status), _stream(draft_logits.device))
     _check(rc, "tv_tree_expand")
     return entropy, width
+
+
+def kv_prune_pages(page_table: torch.Tensor, refcount: torch.Tensor, prefix_len: torch.Tensor,
+                   n_nodes: torch.Tensor, new_len: torch.Tensor, status: torch.Tensor, *, free_list=None,
+                   free_count=None):
+    """Release the pages that hold only rejected tree rows (page-table slots
+    cleared, reference counts decremented in place).  Returns (free_list int32
+    [capacity], free_count int32 [1]): the pages whose count reached zero are
+    free_list[old count : new count]."""
+    B, max_pages = page_table.shape
+    dev = page_table.device
+    _expect(refcount, torch.int32, refcount.shape, "refcount")
+    if free_list is None:
+        free_list = torch.full((B * 8,), -1, dtype=torch.int32, device=dev)
+    if free_count is None:
+        free_count = torch.zeros(1, dtype=torch.int32, device=dev)
+    rc = load_library().tv_kv_prune_pages(
+        _ptr(page_table), max_pages, _ptr(refcount), refcount.numel(), _ptr(prefix_len), _ptr(n_nodes),
+        _ptr(new_len), B, 16, _ptr(free_list), free_list.numel(), _ptr(free_count), _ptr(status),
+        _stream(dev))
+    _check(rc, "tv_kv_prune_pages")
+    return free_list, free_count
 
 
 def version() -> str:

@@ -66,6 +66,7 @@ extern "C" {
 #define TV_DEV_CAPACITY   4   /* L + N positions do not fit in max_pages * page_size               */
 #define TV_DEV_TIMEOUT    8   /* a bounded on-chip wait gave up (about one second)                */
 #define TV_DEV_BAD_TOKEN 16   /* a drafted token id is outside [0, V)                              */
+#define TV_DEV_BAD_REFCOUNT 32 /* a page released by tv_kv_prune_pages had a reference count of 0    */
 
 /*
  * Workspace size in bytes that tv_tree_expand needs for B requests, frontiers
@@ -293,6 +294,42 @@ int tv_kv_commit_path(void* k_cache, void* v_cache, int n_layers, int64_t layer_
                       const int32_t* prefix_len, const int32_t* n_nodes, const int32_t* accept_len,
                       const int32_t* path_nodes, int B, int n_max, int Hkv, int D, int page_size,
                       int64_t* committed_slots, int32_t* new_len, int32_t* status, void* stream);
+
+/*
+ * tv_kv_prune_pages — release, without copying, the pages that hold only
+ * rejected tree rows once the accepted path has been committed ("SGLang
+ * EAGLE-2 Speculative Decoding" (Tech Radar), failure mode 2: rejected
+ * branches leave garbage blocks in the page table, and a prefix-tree page
+ * manager frees them at once without a copy; section 2's sequence diagram:
+ * keep the accepted branch, drop the wrong branches).
+ *
+ * Request b keeps positions [0, new_len[b]) (new_len from tv_kv_commit_path).
+ * Page-table slots ceil(new_len / 16) .. ceil((L + N) / 16) - 1 hold no kept
+ * position: each is set to -1 and refcount[page] drops by one; a page whose
+ * count reaches 0 is appended to free_list (at index *free_count, which is
+ * advanced; the order of pages freed by one call is unspecified).  Pages whose
+ * count stays above 0 (shared with other sequences, e.g. a radix-tree prefix)
+ * remain in use.  Nothing else is read or written; no K/V row moves.
+ *
+ *  page_table  int32 [B, max_pages]  in/out
+ *  refcount    int32 [num_pages]     in/out, references held on each page
+ *  prefix_len, n_nodes, new_len  int32 [B]  (L, N, and L + accept_len + 1)
+ *  page_size   must be 16
+ *  free_list   int32 [free_capacity] out (may be NULL when free_capacity = 0)
+ *  free_count  int32 [1]             in/out
+ *  status      int32 [B] in/out: requests with non-zero status are skipped;
+ *    TV_DEV_CAPACITY when L + N does not fit the row (or L < 0) or when the
+ *    free list is full (the page is then free but not listed); TV_DEV_BAD_TREE
+ *    when new_len is not in [L + 1, L + N]; TV_DEV_PAGE_OOB when a released
+ *    slot holds an id outside [0, num_pages) (nothing released);
+ *    TV_DEV_BAD_REFCOUNT when a released page's count is already 0 (the slot
+ *    is cleared, the count stays 0).
+ * Requests may share pages: counts change atomically.
+ */
+int tv_kv_prune_pages(int32_t* page_table, int max_pages, int32_t* refcount, int64_t num_pages,
+                      const int32_t* prefix_len, const int32_t* n_nodes, const int32_t* new_len, int B,
+                      int page_size, int32_t* free_list, int64_t free_capacity, int32_t* free_count,
+                      int32_t* status, void* stream);
 
 /*
  * tv_selftest_wait_timeout — self-test of the bounded waits every kernel uses
