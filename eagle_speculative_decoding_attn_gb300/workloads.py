@@ -500,3 +500,25 @@ def make_expand_workload(B: int, n_max: int, V: int, *, seed: int, n_levels: int
     return ExpandWorkload(B=B, n_max=n_max, V=V, draft_logits=logits, kinds=kinds, root_tokens=root_tokens,
                           n_levels=n_levels, top_k=top_k, max_new=max_new,
                           budget=n_max if budget is None else budget)
+
+
+# --------------------------------------------------------------------------
+# 4-bit KV caches
+# --------------------------------------------------------------------------
+Q4_GROUP = 32
+
+
+def make_q4_cache(rng: np.random.Generator, num_pages: int, Hkv: int, D: int):
+    """A random 4-bit paged cache: codes uint8 [num_pages, Hkv, 16, D/2] (two
+    4-bit codes per byte, low nibble = even dim) drawn uniformly, and params
+    float16 [num_pages, Hkv, 16, 2 * D / 32]: per row and group of 32 dims a
+    scale ~ U(0.12, 0.30) and a zero ~ -7.5 * scale + N(0, 0.05), so decoded
+    values spread like N(0, 1) around 0."""
+    codes = rng.integers(0, 256, size=(num_pages, Hkv, PAGE_SIZE, D // 2), dtype=np.uint8)
+    g = D // Q4_GROUP
+    s = rng.uniform(0.12, 0.30, size=(num_pages, Hkv, PAGE_SIZE, g))
+    z = -7.5 * s + 0.05 * rng.standard_normal(size=s.shape)
+    params = np.empty((num_pages, Hkv, PAGE_SIZE, 2 * g), dtype=np.float16)
+    params[..., 0::2] = s.astype(np.float16)
+    params[..., 1::2] = z.astype(np.float16)
+    return codes, params

@@ -712,3 +712,51 @@ def kv_prune_pages(page_table, refcount, prefix_len, n_nodes, new_len, status_in
             if rc[pid] == 0:
                 freed.append(pid)
     return pt, rc, sorted(freed), status
+
+
+# --------------------------------------------------------------------------
+# low-bit KV: verify attention over a 4-bit cache
+# --------------------------------------------------------------------------
+Q4_GROUP = 32
+
+
+def f64_to_bf16_bits_via_f32(x):
+    """Round to float32 (nearest even), then to bfloat16 (nearest even);
+    returns the bf16 bit patterns (uint16)."""
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def dequantize_q4(codes, params):
+    """Decode a 4-bit KV cache to bf16 rows (troisinh.com "EAGLE - Draft head
+    ...": EAGLE pairs with an INT4 KV cache, and its further-reading list
+    names KV-cache quantisation to INT4/INT3).
+
+    codes  uint8 [..., D/2]: byte j holds dims 2j (low nibble) and 2j+1 (high
+           nibble), unsigned codes 0..15;
+    params float16 [..., 2 * D / 32]: (scale, zero) of each group of 32 dims.
+    Value of dim d: bf16(fp32(code * scale + zero)) for the group of d (the
+    product and sum exact in fp64, one rounding to fp32, one to bf16).
+    Returns bf16 bit patterns uint16 [..., D].
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    D = codes.shape[-1] * 2
+    c = np.empty(codes.shape[:-1] + (D,), dtype=np.float64)
+    c[..., 0::2] = (codes & 0x0F).astype(np.float64)
+    c[..., 1::2] = (codes >> 4).astype(np.float64)
+    prm = np.asarray(params, dtype=np.float16).astype(np.float64)
+    n_groups = D // Q4_GROUP
+    scale = np.repeat(prm[..., 0:2 * n_groups:2], Q4_GROUP, axis=-1)
+    zero = np.repeat(prm[..., 1:2 * n_groups:2], Q4_GROUP, axis=-1)
+    return f64_to_bf16_bits_via_f32(c * scale + zero)
+
+
+def tree_verify_attn_q4(q_bits, k_codes, k_params, v_codes, v_params, page_table, prefix_len, n_nodes,
+                        parents, scale, page_size=16, rows=None):
+    """Tree-masked attention over a 4-bit paged cache: the cache decoded by
+    ``dequantize_q4`` (caches [num_pages, Hkv, page_size, D/2] codes and
+    [num_pages, Hkv, page_size, 2 * D / 32] params), then ``tree_verify_attn``."""
+    return tree_verify_attn(q_bits, dequantize_q4(k_codes, k_params), dequantize_q4(v_codes, v_params),
+                            page_table, prefix_len, n_nodes, parents, scale, page_size=page_size, rows=rows)

@@ -1,0 +1,97 @@
+"""Pins of the oracle's 4-bit KV decoding and quantised attention (no GPU).
+
+Source: troisinh.com "EAGLE - Draft head ..." (EAGLE pairs with an INT4 KV
+cache; further reading: KV-cache quantisation to INT4/INT3).  Pinned by a
+hand-worked row (tests/golden/q4_example.txt), torch's own float32 -> bfloat16
+cast, the code-0 / code-15 ends and monotonicity, and an exactly representable
+cache (scale 1, zero -8) on which the quantised attention must equal the bf16
+attention of the integer values written out independently.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from eagle_speculative_decoding_attn_gb300 import workloads as W
+from golden_io import read_fixture
+
+
+def test_hand_worked_row():
+    fx = read_fixture("q4_example.txt")
+    prm = [float(x) for x in fx["params"]]
+    codes = np.zeros((1, 32), np.uint8)
+    for kv in fx["bytes_set"]:
+        j, v = kv.split("=")
+        codes[0, int(j)] = int(v, 16)
+    params = np.array([prm], np.float16)
+    bits = oracle.dequantize_q4(codes, params)
+    dims = [int(d) for d in fx["dims"]]
+    assert [int(bits[0, d]) for d in dims] == [int(b, 16) for b in fx["bits"]]
+
+
+def test_bf16_rounding_matches_torch():
+    rng = np.random.default_rng(1)
+    ties = (np.arange(1, 200, dtype=np.uint32) << 16 | 0x8000).view(np.float32).astype(np.float64)
+    ties = np.concatenate([ties, (np.uint32(0x3F810000) | np.uint32(0x8000)).reshape(1).view(np.float32)])
+    x = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-6, 6, 20000),
+                        [0.0, -0.0, 1.0, 3.140625, 65504.0, 1e-30], ties, -ties])
+    ours = oracle.f64_to_bf16_bits_via_f32(x)
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_code_ends_and_monotone():
+    rng = np.random.default_rng(2)
+    D = 128
+    s = rng.uniform(0.1, 0.4, size=(50, 4)).astype(np.float16)
+    z = rng.normal(0, 1, size=(50, 4)).astype(np.float16)
+    params = np.empty((50, 8), np.float16)
+    params[:, 0::2], params[:, 1::2] = s, z
+    vals = []
+    for c in range(16):
+        codes = np.full((50, D // 2), c | (c << 4), np.uint8)
+        vals.append(oracle.bf16_to_f64(oracle.dequantize_q4(codes, params)))
+    g = np.repeat(np.arange(4), 32)
+    np.testing.assert_array_equal(vals[0], oracle.bf16_to_f64(oracle.f64_to_bf16_bits_via_f32(
+        z.astype(np.float64)[:, g])))
+    np.testing.assert_array_equal(vals[15], oracle.bf16_to_f64(oracle.f64_to_bf16_bits_via_f32(
+        15.0 * s.astype(np.float64)[:, g] + z.astype(np.float64)[:, g])))
+    for c in range(15):
+        assert np.all(vals[c + 1] >= vals[c])
+
+
+def test_exact_cache_equals_bf16_attention():
+    """K with scale 1, zero -8 and V with scale 2, zero -15 decode to small
+    integers (exact in bf16): the quantised attention equals the bf16
+    attention over those integers."""
+    w = W.make_custom(B=2, Hq=4, Hkv=2, D=128, prefix_len=[37, 5], parents_list=[W.chain_tree(5), [-1, 0, 0, 1]],
+                      seed=4)
+    rng = np.random.default_rng(5)
+    shape = w.k_bits.shape
+    kc = rng.integers(0, 256, size=shape[:-1] + (64,), dtype=np.uint8)
+    vc = rng.integers(0, 256, size=shape[:-1] + (64,), dtype=np.uint8)
+    kp = np.zeros(shape[:-1] + (8,), np.float16)
+    kp[..., 0::2], kp[..., 1::2] = 1.0, -8.0
+    vp = np.zeros(shape[:-1] + (8,), np.float16)
+    vp[..., 0::2], vp[..., 1::2] = 2.0, -15.0      # V decodes to 2c - 15
+
+    def ints(codes, a, b):
+        out = np.empty(codes.shape[:-1] + (128,), np.float32)
+        out[..., 0::2] = a * (codes & 15).astype(np.float32) + b
+        out[..., 1::2] = a * (codes >> 4).astype(np.float32) + b
+        return torch.from_numpy(out).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+    o1, l1, s1 = oracle.tree_verify_attn_q4(w.q_bits, kc, kp, vc, vp, w.page_table, w.prefix_len,
+                                            w.n_nodes, w.parents, w.scale)
+    o2, l2, s2 = oracle.tree_verify_attn(w.q_bits, ints(kc, 1, -8), ints(vc, 2, -15), w.page_table, w.prefix_len,
+                                         w.n_nodes, w.parents, w.scale)
+    assert np.array_equal(s1, s2)
+    np.testing.assert_array_equal(np.nan_to_num(o1, nan=7.0), np.nan_to_num(o2, nan=7.0))
+    np.testing.assert_array_equal(np.nan_to_num(l1, nan=7.0), np.nan_to_num(l2, nan=7.0))
+
+
+def test_generated_cache_spread():
+    rng = np.random.default_rng(6)
+    codes, params = W.make_q4_cache(rng, 20, 2, 128)
+    v = oracle.bf16_to_f64(oracle.dequantize_q4(codes, params))
+    assert abs(v.mean()) < 0.05 and 0.7 < v.std() < 1.3
