@@ -642,16 +642,21 @@ def main():
             host_in.update(draft=w.draft_logits, u_accept=w.u_accept, u_sample=w.u_sample)
         pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host_in.items()}
         dev_in = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in pinned.items()}
-        h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+        h2d_bytes = sum(v.numel() * v.element_size() for v in pinned.values())
         cp0 = copies[0]
         res_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory()
                     for t in (cp0["acc"][0], cp0["acc"][1], cp0["acc"][2], cp0["com"][1], cp0["com"][0])]
         d2h = sum(t.numel() * t.element_size() for t in res_host)
 
-        def e2e_step(k):
-            cpk = copies[k % R]
+        dev_ins = [dev_in] + [{k2: torch.empty_like(v) for k2, v in dev_in.items()} for _ in range(R - 1)]
+
+        def h2d(k):
             for kk in pinned:
-                dev_in[kk].copy_(pinned[kk], non_blocking=True)
+                dev_ins[k % R][kk].copy_(pinned[kk], non_blocking=True)
+
+        def compute(k):
+            cpk = copies[k % R]
+            dev_in = dev_ins[k % R]
             anc, depth, st = tvb.tree_build_mask(dev_in["parents"], dev_in["n_nodes"], anc_mask=cpk["anc"],
                                                  depth=cpk["depth"], status=cpk["status"])
             tvb.tree_verify_attn(dev_in["q"].view(torch.bfloat16), cpk["k"][0], cpk["v"][0], dev_in["page_table"],
@@ -665,10 +670,15 @@ def main():
             for hdst, dsrc in zip(res_host, [acc[0], acc[1], acc[2], com[1], com[0]]):
                 hdst.copy_(dsrc, non_blocking=True)
 
+        def e2e_step(k):
+            h2d(k)
+            compute(k)
+
         K2 = min(K, 500)
         for k in range(min(Wm, 5)):
             e2e_step(k)
         barrier()
+        # (a) one python call per library function and per copy, every step
         t_start = time.perf_counter()
         x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         x0.record(stream)
@@ -677,21 +687,105 @@ def main():
         x1.record(stream)
         barrier()
         wall = time.perf_counter() - t_start
-        e2e_ms = max(x0.elapsed_time(x1), wall * 1000.0) / K2
-        e2e = {"value": float(np.sum(w.n_nodes)) / (e2e_ms / 1000.0), "unit": "nodes/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms,
-               "steps": K2,
-               "note": "python binding calls per step; KV cache resident in HBM; queries, tree, logits and "
-                       "uniforms copied from pinned host memory each step; results copied back"}
+        eager_ms = max(x0.elapsed_time(x1), wall * 1000.0) / K2
+        # (b) the same step captured once per rotated copy as a CUDA graph (host->device
+        # copies from pinned memory, the four calls, device->host copies of the results)
+        # and replayed: how a serving loop drives the library
+        e2e_graphs = []
+        with torch.cuda.stream(side):
+            for k in range(R):
+                gph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gph, stream=side):
+                    e2e_step(k)
+                e2e_graphs.append(gph)
+        torch.cuda.synchronize()
+        for k in range(min(Wm, 5)):
+            e2e_graphs[k % R].replay()
+        barrier()
+        for t in res_host:
+            t.fill_(-7)
+        t_start = time.perf_counter()
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for k in range(K2):
+            e2e_graphs[k % R].replay()
+        x1.record(stream)
+        barrier()
+        wall = time.perf_counter() - t_start
+        graph_ms = max(x0.elapsed_time(x1), wall * 1000.0) / K2
+        last = copies[(K2 - 1) % R]
+        landed = all(torch.equal(h, d.cpu()) for h, d in zip(
+            res_host, [last["acc"][0], last["acc"][1], last["acc"][2], last["com"][1], last["com"][0]]))
+        # (c) pipelined: the host->device copy of step i+1 runs on a copy stream while step i
+        # computes (each rotated copy has its own input buffers; a copy waits for the
+        # compute that last read its buffers)
+        copy_stream = torch.cuda.Stream(dev)
+        h2d_graphs, comp_graphs = [], []
+        with torch.cuda.stream(side):
+            for k in range(R):
+                g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g1, stream=side):
+                    h2d(k)
+                with torch.cuda.graph(g2, stream=side):
+                    compute(k)
+                h2d_graphs.append(g1)
+                comp_graphs.append(g2)
+        torch.cuda.synchronize()
+        copied = [torch.cuda.Event() for _ in range(R)]
+        done = [torch.cuda.Event() for _ in range(R)]
+        for e in done:
+            e.record(stream)
+
+        def pipelined(n):
+            for i in range(n):
+                k = i % R
+                copy_stream.wait_event(done[k])
+                with torch.cuda.stream(copy_stream):
+                    h2d_graphs[k].replay()
+                    copied[k].record(copy_stream)
+                stream.wait_event(copied[k])
+                comp_graphs[k].replay()
+                done[k].record(stream)
+        pipelined(min(Wm, 5))
+        barrier()
+        for t in res_host:
+            t.fill_(-7)
+        t_start = time.perf_counter()
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        pipelined(K2)
+        x1.record(stream)
+        barrier()
+        wall = time.perf_counter() - t_start
+        pipe_ms = max(x0.elapsed_time(x1), wall * 1000.0) / K2
+        landed = landed and all(torch.equal(h, d.cpu()) for h, d in zip(
+            res_host, [last["acc"][0], last["acc"][1], last["acc"][2], last["com"][1], last["com"][0]]))
+        nodes_b = float(np.sum(w.n_nodes))
+        e2e = {"value": nodes_b / (pipe_ms / 1000.0), "unit": "nodes/s",
+               "h2d_bytes_per_step": int(h2d_bytes), "d2h_bytes_per_step": int(d2h), "ms_per_step": pipe_ms,
+               "steps": K2, "results_landed_on_host": bool(landed),
+               "note": "per step: queries, tree, logits and uniforms copied from pinned host memory, mask + "
+                       "attention + accept + commit through the library, results copied back to pinned host "
+                       "memory; CUDA graphs, the copy of the next step overlapping this step's compute on a "
+                       "second stream; KV cache resident in HBM; wall clock and events, the larger",
+               "serial_graph": {"value": nodes_b / (graph_ms / 1000.0), "ms_per_step": graph_ms,
+                                "note": "copy, compute and copy back in one CUDA graph per step, no overlap"},
+               "eager": {"value": nodes_b / (eager_ms / 1000.0), "ms_per_step": eager_ms,
+                         "note": "the same step as one python binding call per function and per copy"}}
 
     nodes = float(np.sum(w.n_nodes))
-    e2e_in = [e2e["ms_per_step"]] if e2e is not None else []
+    e2e_in = [e2e["ms_per_step"], e2e["eager"]["ms_per_step"], e2e["serial_graph"]["ms_per_step"]] \
+        if e2e is not None else []
     (step_ms, attn_us, ac_us, accept_us, commit_us, expand_us, *e2e_out), (nodes_total,) = reduce_over_ranks(
         [step_ms, attn_us, ac_us, accept_us, commit_us, expand["us_per_tree"]] + e2e_in, [nodes], dev)
     expand["us_per_tree"] = expand_us
     if e2e is not None:
         e2e["ms_per_step"] = e2e_out[0]
         e2e["value"] = nodes_total / (e2e["ms_per_step"] / 1000.0)
+        e2e["eager"]["ms_per_step"] = e2e_out[1]
+        e2e["eager"]["value"] = nodes_total / (e2e_out[1] / 1000.0)
+        e2e["serial_graph"]["ms_per_step"] = e2e_out[2]
+        e2e["serial_graph"]["value"] = nodes_total / (e2e_out[2] / 1000.0)
 
     hbm, tf_burst, peak_src = load_peaks()
     abytes, aflops = w.attn_bytes(), w.attn_flops()
