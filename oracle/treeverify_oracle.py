@@ -760,3 +760,34 @@ def tree_verify_attn_q4(q_bits, k_codes, k_params, v_codes, v_params, page_table
     [num_pages, Hkv, page_size, 2 * D / 32] params), then ``tree_verify_attn``."""
     return tree_verify_attn(q_bits, dequantize_q4(k_codes, k_params), dequantize_q4(v_codes, v_params),
                             page_table, prefix_len, n_nodes, parents, scale, page_size=page_size, rows=rows)
+
+
+def quantize_q4(x_bits):
+    """Encode bf16 rows (uint16 bits [..., D]) in the 4-bit format that
+    ``dequantize_q4`` decodes.  Per row and group of 32 dims, in fp32 IEEE
+    arithmetic (round to nearest even at each step) with fp16 parameters:
+        zero  = fp16(min x)
+        scale = fp16((max x - min x) / 15)
+        code  = clamp(rint((x - zero) / scale), 0, 15)   (0 when scale is 0)
+    Codes are integer decisions taken from floating point, so the arithmetic
+    and its rounding order are part of the definition.  Returns (codes uint8
+    [..., D/2], params float16 [..., 2 * D / 32])."""
+    x = bf16_to_f64(x_bits).astype(np.float32)
+    D = x.shape[-1]
+    g = D // Q4_GROUP
+    xg = x.reshape(x.shape[:-1] + (g, Q4_GROUP))
+    mn = xg.min(axis=-1)
+    mx = xg.max(axis=-1)
+    zero = mn.astype(np.float16)
+    scale = ((mx - mn) / np.float32(15.0)).astype(np.float16)
+    z32 = zero.astype(np.float32)[..., None]
+    s32 = scale.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.rint((xg - z32) / s32)
+    q = np.where(s32 > 0, q, 0.0)
+    q = np.clip(q, 0, 15).astype(np.uint8).reshape(x.shape)
+    codes = (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)
+    params = np.empty(x.shape[:-1] + (2 * g,), dtype=np.float16)
+    params[..., 0::2] = scale
+    params[..., 1::2] = zero
+    return codes, params

@@ -95,3 +95,65 @@ def test_generated_cache_spread():
     codes, params = W.make_q4_cache(rng, 20, 2, 128)
     v = oracle.bf16_to_f64(oracle.dequantize_q4(codes, params))
     assert abs(v.mean()) < 0.05 and 0.7 < v.std() < 1.3
+
+
+# --------------------------------------------------------------------------
+# the encoder
+# --------------------------------------------------------------------------
+def _bits(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_quantize_hand_worked_group():
+    # group 0: values 0.0, 1.5, 3.0 ... (0.25 steps): min 0, max 7.5 -> scale 0.5, codes x / 0.5
+    D = 64
+    x = np.zeros(D, np.float32)
+    x[:32] = np.arange(32) * 0.25 % 7.75          # 0 .. 7.5 in quarter steps
+    x[32:] = -1.0                                 # group 1 constant: scale 0, codes 0
+    codes, params = oracle.quantize_q4(_bits(x))
+    assert params.astype(np.float32).tolist() == [0.5, 0.0, 0.0, -1.0]
+    c = np.empty(D, np.int64)
+    c[0::2], c[1::2] = codes & 15, codes >> 4
+    expect = np.rint(x[:32] / 0.5).astype(np.int64)     # ties to even: 0.25 / 0.5 = 0.5 -> 0, 0.75 -> 2
+    assert c[:32].tolist() == expect.tolist()
+    assert c[32:].tolist() == [0] * 32
+    assert oracle.bf16_to_f64(oracle.dequantize_q4(codes, params))[32:].tolist() == [-1.0] * 32
+
+
+def test_quantize_round_trip_error_bound():
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((300, 128)).astype(np.float32) * rng.uniform(0.1, 5, size=(300, 1)).astype(np.float32)
+    xb = _bits(x)
+    codes, params = oracle.quantize_q4(xb)
+    back = oracle.bf16_to_f64(oracle.dequantize_q4(codes, params))
+    xv = oracle.bf16_to_f64(xb)
+    s = np.repeat(params[:, 0::2].astype(np.float64), 32, axis=1)
+    z = np.repeat(params[:, 1::2].astype(np.float64), 32, axis=1)
+    # half a step, plus the fp16 rounding of zero and scale (at most 15 steps of it), plus bf16 output rounding
+    bound = 0.5 * s + np.abs(xv.reshape(300, 4, 32).min(-1).repeat(32, 1) - z) + 15 * s * 2.0 ** -11 \
+        + np.abs(back) * 2.0 ** -8
+    assert np.all(np.abs(back - xv) <= bound + 1e-12)
+    # codes reach both ends of every non-constant group
+    q = np.empty((300, 128), np.int64)
+    q[:, 0::2], q[:, 1::2] = codes & 15, codes >> 4
+    assert (q.reshape(300, 4, 32).min(-1) == 0).all()
+    assert (q.reshape(300, 4, 32).max(-1) >= 14).all()
+
+
+def test_quantize_codes_match_float32_definition():
+    """Each code is rint((x - zero) / scale) in float32, written out with
+    Python's own float rounding of every step (struct pack to float32)."""
+    import struct
+    f32 = lambda v: struct.unpack("f", struct.pack("f", v))[0]
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((20, 64)).astype(np.float32)
+    codes, params = oracle.quantize_q4(_bits(x))
+    xv = oracle.bf16_to_f64(_bits(x))
+    for r in range(20):
+        for d in range(64):
+            grp = d // 32
+            s, z = float(params[r, 2 * grp]), float(params[r, 2 * grp + 1])
+            c = round(f32(f32(xv[r, d] - z) / s))   # Python round: half to even
+            c = min(15, max(0, c))
+            got = (codes[r, d // 2] >> (4 * (d % 2))) & 15
+            assert got == c
