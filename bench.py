@@ -387,6 +387,11 @@ def breakdown(args, W, tvb, dev):
                                                                  free_count=fc))) - gtime(restore)
         freed = int(fc.item())
         ok = bool((status == 0).all().item())
+        # 4-bit encoding of one layer's K cache (every page of the batch)
+        qc, qp = tvb.kv_quantize_q4(k[0])
+        t_q4 = gtime(lambda: tvb.kv_quantize_q4(k[0], codes=qc, params=qp))
+        q4_bytes = k[0].numel() * 2 + qc.numel() + qp.numel() * 2
+        del qc, qp
         del k, v, target, draft
         torch.cuda.empty_cache()
         # six levels of expansion from a fresh root, the reset outside the graph
@@ -436,6 +441,7 @@ def breakdown(args, W, tvb, dev):
                 "mask": t_mask, "attn": t_attn, "accept": t_acc, "accept_siblings_without_replacement": t_acc_wor,
                 "commit": t_com, "prune_pages": t_prune},
             "pages_freed": freed,
+            "kv_quantize_q4_one_layer_k": {"us": t_q4, "bytes": q4_bytes, "tbps": q4_bytes / t_q4 / 1e6},
             "attn_roofline_us": t_roof, "attn_bound": "hbm" if abytes / hbm >= aflops / tf_burst / 1e3 else "tensor",
             "attn_roofline_frac": t_roof / t_attn, "accept_mode": "sampling" if sampling else "greedy",
             "commit_layers": layers,

@@ -1,0 +1,78 @@
+// tv_kv_quantize_q4: encode bf16 KV rows in the 4-bit cache format.
+//
+// The pages pair EAGLE with a quantised KV cache (troisinh.com "EAGLE - Draft
+// head ...": an INT4 KV cache leaves room for the draft head; further reading:
+// KV-cache quantisation to INT4/INT3).  Format, per row and group of 32 dims:
+// fp16 scale and zero, and 4-bit codes two per byte (low nibble = even dim),
+// decoding to bf16(fp32(code * scale + zero)).  Encoding in fp32 with IEEE
+// rounding at every step:
+//   zero = fp16(min x), scale = fp16((max x - min x) / 15),
+//   code = clamp(rint((x - zero) / scale), 0, 15)   (0 when scale is 0).
+// The codes are integer decisions taken from floating point: the steps and
+// their rounding are part of the format, so they are written out one by one.
+//
+// One thread per group: 64 bytes in (four 16-byte loads), 16 bytes of codes and
+// 4 bytes of parameters out; the kernel is bound by HBM.
+#include <cuda_fp16.h>
+
+#include "tv_common.cuh"
+
+namespace tv {
+
+constexpr int kQ4Group = 32;
+
+__global__ void __launch_bounds__(256) q4_encode_kernel(const uint4* __restrict__ x, int64_t n_groups,
+                                                        uint4* __restrict__ codes, uint32_t* __restrict__ params) {
+  griddep_wait();
+  const int64_t gi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gi >= n_groups) return;
+  float v[kQ4Group];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 w = __ldcs(x + gi * 4 + q);
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[q * 8 + 2 * k] = __uint_as_float(u[k] << 16);
+      v[q * 8 + 2 * k + 1] = __uint_as_float(u[k] & 0xFFFF0000u);
+    }
+  }
+  float mn = v[0], mx = v[0];
+#pragma unroll
+  for (int k = 1; k < kQ4Group; ++k) {
+    mn = fminf(mn, v[k]);
+    mx = fmaxf(mx, v[k]);
+  }
+  const __half zh = __float2half_rn(mn);
+  const __half sh = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 15.f));
+  const float z = __half2float(zh), s = __half2float(sh);
+  uint32_t packed[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int k = 0; k < kQ4Group; ++k) {
+    int c = 0;
+    if (s > 0.f) c = min(15, max(0, __float2int_rn(__fdiv_rn(__fsub_rn(v[k], z), s))));
+    packed[k >> 3] |= (uint32_t)c << (4 * (k & 7));
+  }
+  __stcs(codes + gi, make_uint4(packed[0], packed[1], packed[2], packed[3]));
+  __stcs(params + gi, (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(zh) << 16));
+}
+
+}  // namespace tv
+
+extern "C" int tv_kv_quantize_q4(const void* x, int64_t rows, int D, uint8_t* codes, void* params, void* stream) {
+  tv::clear_error();
+  TV_REQUIRE(x && codes && params, TV_ERR_INVALID_ARG, "tv_kv_quantize_q4: NULL pointer");
+  TV_REQUIRE(rows >= 0 && D >= tv::kQ4Group && D % tv::kQ4Group == 0 && D <= 1024, TV_ERR_INVALID_ARG,
+             "tv_kv_quantize_q4: rows = %lld, D = %d (need D a multiple of 32, at most 1024)", (long long)rows, D);
+  TV_REQUIRE(tv::aligned16(x) && tv::aligned16(codes) && (reinterpret_cast<uintptr_t>(params) & 3u) == 0,
+             TV_ERR_INVALID_ARG, "tv_kv_quantize_q4: x and codes must be 16-byte aligned, params 4-byte aligned");
+  const int64_t n_groups = rows * (D / tv::kQ4Group);
+  if (n_groups == 0) return TV_OK;
+  const int64_t blocks = (n_groups + 255) / 256;
+  TV_REQUIRE(blocks < (1ll << 31), TV_ERR_UNSUPPORTED, "tv_kv_quantize_q4: too many rows");
+  TV_CUDA_CHECK(tv::launch_pdl(tv::q4_encode_kernel, dim3((unsigned)blocks), dim3(256), 0, tv::as_stream(stream),
+                               reinterpret_cast<const uint4*>(x), n_groups, reinterpret_cast<uint4*>(codes),
+                               reinterpret_cast<uint32_t*>(params)));
+  TV_CUDA_CHECK(cudaGetLastError());
+  return TV_OK;
+}

@@ -52,6 +52,7 @@ _SIGNATURES = {
     "tv_tree_expand_workspace": (_SZ, [_I, _I, _I]),
     "tv_tree_expand": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _P]),
     "tv_kv_prune_pages": (_I, [_P, _I, _P, _I64, _P, _P, _P, _I, _I, _P, _I64, _P, _P, _P]),
+    "tv_kv_quantize_q4": (_I, [_P, _I64, _I, _P, _P, _P]),
     "tv_selftest_wait_timeout": (_I, [_P, _P]),
     "tv_last_error": (ctypes.c_char_p, []),
     "tv_version": (ctypes.c_char_p, []),
@@ -293,6 +294,22 @@ def kv_prune_pages(page_table: torch.Tensor, refcount: torch.Tensor, prefix_len:
         _stream(dev))
     _check(rc, "tv_kv_prune_pages")
     return free_list, free_count
+
+
+def kv_quantize_q4(x: torch.Tensor, *, codes=None, params=None):
+    """Encode bf16 rows [..., D] in the 4-bit cache format.  Returns (codes
+    uint8 [..., D/2], params float16 [..., 2*D/32])."""
+    if x.dtype != torch.bfloat16:
+        raise TreeVerifyError(f"x: expected torch.bfloat16, got {x.dtype}")
+    D = x.shape[-1]
+    rows = x.numel() // D
+    if codes is None:
+        codes = torch.empty(x.shape[:-1] + (D // 2,), dtype=torch.uint8, device=x.device)
+    if params is None:
+        params = torch.empty(x.shape[:-1] + (2 * D // 32,), dtype=torch.float16, device=x.device)
+    rc = load_library().tv_kv_quantize_q4(_ptr(x), rows, D, _ptr(codes), _ptr(params), _stream(x.device))
+    _check(rc, "tv_kv_quantize_q4")
+    return codes, params
 
 
 def version() -> str:

@@ -332,6 +332,24 @@ int tv_kv_prune_pages(int32_t* page_table, int max_pages, int32_t* refcount, int
                       int32_t* status, void* stream);
 
 /*
+ * tv_kv_quantize_q4 — encode bf16 KV rows in a 4-bit cache format
+ * (troisinh.com "EAGLE - Draft head ...": EAGLE pairs with an INT4 KV cache;
+ * further reading: KV-cache quantisation to INT4/INT3).  Per row and group
+ * of 32 dims: scale and zero in fp16, codes 0..15 two per byte (low nibble =
+ * even dim); a value decodes to bf16(fp32(code * scale + zero)).  Encoding, in
+ * fp32 with round-to-nearest-even at each step: zero = fp16(min x),
+ * scale = fp16((max x - min x) / 15), code = clamp(rint((x - zero) / scale),
+ * 0, 15), or 0 when scale is 0.  Inputs must be finite.
+ *
+ *  x       bf16 [rows, D] (any row layout: a paged cache [pages, Hkv, 16, D]
+ *          is pages * Hkv * 16 rows), 16-byte aligned
+ *  D       a multiple of 32, at most 1024
+ *  codes   uint8 [rows, D / 2] out, 16-byte aligned
+ *  params  fp16 [rows, 2 * D / 32] out: (scale, zero) per group, 4-byte aligned
+ */
+int tv_kv_quantize_q4(const void* x, int64_t rows, int D, uint8_t* codes, void* params, void* stream);
+
+/*
  * tv_selftest_wait_timeout — self-test of the bounded waits every kernel uses
  * (no counterpart in the pages).  One CTA waits on an mbarrier that nothing
  * ever completes; after the wait limit (1 s) it ORs TV_DEV_TIMEOUT into
