@@ -7,6 +7,7 @@ import torch
 from eagle_speculative_decoding_attn_gb300 import treeverify as tvb
 
 ATOL_MAX = 1e-2     # attention: max |gpu - oracle| (bf16 inputs, fp32 accumulation, bf16 output)
+OUT_ROUND = 2.0 ** -8  # half an ulp of a bf16 output, relative: added per element on rows with few keys
 ATOL_MEAN = 1e-3    # attention: mean |gpu - oracle|
 LSE_ATOL = 2e-3     # log-sum-exp (fp32 accumulation of ~1e4 terms, ex2.approx)
 
@@ -56,8 +57,14 @@ class DevWorkload:
         return out.float().cpu().numpy(), lse.cpu().numpy(), status.cpu().numpy()
 
 
-def compare_attn(out, lse, ref_out, ref_lse, w, rows=None):
-    """Element-wise comparison on every computed oracle row; returns (max, mean)."""
+def compare_attn(out, lse, ref_out, ref_lse, w, rows=None, output_rounding=False):
+    """Element-wise comparison on every computed oracle row; returns (max, mean).
+
+    With ``output_rounding`` the per-element bound is ATOL_MAX plus the bf16
+    output's own rounding (half an ulp, at most 2^-8 |ref|): rows that attend
+    to a handful of keys keep outputs as large as single V entries (|o| up to
+    ~4), where that rounding alone approaches 1e-2.  The Llama-shaped workloads
+    are held to the plain bound."""
     if rows is None:
         rows = [(b, i, h) for b in range(w.B) for i in range(int(w.n_nodes[b])) for h in range(w.Hq)]
     got = np.stack([out[b, i, h] for (b, i, h) in rows])
@@ -65,7 +72,8 @@ def compare_attn(out, lse, ref_out, ref_lse, w, rows=None):
     err = np.abs(got - ref)
     assert np.all(np.isfinite(got)), "non-finite attention output"
     mx, mean = float(err.max()), float(err.mean())
-    assert mx <= ATOL_MAX, f"max abs err {mx} > {ATOL_MAX}"
+    bound = ATOL_MAX + (OUT_ROUND * np.abs(ref) if output_rounding else 0.0)
+    assert np.all(err <= bound), f"max abs err {mx} above the bound (largest excess {float((err - bound).max())})"
     assert mean <= ATOL_MEAN, f"mean abs err {mean} > {ATOL_MEAN}"
     gl = np.array([lse[b, i, h] for (b, i, h) in rows])
     rl = np.array([ref_lse[b, i, h] for (b, i, h) in rows])
