@@ -768,7 +768,8 @@ def quantize_q4(x_bits):
     arithmetic (round to nearest even at each step) with fp16 parameters:
         zero  = fp16(min x)
         scale = fp16((max x - min x) / 15)
-        code  = clamp(rint((x - zero) / scale), 0, 15)   (0 when scale is 0)
+        inv   = fp32(1 / scale)
+        code  = clamp(rint((x - zero) * inv), 0, 15)   (0 when scale is 0)
     Codes are integer decisions taken from floating point, so the arithmetic
     and its rounding order are part of the definition.  Returns (codes uint8
     [..., D/2], params float16 [..., 2 * D / 32])."""
@@ -783,7 +784,8 @@ def quantize_q4(x_bits):
     z32 = zero.astype(np.float32)[..., None]
     s32 = scale.astype(np.float32)[..., None]
     with np.errstate(divide="ignore", invalid="ignore"):
-        q = np.rint((xg - z32) / s32)
+        inv = np.float32(1.0) / s32
+        q = np.rint((xg - z32) * inv)
     q = np.where(s32 > 0, q, 0.0)
     q = np.clip(q, 0, 15).astype(np.uint8).reshape(x.shape)
     codes = (q[..., 0::2] | (q[..., 1::2] << 4)).astype(np.uint8)

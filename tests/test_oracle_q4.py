@@ -141,8 +141,8 @@ def test_quantize_round_trip_error_bound():
 
 
 def test_quantize_codes_match_float32_definition():
-    """Each code is rint((x - zero) / scale) in float32, written out with
-    Python's own float rounding of every step (struct pack to float32)."""
+    """Each code is rint((x - zero) * fp32(1 / scale)) in float32, written out
+    with Python's own float rounding of every step (struct pack to float32)."""
     import struct
     f32 = lambda v: struct.unpack("f", struct.pack("f", v))[0]
     rng = np.random.default_rng(8)
@@ -153,7 +153,7 @@ def test_quantize_codes_match_float32_definition():
         for d in range(64):
             grp = d // 32
             s, z = float(params[r, 2 * grp]), float(params[r, 2 * grp + 1])
-            c = round(f32(f32(xv[r, d] - z) / s))   # Python round: half to even
+            c = round(f32(f32(xv[r, d] - z) * f32(1.0 / s)))   # Python round: half to even
             c = min(15, max(0, c))
             got = (codes[r, d // 2] >> (4 * (d % 2))) & 15
             assert got == c
