@@ -6,10 +6,12 @@
 // fp16 scale and zero, and 4-bit codes two per byte (low nibble = even dim),
 // decoding to bf16(fp32(code * scale + zero)).  Encoding in fp32 with IEEE
 // rounding at every step:
-//   zero = fp16(min x), scale = fp16((max x - min x) / 15),
-//   code = clamp(rint((x - zero) / scale), 0, 15)   (0 when scale is 0).
+//   zero = fp16(min x), scale = fp16((max x - min x) / 15), inv = fp32(1 / scale),
+//   code = clamp(rint((x - zero) * inv), 0, 15)   (0 when scale is 0).
 // The codes are integer decisions taken from floating point: the steps and
 // their rounding are part of the format, so they are written out one by one.
+// rint of a value clamped to [0, 15] is the low bits of its sum with 1.5 * 2^23
+// (the addition rounds to the nearest integer, ties to even).
 //
 // One thread per group: 64 bytes in (four 16-byte loads), 16 bytes of codes and
 // 4 bytes of parameters out; the kernel is bound by HBM.
@@ -46,12 +48,14 @@ __global__ void __launch_bounds__(256) q4_encode_kernel(const uint4* __restrict_
   const __half zh = __float2half_rn(mn);
   const __half sh = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 15.f));
   const float z = __half2float(zh), s = __half2float(sh);
+  // inv = 0 for a constant group: every code is then 0
+  const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
   uint32_t packed[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
   for (int k = 0; k < kQ4Group; ++k) {
-    int c = 0;
-    if (s > 0.f) c = min(15, max(0, __float2int_rn(__fdiv_rn(__fsub_rn(v[k], z), s))));
-    packed[k >> 3] |= (uint32_t)c << (4 * (k & 7));
+    const float q = fminf(15.f, fmaxf(0.f, __fmul_rn(__fsub_rn(v[k], z), inv)));
+    const uint32_t c = __float_as_uint(__fadd_rn(q, 12582912.f)) & 15u;
+    packed[k >> 3] |= c << (4 * (k & 7));
   }
   __stcs(codes + gi, make_uint4(packed[0], packed[1], packed[2], packed[3]));
   __stcs(params + gi, (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(zh) << 16));

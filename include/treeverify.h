@@ -338,8 +338,9 @@ int tv_kv_prune_pages(int32_t* page_table, int max_pages, int32_t* refcount, int
  * of 32 dims: scale and zero in fp16, codes 0..15 two per byte (low nibble =
  * even dim); a value decodes to bf16(fp32(code * scale + zero)).  Encoding, in
  * fp32 with round-to-nearest-even at each step: zero = fp16(min x),
- * scale = fp16((max x - min x) / 15), code = clamp(rint((x - zero) / scale),
- * 0, 15), or 0 when scale is 0.  Inputs must be finite.
+ * scale = fp16((max x - min x) / 15), inv = fp32(1 / scale),
+ * code = clamp(rint((x - zero) * inv), 0, 15), or 0 when scale is 0.
+ * Inputs must be finite.
  *
  *  x       bf16 [rows, D] (any row layout: a paged cache [pages, Hkv, 16, D]
  *          is pages * Hkv * 16 rows), 16-byte aligned
