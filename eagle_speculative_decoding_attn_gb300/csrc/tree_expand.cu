@@ -396,13 +396,24 @@ __device__ int request_merge(ExpShared& sh, const ExpandParams& p, int b, int n,
     }
   }
   __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int r = 0; r < F; ++r) {
-      sh.row_off[r] = acc;
-      acc += sh.row_w[r];
+  if (warp == 0) {  // exclusive scan of the widths over the (at most 64) frontier rows
+    const int w0 = lane < F ? sh.row_w[lane] : 0;
+    const int w1 = lane + 32 < F ? sh.row_w[lane + 32] : 0;
+    int i0 = w0, i1 = w1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y0 = __shfl_up_sync(0xffffffffu, i0, o);
+      const int y1 = __shfl_up_sync(0xffffffffu, i1, o);
+      if (lane >= o) {
+        i0 += y0;
+        i1 += y1;
+      }
     }
-    sh.row_off[F] = acc;
+    const int tot0 = __shfl_sync(0xffffffffu, i0, 31);
+    const int tot1 = __shfl_sync(0xffffffffu, i1, 31);
+    if (lane < F) sh.row_off[lane] = i0 - w0;
+    if (lane + 32 < F) sh.row_off[lane + 32] = tot0 + i1 - w1;
+    if (lane == 0) sh.row_off[F] = tot0 + tot1;
   }
   __syncthreads();
   const int C = sh.row_off[F];
@@ -424,6 +435,7 @@ __device__ int request_merge(ExpShared& sh, const ExpandParams& p, int b, int n,
     if (d < C) {
       const float c = sh.mc[d];
       int rank = 0;
+#pragma unroll 8
       for (int e = 0; e < C; ++e) {
         const float ce = sh.mc[e];
         rank += (ce > c) || (ce == c && e < d);
