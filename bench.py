@@ -49,6 +49,11 @@ def parse_args():
                     help="only run this many eager tv_tree_verify_attn calls (for profiler captures)")
     ap.add_argument("--profile-expand", type=int, default=0,
                     help="profiler capture mode: build N trees (6 levels each) with tv_tree_expand and exit")
+    ap.add_argument("--profile-accept", type=int, default=0,
+                    help="profiler capture mode: N tree_accept calls on the chosen config (its greedy or sampling "
+                         "mode) and exit")
+    ap.add_argument("--profile-quant", type=int, default=0,
+                    help="profiler capture mode: N 4-bit encodings of the chosen config's K cache layer and exit")
     ap.add_argument("--breakdown", action="store_true",
                     help="print per-call times of every kernel on each verification workload (CUDA graphs of ten "
                          "calls, L2-warm) and the 6-level expansion time, one JSON line per workload, and exit")
@@ -449,6 +454,45 @@ def breakdown(args, W, tvb, dev):
                                 "tbps": rows * w.V * 4 / t_exp / 1e6}}), flush=True)
 
 
+def profile_accept(args, W, tvb, dev):
+    """A small self-contained command for profiler captures: N acceptance
+    calls on the chosen config's tree and logits."""
+    import numpy as np
+    import torch
+    w = W.make_workload(args.config)
+    g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    sampling = w.temperature > 0
+    parents, n_nodes, tokens = g(w.parents), g(w.n_nodes), g(w.tokens)
+    target = g(w.target_logits)
+    draft = g(w.draft_logits) if sampling else None
+    ua = g(w.u_accept) if sampling else None
+    us = g(w.u_sample) if sampling else None
+    anc, depth, status = tvb.tree_build_mask(parents, n_nodes)
+    aws = tvb.new_accept_workspace(w.B, w.n_max, w.V, dev)
+    for _ in range(args.profile_accept):
+        acc = tvb.tree_accept(target, draft, tokens, parents, n_nodes, anc, depth, w.temperature, ua, us, status,
+                              workspace=aws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_accept": args.config, "calls": args.profile_accept,
+                      "mode": "sampling" if sampling else "greedy", "accept_len": acc[0].cpu().numpy().tolist(),
+                      "status": status.cpu().numpy().tolist()}))
+
+
+def profile_quant(args, W, tvb, dev):
+    """A small self-contained command for profiler captures: N 4-bit
+    encodings of the chosen config's K cache (one layer)."""
+    import numpy as np
+    import torch
+    w = W.make_workload(args.config, with_logits=False)
+    k = torch.from_numpy(np.ascontiguousarray(w.k_bits).view(np.int16)).to(dev).view(torch.bfloat16)
+    codes, params = tvb.kv_quantize_q4(k)
+    for _ in range(args.profile_quant):
+        tvb.kv_quantize_q4(k, codes=codes, params=params)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_quant": args.config, "calls": args.profile_quant,
+                      "bytes_per_call": int(k.numel() * 2 + codes.numel() + params.numel() * 2)}))
+
+
 def main():
     args = parse_args()
     if args.oracle_sample:
@@ -482,6 +526,10 @@ def main():
         return profile_expand(args, W, tvb, dev)
     if args.breakdown:
         return breakdown(args, W, tvb, dev)
+    if args.profile_accept:
+        return profile_accept(args, W, tvb, dev)
+    if args.profile_quant:
+        return profile_quant(args, W, tvb, dev)
 
     cfg = W.CONFIG_BY_NAME[args.config]
     w = W.make_workload(cfg)

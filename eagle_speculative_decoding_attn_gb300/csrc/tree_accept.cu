@@ -13,7 +13,9 @@
 // max(0, p - q) normalised.  When every child is rejected (or n is a leaf)
 // the bonus is drawn from the current p by inverse CDF.
 //
-// Design: one thread-block cluster of kCL CTAs per request.  CTA r owns the
+// Design: one thread-block cluster of CL CTAs per request (8, or 16 or 12
+// for a sampling batch small enough that all its clusters of that size are
+// resident at once: the residual passes then cover a smaller slice per CTA).  CTA r owns the
 // vocabulary slice [r*chunk, (r+1)*chunk).  Rows are read from HBM only for
 // the nodes the walk visits; in sampling mode the visited node's p and q
 // slices stay in shared memory for the residual passes and the inverse CDF.
@@ -29,7 +31,9 @@ namespace cg = cooperative_groups;
 
 namespace tv {
 
-constexpr int kCL = 8;
+constexpr int kCL = 8;             // CTAs per request when 16 would not all be resident
+constexpr int kMidCL = 12;         // CTAs per request for sampling batches that fit as 12-CTA clusters
+constexpr int kMaxCL = 16;         // CTAs per request for small sampling batches (non-portable cluster size)
 constexpr int kAccThreads = 512;
 constexpr int kAccWarps = kAccThreads / 32;
 constexpr int kMaxChunk = 26624;  // floats per CTA and array (sampling keeps two arrays)
@@ -113,7 +117,7 @@ struct AccShared {
   Df wd[kAccWarps][2];
   Df thr_excl[kAccThreads];  // exclusive scan of per-thread sums (inverse CDF)
   ClSlot slot[2];
-  ClSlot gath[kCL];  // this exchange's slots of every CTA, copied in (rank order)
+  ClSlot gath[kMaxCL];  // this exchange's slots of every CTA, copied in (rank order)
   float ua[kMaxNodes];
   float bf;
   int bi;
@@ -217,18 +221,19 @@ __device__ void block_sum2(Df a, Df b, AccShared& sh) {
 }
 
 // Cluster exchange: thread 0 of every CTA publishes its slot, then every
-// thread reads all kCL slots in rank order.  Slots are double buffered so a
+// thread reads all CL slots in rank order.  Slots are double buffered so a
 // slot is never rewritten before every CTA has passed the next cluster barrier.
+template <int CL>
 struct ClusterEx {
   cg::cluster_group cl;
   int buf;
   __device__ ClusterEx() : cl(cg::this_cluster()), buf(0) {}
   __device__ ClSlot* publish(AccShared& sh) { return &sh.slot[buf]; }
-  // cluster barrier, then the first kCL threads copy every CTA's slot into this
+  // cluster barrier, then the first CL threads copy every CTA's slot into this
   // CTA's shared memory (one remote read per slot instead of one per thread)
   __device__ void exchange(AccShared& sh) {
     cl.sync();
-    if (threadIdx.x < kCL) sh.gath[threadIdx.x] = *cl.map_shared_rank(&sh.slot[buf], (int)threadIdx.x);
+    if (threadIdx.x < CL) sh.gath[threadIdx.x] = *cl.map_shared_rank(&sh.slot[buf], (int)threadIdx.x);
     __syncthreads();
   }
   __device__ const ClSlot* got(AccShared& sh, int r) { return &sh.gath[r]; }
@@ -282,13 +287,14 @@ __device__ __forceinline__ void residual_pass(float* wt, float* wq, int len, boo
 }
 
 // ---------------------------------------------------------------- the kernel
-__global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
+template <int CL>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kAccThreads, 1)
     tree_accept_kernel(const AcceptParams p) {
   extern __shared__ __align__(16) float dyn[];
   __shared__ AccShared sh;
-  ClusterEx ex;
+  ClusterEx<CL> ex;
   const int rank = (int)ex.cl.block_rank();
-  const int b = blockIdx.x / kCL;
+  const int b = blockIdx.x / CL;
   const int tid = threadIdx.x;
   const int n_max = p.n_max, V = p.V;
   const int lo = min(V, rank * p.chunk);
@@ -401,7 +407,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
         ex.exchange(sh);
         float gv = -FLT_MAX;
         int gi = INT_MAX;
-        for (int r = 0; r < kCL; ++r) {
+        for (int r = 0; r < CL; ++r) {
           const ClSlot* s = ex.got(sh, r);
           argmax_take(gv, gi, s->f[0], s->i[0]);
         }
@@ -473,7 +479,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
       }
       ex.exchange(sh);
       float Mt = -FLT_MAX, Mq = -FLT_MAX;
-      for (int r = 0; r < kCL; ++r) {
+      for (int r = 0; r < CL; ++r) {
         const ClSlot* s = ex.got(sh, r);
         Mt = fmaxf(Mt, s->f[0]);
         Mq = fmaxf(Mq, s->f[1]);
@@ -518,7 +524,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
       }
       ex.exchange(sh);
       Df St{0.f, 0.f}, Sq{0.f, 0.f};
-      for (int r = 0; r < kCL; ++r) {  // rank order: identical in every CTA
+      for (int r = 0; r < CL; ++r) {  // rank order: identical in every CTA
         const ClSlot* s = ex.got(sh, r);
         St = df_add(St, s->d[0]);
         Sq = df_add(Sq, s->d[1]);
@@ -586,7 +592,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
         }
         ex.exchange(sh);
         Df Z{0.f, 0.f}, Zq{0.f, 0.f};
-        for (int r = 0; r < kCL; ++r) {
+        for (int r = 0; r < CL; ++r) {
           Z = df_add(Z, ex.got(sh, r)->d[0]);
           Zq = df_add(Zq, ex.got(sh, r)->d[1]);
         }
@@ -667,9 +673,9 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
           s->d[0] = s_r;
         }
         ex.exchange(sh);
-        Df pre[kCL], srk[kCL];
+        Df pre[CL], srk[CL];
         Df S{0.f, 0.f};
-        for (int r = 0; r < kCL; ++r) {
+        for (int r = 0; r < CL; ++r) {
           pre[r] = S;
           srk[r] = ex.got(sh, r)->d[0];
           S = df_add(S, srk[r]);
@@ -677,7 +683,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
         ex.flip();
         const Df t = df_mul1(S, p.u_sample[(int64_t)b * n_max + node]);
         int rstar = -1, rlast = -1;
-        for (int r = 0; r < kCL; ++r) {
+        for (int r = 0; r < CL; ++r) {
           if (df_pos(srk[r])) rlast = r;
           if (rstar < 0 && df_gt(df_add(pre[r], srk[r]), t)) rstar = r;
         }
@@ -719,7 +725,7 @@ __global__ void __cluster_dims__(kCL, 1, 1) __launch_bounds__(kAccThreads, 1)
         }
         ex.exchange(sh);
         int tokv = -1;
-        for (int r = 0; r < kCL; ++r) tokv = max(tokv, ex.got(sh, r)->i[0]);
+        for (int r = 0; r < CL; ++r) tokv = max(tokv, ex.got(sh, r)->i[0]);
         ex.flip();
         bonus = tokv;
       }
@@ -945,6 +951,48 @@ __global__ void __launch_bounds__(kArgThreads) greedy_onepass_kernel(const OnePa
 }  // namespace tv
 
 namespace {
+// CTAs per request: for sampling, the largest of 16 and 12 whose clusters of
+// the whole batch can be resident at once (non-portable sizes allowed, at
+// least B such clusters active), else 8.  0 when a CUDA call fails.
+template <int CL>
+int active_clusters(int dev) {
+  static int known[64] = {};  // per device: clusters of CL that fit at once, plus 1 (0 = not yet known)
+  if (known[dev] == 0) {
+    const void* f = (const void*)tv::tree_accept_kernel<CL>;
+    if (cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return -1;
+    if (tv::ensure_smem_attr(f, 2ull * tv::kMaxChunk * sizeof(float)) != cudaSuccess) return -1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CL);
+    cfg.blockDim = dim3(tv::kAccThreads);
+    cfg.dynamicSmemBytes = 2ull * tv::kMaxChunk * sizeof(float);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tv::tree_accept_kernel<CL>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    known[dev] = n + 1;
+  }
+  return known[dev] - 1;
+}
+
+int accept_cluster_size(bool sampling, int B) {
+  if (!sampling) return tv::kCL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int sms = tv::current_sm_count();
+  if ((int64_t)B * tv::kMaxCL <= sms) {
+    const int n = active_clusters<tv::kMaxCL>(dev);
+    if (n < 0) return 0;
+    if (n >= B) return tv::kMaxCL;
+  }
+  if ((int64_t)B * tv::kMidCL <= sms) {
+    const int n = active_clusters<tv::kMidCL>(dev);
+    if (n < 0) return 0;
+    if (n >= B) return tv::kMidCL;
+  }
+  return tv::kCL;
+}
+
 int onepass_slices(int V) { return (V + tv::kArgSlice - 1) / tv::kArgSlice; }
 bool onepass_eligible(int B, int n_max, int V) { return (int64_t)B * n_max * V * 4 <= tv::kOnePassMaxBytes; }
 size_t onepass_ws_bytes(int B, int n_max, int V) {
@@ -981,11 +1029,13 @@ extern "C" int tv_tree_accept(const float* target_logits, const float* draft_log
              "tv_tree_accept: n_max = %d not in [1, 64]", n_max);
   TV_REQUIRE(tv::aligned16(target_logits) && (!sampling || tv::aligned16(draft_logits)), TV_ERR_INVALID_ARG,
              "tv_tree_accept: logits must be 16-byte aligned");
-  const int per = (V + tv::kCL - 1) / tv::kCL;
+  if (B == 0) return TV_OK;
+  const int cl = accept_cluster_size(sampling, B);
+  TV_REQUIRE(cl > 0, TV_ERR_CUDA, "tv_tree_accept: cluster attribute query failed");
+  const int per = (V + cl - 1) / cl;
   const int chunk = (per + 3) & ~3;
   TV_REQUIRE(!sampling || chunk <= tv::kMaxChunk, TV_ERR_UNSUPPORTED,
-             "tv_tree_accept: V = %d too large for on-chip sampling (max %d)", V, tv::kMaxChunk * tv::kCL);
-  if (B == 0) return TV_OK;
+             "tv_tree_accept: V = %d too large for on-chip sampling (max %d)", V, tv::kMaxChunk * cl);
   if (!sampling && onepass_eligible(B, n_max, V)) {
     const size_t need = onepass_ws_bytes(B, n_max, V);
     TV_REQUIRE(ws != nullptr && ws_bytes >= need && tv::aligned16(ws), TV_ERR_INVALID_ARG,
@@ -1011,7 +1061,7 @@ extern "C" int tv_tree_accept(const float* target_logits, const float* draft_log
     TV_CUDA_CHECK(cudaGetLastError());
     return TV_OK;
   }
-  TV_REQUIRE((int64_t)B * tv::kCL < (1ll << 31), TV_ERR_UNSUPPORTED, "tv_tree_accept: B too large");
+  TV_REQUIRE((int64_t)B * cl < (1ll << 31), TV_ERR_UNSUPPORTED, "tv_tree_accept: B too large");
   tv::AcceptParams p;
   p.target = target_logits;
   p.draft = draft_logits;
@@ -1031,9 +1081,22 @@ extern "C" int tv_tree_accept(const float* target_logits, const float* draft_log
   p.out_tokens = out_tokens;
   p.status = status;
   const size_t smem = sampling ? 2ull * chunk * sizeof(float) : 0;
-  TV_CUDA_CHECK(tv::ensure_smem_attr((const void*)tv::tree_accept_kernel, 2ull * tv::kMaxChunk * sizeof(float)));
-  TV_CUDA_CHECK(tv::launch_pdl(tv::tree_accept_kernel, dim3(B * tv::kCL), dim3(tv::kAccThreads), smem,
-                               tv::as_stream(stream), p));
+  if (cl == tv::kMaxCL) {
+    TV_CUDA_CHECK(tv::ensure_smem_attr((const void*)tv::tree_accept_kernel<tv::kMaxCL>,
+                                       2ull * tv::kMaxChunk * sizeof(float)));
+    TV_CUDA_CHECK(tv::launch_pdl(tv::tree_accept_kernel<tv::kMaxCL>, dim3(B * cl), dim3(tv::kAccThreads), smem,
+                                 tv::as_stream(stream), p));
+  } else if (cl == tv::kMidCL) {
+    TV_CUDA_CHECK(tv::ensure_smem_attr((const void*)tv::tree_accept_kernel<tv::kMidCL>,
+                                       2ull * tv::kMaxChunk * sizeof(float)));
+    TV_CUDA_CHECK(tv::launch_pdl(tv::tree_accept_kernel<tv::kMidCL>, dim3(B * cl), dim3(tv::kAccThreads), smem,
+                                 tv::as_stream(stream), p));
+  } else {
+    TV_CUDA_CHECK(tv::ensure_smem_attr((const void*)tv::tree_accept_kernel<tv::kCL>,
+                                       2ull * tv::kMaxChunk * sizeof(float)));
+    TV_CUDA_CHECK(tv::launch_pdl(tv::tree_accept_kernel<tv::kCL>, dim3(B * cl), dim3(tv::kAccThreads), smem,
+                                 tv::as_stream(stream), p));
+  }
   TV_CUDA_CHECK(cudaGetLastError());
   return TV_OK;
 }

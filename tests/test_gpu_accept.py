@@ -216,12 +216,15 @@ def test_accept_errors():
     assert int(a.cpu()[0]) == 0 and (pn.cpu().numpy() == -1).all() and (ot.cpu().numpy() == -1).all()
     with pytest.raises(tvb.TreeVerifyError):
         tvb.tree_accept(dw.target, None, dw.tokens, dw.parents, dw.n_nodes, anc, depth, 1.0, None, None, st)
-    big = torch.zeros((1, 2, 8 * 26624 + 64), dtype=torch.float32, device=dev)
-    with pytest.raises(tvb.TreeVerifyError):
-        tvb.tree_accept(big, big, dw.tokens[:, :2].contiguous(), dw.parents[:, :2].contiguous(),
-                        torch.ones(1, dtype=torch.int32, device=dev), None, None, 1.0,
-                        dw.u_accept[:, :2].contiguous(), dw.u_sample[:, :2].contiguous(),
-                        torch.zeros(1, dtype=torch.int32, device=dev))
+    # sampling keeps each CTA's vocabulary slice on chip: at most 26624 entries per
+    # CTA, with 16 CTAs per request for one request and 8 for a batch of 12
+    for B, V in ((1, 16 * 26624 + 64), (12, 8 * 26624 + 64)):
+        big = torch.zeros((B, 2, V), dtype=torch.float32, device=dev)
+        two = lambda t: t[:, :2].expand(B, 2).contiguous()
+        with pytest.raises(tvb.TreeVerifyError):
+            tvb.tree_accept(big, big, two(dw.tokens), two(dw.parents), torch.ones(B, dtype=torch.int32, device=dev),
+                            None, None, 1.0, two(dw.u_accept), two(dw.u_sample),
+                            torch.zeros(B, dtype=torch.int32, device=dev))
 
 
 # --------------------------------------------------------------------------
