@@ -13,9 +13,10 @@
 // max(0, p - q) normalised.  When every child is rejected (or n is a leaf)
 // the bonus is drawn from the current p by inverse CDF.
 //
-// Design: one thread-block cluster of CL CTAs per request (8, or 16 or 12
-// for a sampling batch small enough that all its clusters of that size are
-// resident at once: the residual passes then cover a smaller slice per CTA).  CTA r owns the
+// Design: one thread-block cluster of CL CTAs per request: 8, or 16 or 12 for
+// a sampling batch small enough that all its clusters of that size are
+// resident at once (the residual passes then cover a smaller slice per CTA),
+// or 4 for a greedy batch whose 8-CTA clusters would not all be resident.  CTA r owns the
 // vocabulary slice [r*chunk, (r+1)*chunk).  Rows are read from HBM only for
 // the nodes the walk visits; in sampling mode the visited node's p and q
 // slices stay in shared memory for the residual passes and the inverse CDF.
@@ -32,6 +33,7 @@ namespace cg = cooperative_groups;
 namespace tv {
 
 constexpr int kCL = 8;             // CTAs per request when 16 would not all be resident
+constexpr int kMinCL = 4;          // CTAs per request for large greedy batches (all clusters resident)
 constexpr int kMidCL = 12;         // CTAs per request for sampling batches that fit as 12-CTA clusters
 constexpr int kMaxCL = 16;         // CTAs per request for small sampling batches (non-portable cluster size)
 constexpr int kAccThreads = 512;
@@ -976,10 +978,17 @@ int active_clusters(int dev) {
 }
 
 int accept_cluster_size(bool sampling, int B) {
-  if (!sampling) return tv::kCL;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   const int sms = tv::current_sm_count();
+  if (!sampling) {
+    // greedy level walk: 8 CTAs per request unless the batch's 8-CTA clusters
+    // cannot all be resident at once, then 4
+    if ((int64_t)B * tv::kCL <= sms) return tv::kCL;
+    const int n8 = active_clusters<tv::kCL>(dev);
+    if (n8 < 0) return 0;
+    return n8 >= B ? tv::kCL : tv::kMinCL;
+  }
   if ((int64_t)B * tv::kMaxCL <= sms) {
     const int n = active_clusters<tv::kMaxCL>(dev);
     if (n < 0) return 0;
@@ -1085,6 +1094,11 @@ extern "C" int tv_tree_accept(const float* target_logits, const float* draft_log
     TV_CUDA_CHECK(tv::ensure_smem_attr((const void*)tv::tree_accept_kernel<tv::kMaxCL>,
                                        2ull * tv::kMaxChunk * sizeof(float)));
     TV_CUDA_CHECK(tv::launch_pdl(tv::tree_accept_kernel<tv::kMaxCL>, dim3(B * cl), dim3(tv::kAccThreads), smem,
+                                 tv::as_stream(stream), p));
+  } else if (cl == tv::kMinCL) {
+    TV_CUDA_CHECK(tv::ensure_smem_attr((const void*)tv::tree_accept_kernel<tv::kMinCL>,
+                                       2ull * tv::kMaxChunk * sizeof(float)));
+    TV_CUDA_CHECK(tv::launch_pdl(tv::tree_accept_kernel<tv::kMinCL>, dim3(B * cl), dim3(tv::kAccThreads), smem,
                                  tv::as_stream(stream), p));
   } else if (cl == tv::kMidCL) {
     TV_CUDA_CHECK(tv::ensure_smem_attr((const void*)tv::tree_accept_kernel<tv::kMidCL>,
