@@ -74,9 +74,30 @@ def oracle_sample_plan(cfg_name):
                      f"attention, full accept/commit; scaled to the full batch by attention key counts")
 
 
+_POOL_W = None
+
+
+def _pool_init(cfg_name, B):
+    """Worker set-up for the all-cores oracle timing: the same seeded sample."""
+    global _POOL_W
+    from eagle_speculative_decoding_attn_gb300 import workloads as W
+    _POOL_W = W.make_workload(cfg_name, B=B)
+
+
+def _pool_attn(rows):
+    """The oracle's attention on a share of the sample's (request, node, head) rows."""
+    import oracle
+    w = _POOL_W
+    oracle.tree_verify_attn(w.q_bits, w.k_bits, w.v_bits, w.page_table, w.prefix_len, w.n_nodes, w.parents,
+                            w.scale, rows=rows)
+    return len(rows)
+
+
 def run_oracle_sample(cfg_name):
     """Time the oracle (as it stands) on the bounded sample; returns seconds
-    per full step (scaled) and the sample description."""
+    per full step (scaled) and the sample description.  The attention part is
+    also timed with its rows spread over every host core (spawned worker
+    processes, one thread each); mask, accept and commit stay single-thread."""
     import numpy as np
     import oracle
     from eagle_speculative_decoding_attn_gb300 import workloads as W
@@ -104,9 +125,26 @@ def run_oracle_sample(cfg_name):
     smp_keys = float(sum(int(w.prefix_len[b]) + int(w.n_nodes[b]) for (b, i, h) in rows))
     f_attn = tot_keys / max(smp_keys, 1.0)
     f_req = full.B / w.B
-    t_step = (t1 - t0) * f_req + (t2 - t1) * f_attn + (t3 - t2) * f_req + (t4 - t3) * f_req * cfg.n_layers_commit
+    t_rest = (t1 - t0) * f_req + (t3 - t2) * f_req + (t4 - t3) * f_req * cfg.n_layers_commit
+    t_step = t_rest + (t2 - t1) * f_attn
+    # the attention rows over every core
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    t_par = t2 - t1
+    if cores > 1:
+        # whole nodes per worker: the oracle gathers a node's key sequence once for all its heads
+        nodes = sorted({(b, i) for (b, i, h) in rows})
+        share = {n: k % cores for k, n in enumerate(nodes)}
+        chunks = [[r for r in rows if share[(r[0], r[1])] == k] for k in range(cores)]
+        chunks = [c for c in chunks if c]
+        with mp.get_context("spawn").Pool(len(chunks), initializer=_pool_init, initargs=(cfg_name, plan["B"])) as pool:
+            pool.map(_pool_attn, [c[:1] for c in chunks])        # workers ready, code warm
+            tp = time.perf_counter()
+            pool.map(_pool_attn, chunks)
+            t_par = time.perf_counter() - tp
     return dict(seconds_per_step=t_step, nodes=float(np.sum(full.n_nodes)), cpu_seconds=t4 - t0,
-                desc=plan["desc"])
+                desc=plan["desc"], cores=cores if cores > 1 else 1,
+                seconds_per_step_all_cores=t_rest + t_par * f_attn)
 
 
 def oracle_leg_subprocess(cfg_name):
@@ -120,9 +158,13 @@ def oracle_leg_subprocess(cfg_name):
 
 
 def cpu_baseline_obj(res):
-    return {"value": res["nodes"] / res["seconds_per_step"], "unit": "nodes/s", "cores": 1, "kind": "oracle",
+    return {"value": res["nodes"] / res["seconds_per_step_all_cores"], "unit": "nodes/s", "cores": res["cores"],
+            "kind": "oracle",
+            "single_thread": {"value": res["nodes"] / res["seconds_per_step"], "cores": 1},
             "sample": f"{res['desc']}; {res['cpu_seconds']:.1f} s of single-thread CPU work, "
-                      f"{res['seconds_per_step']:.1f} s per full step"}
+                      f"{res['seconds_per_step']:.1f} s per full step on one core, "
+                      f"{res['seconds_per_step_all_cores']:.2f} s with the attention rows spread over "
+                      f"{res['cores']} cores (one process each)"}
 
 
 # ------------------------------------------------------------------ clocks
@@ -884,13 +926,15 @@ def main():
                    "hbm_us_all_rows": accept_bytes_all / (hbm * 1e3),
                    "hbm_us_path_rows": accept_bytes_path / (hbm * 1e3)},
         "commit": {"us": commit_us, "layers": layers, "moved_rows_per_layer_head": moved,
-                   "bytes": commit_bytes, "hbm_us": commit_bytes / (hbm * 1e3)},
+                   "bytes": commit_bytes, "bytes_one_layer": commit_bytes // max(layers, 1),
+                   "hbm_us": commit_bytes / (hbm * 1e3)},
         "nodes_per_s_attn_accept_commit": nodes_total / ((attn_us + accept_us + commit_us) * 1e-6),
         "expand": dict(expand, us_per_level=expand_us / expand["levels"],
                        hbm_us=expand["bytes"] / (hbm * 1e3), hbm_frac=expand["bytes"] / (hbm * 1e3) / expand_us),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json)",
-                     "algorithmic": {"bytes": abytes, "flops": aflops}},
+                     "algorithmic": {"bytes": abytes, "flops": aflops, "exps": aflops // (4 * D),
+                                     "out_bytes": w.out_bytes()}},
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
     }
@@ -909,8 +953,9 @@ def main():
 
 
 def run_reference(args, world, rank):
-    """The oracle as it stands, on the host cores (single thread), on bounded
-    samples of the same workload."""
+    """The oracle as it stands, on the host cores (the attention rows spread
+    over every core, the rest single-thread), on bounded samples of the same
+    workload."""
     if rank != 0:
         return
     import numpy as np
@@ -921,15 +966,15 @@ def run_reference(args, world, rank):
     res, times = None, []
     for _ in range(steps):
         res = oracle_leg_subprocess(args.config)
-        times.append(res["seconds_per_step"])
+        times.append(res["seconds_per_step_all_cores"])
     sps = float(np.mean(times))
     value = res["nodes"] / sps
     print(json.dumps({"impl": "reference", "metric": METRIC, "value": value, "unit": "nodes/s", "n_gpus": world,
                       "steps": steps, "warmup": warm, "ms_per_step": sps * 1000.0, "higher_is_better": True,
                       "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                       "config": {"workload": args.config},
-                      "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": 1, "kind": "oracle",
-                                       "sample": res["desc"]},
+                      "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": res["cores"], "kind": "oracle",
+                                       "sample": res["desc"] + "; attention rows spread over the cores"},
                       "e2e": {"value": value, "unit": "nodes/s", "h2d_bytes_per_step": 0,
                               "d2h_bytes_per_step": 0}}))
 
