@@ -493,7 +493,7 @@ def make_expand_workload(B: int, n_max: int, V: int, *, seed: int, n_levels: int
             elif k == ROW_PEAKED:
                 logits[b, f, int(rng.integers(0, V))] += np.float32(spike)
             else:
-                cnt = int(rng.integers(2, 7))
+                cnt = min(V, int(rng.integers(2, 7)))
                 toks = rng.choice(V, size=cnt, replace=False)
                 logits[b, f, toks] += (spike + 0.7 * rng.standard_normal(cnt)).astype(np.float32)
     root_tokens = rng.integers(0, V, size=B).astype(np.int32)

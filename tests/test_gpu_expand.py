@@ -123,6 +123,8 @@ def test_hand_worked_example():
     (2, 16, 24576, 4, 8, 8),       # whole slices, no tail
     (5, 64, 37, 6, 3, 64),         # tiny vocabulary, one level may add every candidate
     (1, 64, 128256, 6, 8, 16),     # the 128K vocabulary, 16 slices
+    (3, 16, 1, 3, 8, 8),           # one token: every node has one child, score 0
+    (2, 16, 5, 4, 8, 16),          # fewer tokens than top_k
 ])
 def test_levels_match_oracle(B, n_max, V, levels, top_k, max_new):
     dev = require_gpu()
