@@ -18,6 +18,9 @@ __global__ void __launch_bounds__(64) tree_mask_kernel(const int32_t* __restrict
   const int b = blockIdx.x;
   const int i = threadIdx.x;
   griddep_wait();
+  // a few hundred threads of integer work: the next kernel (the attention, which
+  // needs a whole SM per CTA) may start its on-chip prologue beside it
+  griddep_launch_dependents();
   const int n = n_nodes[b];
   const bool n_ok = n >= 1 && n <= n_max;
   const int p = i < n_max ? parents[(int64_t)b * n_max + i] : 0;

@@ -13,6 +13,11 @@ namespace tv {
 // has completed and its writes are visible.  (No kernel triggers its dependents
 // early: a waiting dependent's CTAs would take SM slots from the running grid.)
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel on the stream start launching its CTAs now; they still
+// wait in griddep_wait() until this grid has completed and its writes are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
