@@ -47,6 +47,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-attn", type=int, default=0,
                     help="only run this many eager tv_tree_verify_attn calls (for profiler captures)")
+    ap.add_argument("--profile-attn-q4", type=int, default=0,
+                    help="profiler capture mode: N eager tv_tree_verify_attn_q4 calls on the chosen config's cache "
+                         "encoded in the 4-bit format, and exit")
     ap.add_argument("--profile-expand", type=int, default=0,
                     help="profiler capture mode: build N trees (6 levels each) with tv_tree_expand and exit")
     ap.add_argument("--profile-accept", type=int, default=0,
@@ -249,6 +252,16 @@ def profile_attn(args, W, tvb, dev):
     pt, L = g(w.page_table), g(w.prefix_len)
     anc, depth, status = tvb.tree_build_mask(parents, n_nodes)
     ws = tvb.new_attn_workspace(w.B, w.n_max, w.Hq, w.Hkv, w.D, dev)
+    if args.profile_attn_q4:
+        kc, kp = tvb.kv_quantize_q4(k)
+        vc, vp = tvb.kv_quantize_q4(v)
+        del k, v
+        for _ in range(args.profile_attn_q4):
+            tvb.tree_verify_attn_q4(q, kc, kp, vc, vp, pt, L, n_nodes, anc, w.scale, status, workspace=ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_attn_q4": args.config, "calls": args.profile_attn_q4,
+                          "status": status.cpu().numpy().tolist(), "attn_bytes_q4": w.attn_bytes_q4()}))
+        return
     for _ in range(args.profile_attn):
         tvb.tree_verify_attn(q, k, v, pt, L, n_nodes, anc, w.scale, status, workspace=ws)
     torch.cuda.synchronize()
@@ -405,6 +418,12 @@ def breakdown(args, W, tvb, dev):
         t_mask = gtime(lambda: tvb.tree_build_mask(parents, n_nodes, anc_mask=anc, depth=depth, status=status))
         t_attn = gtime(lambda: tvb.tree_verify_attn(q, k[0], v[0], pt, L, n_nodes, anc, w.scale, status, out=out,
                                                     lse=lse, workspace=ws))
+        # the same attention over the layer's cache encoded in the 4-bit format
+        kc, kp = tvb.kv_quantize_q4(k[0])
+        vc, vp = tvb.kv_quantize_q4(v[0])
+        t_attn_q4 = gtime(lambda: tvb.tree_verify_attn_q4(q, kc, kp, vc, vp, pt, L, n_nodes, anc, w.scale, status,
+                                                          out=out, lse=lse, workspace=ws))
+        del kc, kp, vc, vp
         acc = tvb.tree_accept(target, draft, tokens, parents, n_nodes, anc, depth, w.temperature, ua, us, status,
                               workspace=aws)
         t_acc = gtime(lambda: tvb.tree_accept(target, draft, tokens, parents, n_nodes, anc, depth, w.temperature, ua,
@@ -483,6 +502,8 @@ def breakdown(args, W, tvb, dev):
         torch.cuda.empty_cache()
         abytes, aflops = w.attn_bytes(), w.attn_flops()
         t_roof = max(abytes / (hbm * 1e3), aflops / (tf_burst * 1e6))
+        qbytes = w.attn_bytes_q4()
+        t_roof_q4 = max(qbytes / (hbm * 1e3), aflops / (tf_burst * 1e6))
         print(json.dumps({
             "workload": name, "status_ok": ok, "us_per_call": {
                 "mask": t_mask, "attn": t_attn, "accept": t_acc, "accept_siblings_without_replacement": t_acc_wor,
@@ -490,7 +511,11 @@ def breakdown(args, W, tvb, dev):
             "pages_freed": freed,
             "kv_quantize_q4_one_layer_k": {"us": t_q4, "bytes": q4_bytes, "tbps": q4_bytes / t_q4 / 1e6},
             "attn_roofline_us": t_roof, "attn_bound": "hbm" if abytes / hbm >= aflops / tf_burst / 1e3 else "tensor",
-            "attn_roofline_frac": t_roof / t_attn, "accept_mode": "sampling" if sampling else "greedy",
+            "attn_roofline_frac": t_roof / t_attn,
+            "attn_q4": {"us": t_attn_q4, "bytes": qbytes, "roofline_us": t_roof_q4,
+                        "bound": "hbm" if qbytes / hbm >= aflops / tf_burst / 1e3 else "tensor",
+                        "roofline_frac": t_roof_q4 / t_attn_q4},
+            "accept_mode": "sampling" if sampling else "greedy",
             "commit_layers": layers,
             "expand_6_levels": {"us": t_exp, "rows_read": rows, "bytes": rows * w.V * 4,
                                 "tbps": rows * w.V * 4 / t_exp / 1e6}}), flush=True)
@@ -562,7 +587,7 @@ def main():
     if world > 1:
         dist.barrier()
     tvb.load_library()
-    if args.profile_attn:
+    if args.profile_attn or args.profile_attn_q4:
         return profile_attn(args, W, tvb, dev)
     if args.profile_expand:
         return profile_expand(args, W, tvb, dev)

@@ -53,16 +53,23 @@ constexpr int kBM = 128;                       // query rows per M tile
 constexpr int kBN = 128;                       // keys per KV tile
 constexpr int kNT = 2;                         // M tiles per work group
 constexpr int kStages = 2;                     // K and V ring depth
-constexpr int kThreads = 384;                  // 12 warps
+constexpr int kThreads = 384;                  // 12 warps (bf16 cache)
+constexpr int kThreadsQ4 = 512;                // 16 warps (4-bit cache: warps 12-15 decode)
 constexpr int kPagesPerTile = kBN / kPageSize; // 8
 constexpr int kRowsPerSlot = kNT * kBM;        // rows of one partial slot
 constexpr int kMaxBatch = 1024;
+constexpr int kMaxBatchQ4 = 256;               // the 4-bit cache's code ring leaves less room for the plan
 constexpr float kRescaleLog2 = 8.0f;           // lazy O rescale threshold (factor 256)
 constexpr float kLog2e = 1.4426950408889634f;
 // register split: 384 threads x 168 at launch = 128 x 88 (warps 0-3) + 256 x 208 (softmax warps)
 constexpr uint32_t kRegsControl = 88;
 constexpr uint32_t kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax == kThreads * 168, "register split must match the launch");
+// 4-bit cache: 512 threads at 128 registers each, no re-split (the compiler's
+// limit is the launch's 128 registers for every role, so the softmax works on
+// half an S row at a time)
+constexpr int kQ4Group = 32;                   // dims sharing one (scale, zero) pair
+constexpr int kHalfKeys = kBN / 2;             // keys of one code slot (half a KV tile)
 
 struct AttnParams {
   CUtensorMap tmQ;
@@ -81,13 +88,18 @@ struct AttnParams {
   uint4* part_o;        // [2 * gridDim][D/8][256] 8 x fp16: column group major, rows contiguous
   float* part_lse;      // [2 * gridDim][256] log-sum-exp of each partial row
   float* part_scale;    // [2 * gridDim][256] max |O| of each partial row (its fp16 values are O / max)
+  // 4-bit cache only: codes [pages][Hkv][16][D/2] bytes, params [pages][Hkv][16][D/16] fp16
+  const uint8_t* k_codes;
+  const uint8_t* k_params;
+  const uint8_t* v_codes;
+  const uint8_t* v_params;
   int64_t num_pages;
   int B, max_pages, n_max, Hq, Hkv, G, q_box_nodes, mp_max;
   float scale_log2;
 };
 
 // dynamic shared-memory layout (1024-byte aligned base)
-template <int D>
+template <int D, bool kQ4>
 struct Smem {
   static constexpr int kDBlocks = D / 64;                 // 128-byte swizzle atoms along D
   static constexpr int kQTile = kBM * D * 2;
@@ -95,11 +107,21 @@ struct Smem {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kNT * kQTile;
   static constexpr int kV = kK + kStages * kKVTile;
-  static constexpr int kRqStart = kV + kStages * kKVTile;           // int64 [kMaxBatch + 1]
-  static constexpr int kRqT = kRqStart + 8 * (kMaxBatch + 1) + 8;   // int32 [kMaxBatch]
-  static constexpr int kRqMT = kRqT + 4 * kMaxBatch;                // int32 [kMaxBatch]
-  static constexpr int kBytes = kRqMT + 4 * kMaxBatch;
+  // 4-bit cache: for K and for V two code slots of half a tile each, a slot
+  // holding the codes [64 keys][D/2] followed by the params [64 keys][D/16] fp16
+  static constexpr int kCodeRow = D / 2;
+  static constexpr int kParamRow = D / 8;
+  static constexpr int kSlotParams = kHalfKeys * kCodeRow;
+  static constexpr int kSlot = kHalfKeys * (kCodeRow + kParamRow);
+  static constexpr int kKC = kV + kStages * kKVTile;
+  static constexpr int kVC = kKC + (kQ4 ? 2 * kSlot : 0);
+  static constexpr int kMB = kQ4 ? kMaxBatchQ4 : kMaxBatch;
+  static constexpr int kRqStart = kVC + (kQ4 ? 2 * kSlot : 0);   // int64 [kMB + 1]
+  static constexpr int kRqT = kRqStart + 8 * (kMB + 1) + 8;      // int32 [kMB]
+  static constexpr int kRqMT = kRqT + 4 * kMB;                   // int32 [kMB]
+  static constexpr int kBytes = kRqMT + 4 * kMB;
   static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kAlloc + 2048 <= 227 * 1024, "shared memory over the per-CTA limit");
 };
 
 // ---------------------------------------------------------------- plan
@@ -365,13 +387,64 @@ __device__ __forceinline__ void merge_tile(const AttnParams& p, const Item& it, 
   else merge_items<D, 8, 2>(p, it, mtile, n_rows, r);
 }
 
+// Decodes key row r of a 4-bit code slot into a bf16 K or V stage, laid out as
+// the TMA copies of a bf16 cache are (64-dim blocks of 128-byte rows, 16-byte
+// chunks swizzled by the row's low three bits).  Dim d of the row takes the
+// value bf16(fp32(code * scale + zero)) with the (scale, zero) fp16 pair of its
+// 32-dim group; byte j of the codes holds dim 2j in its low nibble and 2j + 1
+// in its high nibble.  A code becomes a float exactly by placing it in the low
+// mantissa bits of 2^23 and subtracting 2^23; the fused multiply-add then
+// rounds the exact code * scale + zero once to fp32, and the conversion rounds
+// that once to bf16.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_constant__ AttnParams p) {
-  using S = Smem<D>;
+__device__ __forceinline__ void decode_row_q4(const uint8_t* codes, const uint8_t* params, uint8_t* stage, int r) {
+  constexpr int kGroups = D / kQ4Group;
+  uint32_t pw[kGroups];  // (scale, zero) of each group, scale in the low half
+  if constexpr (kGroups == 4) {
+    const uint4 t = *reinterpret_cast<const uint4*>(params);
+    pw[0] = t.x; pw[1] = t.y; pw[2] = t.z; pw[3] = t.w;
+  } else {
+    const uint2 t = *reinterpret_cast<const uint2*>(params);
+    pw[0] = t.x; pw[1] = t.y;
+  }
+  const uint64_t neg_magic = f2_pack(-8388608.f, -8388608.f);
+#pragma unroll
+  for (int gi = 0; gi < kGroups; ++gi) {
+    const uint4 c = reinterpret_cast<const uint4*>(codes)[gi];  // the group's 32 codes
+    const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&pw[gi]));
+    const uint64_t s2 = f2_pack(sz.x, sz.x), z2 = f2_pack(sz.y, sz.y);
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // dims 8q .. 8q + 7 of the group: one 16-byte chunk
+      const uint32_t lo = w[q] & 0x0F0F0F0Fu, hi = (w[q] >> 4) & 0x0F0F0F0Fu;
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float ce = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440u + j));
+        const float co = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440u + j));
+        float ve, vo;
+        f2_unpack(f2_fma(f2_add(f2_pack(ce, co), neg_magic), s2, z2), ve, vo);
+        o[j] = pack_bf16x2(ve, vo);
+      }
+      const int d0 = gi * kQ4Group + q * 8;
+      const int db = d0 / 64, ch = (d0 % 64) / 8;
+      *reinterpret_cast<uint4*>(stage + db * (kBN * 128) + r * 128 + ((ch ^ (r & 7)) << 4)) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+template <int D, bool kQ4>
+__global__ void __launch_bounds__(kQ4 ? kThreadsQ4 : kThreads, 1)
+    verify_attn_kernel(const __grid_constant__ AttnParams p) {
+  using S = Smem<D, kQ4>;
+  constexpr int kNThreads = kQ4 ? kThreadsQ4 : kThreads;
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_q, bar_qe, bar_kf[kStages], bar_ke[kStages], bar_vf[kStages], bar_ve[kStages];
   __shared__ uint64_t bar_s[kNT], bar_p[kNT], bar_o[kNT], bar_of[kNT], bar_wg[kNT], bar_ml;
+  // 4-bit cache: code slots full / free (K and V), one pair per half tile
+  __shared__ uint64_t bar_kcf[2], bar_kce[2], bar_vcf[2], bar_vce[2];
   __shared__ float ml_sh[2][kBM];  // dual mode: warpgroup 1's running max and sum per row
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
@@ -395,10 +468,19 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
     mbar_init(&bar_q, 1);
     mbar_init(&bar_qe, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bar_kf[s], 1);
+      // a bf16 stage is filled by TMA (one arrival plus bytes) or by 64 decoding threads
+      mbar_init(&bar_kf[s], kQ4 ? kHalfKeys : 1);
       mbar_init(&bar_ke[s], 1);
-      mbar_init(&bar_vf[s], 1);
+      mbar_init(&bar_vf[s], kQ4 ? kHalfKeys : 1);
       mbar_init(&bar_ve[s], 1);
+    }
+    if (kQ4) {
+      for (int h = 0; h < 2; ++h) {
+        mbar_init(&bar_kcf[h], 1);
+        mbar_init(&bar_kce[h], kHalfKeys);
+        mbar_init(&bar_vcf[h], 1);
+        mbar_init(&bar_vce[h], kHalfKeys);
+      }
     }
     for (int t = 0; t < kNT; ++t) {
       mbar_init(&bar_s[t], 1);
@@ -412,8 +494,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
   }
   if (warp == 0) {
     tma_prefetch_desc(&p.tmQ);
-    tma_prefetch_desc(&p.tmK);
-    tma_prefetch_desc(&p.tmV);
+    if (!kQ4) {
+      tma_prefetch_desc(&p.tmK);
+      tma_prefetch_desc(&p.tmV);
+    }
   }
   if (warp == 2) {
     tmem_alloc(&tmem_sh, 512);
@@ -479,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
     // ------------------------------------------------------------ TMA producers
     // warp 0 loads Q and the K stages, warp 2 the V stages: a V stage waits for the
     // PVs of the stage it replaces, which must not hold back later K stages
-    setmaxnreg_dec<kRegsControl>();
+    if constexpr (!kQ4) setmaxnreg_dec<kRegsControl>();
     const bool is_k = warp == 0;
     if (elect_one_sync()) {
       ItemIter it;
@@ -513,16 +597,45 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
           for (int pg = 0; pg < kPagesPerTile; ++pg) pages[pg] = pg < npg ? pt[key0 / kPageSize + pg] : 0;
           // an out-of-range page id reads the TMA fill value (zeros); the request is
           // reported and zero-filled at exit
-          uint64_t* empty = is_k ? &bar_ke[s] : &bar_ve[s];
-          uint64_t* full = is_k ? &bar_kf[s] : &bar_vf[s];
-          uint8_t* dst = (is_k ? sK : sV) + s * S::kKVTile;
-          const CUtensorMap* map = is_k ? &p.tmK : &p.tmV;
-          ok = mbar_wait(empty, ph ^ 1u, &abort_sh);
-          if (!ok) break;
-          mbar_arrive_expect_tx(full, bytes);
-          for (int pg = 0; pg < npg; ++pg)
-            for (int db = 0; db < S::kDBlocks; ++db)
-              tma_load_4d(dst + db * (kBN * 128) + pg * (kPageSize * 128), map, full, db * 64, 0, item.g, pages[pg]);
+          if constexpr (kQ4) {
+            // codes and params of each half tile into its code slot (bulk copies of the
+            // contiguous per-page blocks); an out-of-range page id reads page 0 instead
+            // (the request is reported and zero-filled at exit)
+            (void)s;
+            (void)bytes;
+            const uint8_t* codes = is_k ? p.k_codes : p.v_codes;
+            const uint8_t* prm = is_k ? p.k_params : p.v_params;
+            constexpr uint32_t kPgCodes = kPageSize * S::kCodeRow, kPgParams = kPageSize * S::kParamRow;
+            for (int h = 0; h < 2 && ok; ++h) {
+              uint64_t* cfree = is_k ? &bar_kce[h] : &bar_vce[h];
+              uint64_t* cfull = is_k ? &bar_kcf[h] : &bar_vcf[h];
+              uint8_t* slot = smem + (is_k ? S::kKC : S::kVC) + h * S::kSlot;
+              ok = mbar_wait(cfree, (kv_it & 1u) ^ 1u, &abort_sh);
+              if (!ok) break;
+              const int pg0 = h * (kPagesPerTile / 2);
+              const int n_pg = max(0, min(kPagesPerTile / 2, npg - pg0));
+              mbar_arrive_expect_tx(cfull, (uint32_t)n_pg * (kPgCodes + kPgParams));
+              for (int i = 0; i < n_pg; ++i) {
+                int id = pages[pg0 + i];
+                if (id < 0 || (int64_t)id >= p.num_pages) id = 0;
+                const int64_t blk = (int64_t)id * p.Hkv + item.g;
+                bulk_g2s(slot + i * kPgCodes, codes + blk * kPgCodes, kPgCodes, cfull);
+                bulk_g2s(slot + S::kSlotParams + i * kPgParams, prm + blk * kPgParams, kPgParams, cfull);
+              }
+            }
+          } else {
+            uint64_t* empty = is_k ? &bar_ke[s] : &bar_ve[s];
+            uint64_t* full = is_k ? &bar_kf[s] : &bar_vf[s];
+            uint8_t* dst = (is_k ? sK : sV) + s * S::kKVTile;
+            const CUtensorMap* map = is_k ? &p.tmK : &p.tmV;
+            ok = mbar_wait(empty, ph ^ 1u, &abort_sh);
+            if (!ok) break;
+            mbar_arrive_expect_tx(full, bytes);
+            for (int pg = 0; pg < npg; ++pg)
+              for (int db = 0; db < S::kDBlocks; ++db)
+                tma_load_4d(dst + db * (kBN * 128) + pg * (kPageSize * 128), map, full, db * 64, 0, item.g,
+                            pages[pg]);
+          }
         }
         ++n_item;
       }
@@ -530,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
     __syncwarp();
   } else if (has_work && warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    setmaxnreg_dec<kRegsControl>();
+    if constexpr (!kQ4) setmaxnreg_dec<kRegsControl>();
     if (elect_one_sync()) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
@@ -558,7 +671,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
         const uint64_t b = dv0 + (uint64_t)((s * S::kKVTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(d, tmem + t * 128 + kk * 8, b + (uint64_t)((kk * 2048) >> 4), idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          mma_ts(d, tmem + t * 128 + kk * 8 + ((kQ4 && kk >= 4) ? 32 : 0), b + (uint64_t)((kk * 2048) >> 4), idesc_pv,
+                 (acc || kk > 0) ? 1u : 0u);
       };
       ItemIter it;
       iter_init(it, pv, cta);
@@ -645,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
     __syncwarp();
   } else if (has_work && warp == 3) {
     // ------------------------------------------------------------ page-table check
-    setmaxnreg_dec<kRegsControl>();
+    if constexpr (!kQ4) setmaxnreg_dec<kRegsControl>();
     // every needed page of each request this CTA touches
     ItemIter it;
     iter_init(it, pv, cta);
@@ -661,9 +775,46 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
       for (int k = lane; k < need; k += 32) bad |= (pt[k] < 0 || (int64_t)pt[k] >= p.num_pages);
       if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.ws_bits + item.b, TV_DEV_PAGE_OOB);
     }
+  } else if (kQ4 && has_work && warp >= 12) {
+    // ------------------------------------------------------------ 4-bit decoders
+    // warps 12-13 decode K, warps 14-15 V: thread i takes key row 64 h + i of half h
+    const bool is_k = warp < 14;
+    const int ri = tid - (is_k ? 384 : 448);
+    uint8_t* const stage0 = is_k ? sK : sV;
+    const uint8_t* const slots = smem + (is_k ? S::kKC : S::kVC);
+    ItemIter it;
+    iter_init(it, pv, cta);
+    Item item;
+    uint32_t kv_it = 0;
+    bool ok = true;
+    while (ok && iter_next(it, pv, cta, item)) {
+      const int L = p.prefix_len[item.b], N = p.n_nodes[item.b];
+      for (int tile = item.tile_begin; tile < item.tile_end && ok; ++tile, ++kv_it) {
+        const int s = kv_it % kStages;
+        const uint32_t ph = (kv_it / kStages) & 1u;
+        const int key0 = tile * kBN;
+        const int npg = min(kPagesPerTile, (L + N - key0 + kPageSize - 1) / kPageSize);
+        // the bf16 stage is free once the MMAs of the tile it held have completed
+        ok = warp_wait(is_k ? &bar_ke[s] : &bar_ve[s], ph ^ 1u, &abort_sh);
+        if (!ok) break;
+        uint8_t* const stage = stage0 + s * S::kKVTile;
+        for (int h = 0; h < 2; ++h) {
+          ok = warp_wait(is_k ? &bar_kcf[h] : &bar_vcf[h], kv_it & 1u, &abort_sh);
+          if (!ok) break;
+          const int r = h * kHalfKeys + ri;  // key row of the tile
+          if (r < npg * kPageSize)
+            decode_row_q4<D>(slots + h * S::kSlot + ri * S::kCodeRow,
+                             slots + h * S::kSlot + S::kSlotParams + ri * S::kParamRow, stage, r);
+          mbar_arrive(is_k ? &bar_kce[h] : &bar_vce[h]);
+        }
+        if (!ok) break;
+        fence_proxy_async_smem();  // the tensor pipe reads what these threads wrote
+        mbar_arrive(is_k ? &bar_kf[s] : &bar_vf[s]);
+      }
+    }
   } else if (has_work && warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
-    setmaxnreg_inc<kRegsSoftmax>();
+    if constexpr (!kQ4) setmaxnreg_inc<kRegsSoftmax>();
     const int t = (warp - 4) >> 2;
     const int r = (warp & 3) * 32 + lane;                 // row of the M tile = TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -709,27 +860,47 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
         tc_fence_after();
         if (!ok) break;
         const int key0 = (item.tile_begin + j) * kBN;             // first key of the stage
-        uint32_t v[kBN];
-        tmem_ld128(tS, v);
-        if (key0 + kBN > L) {
+        // S values of invisible keys become -inf
+        auto mask_keys = [&](uint32_t* x, int n, int k0) {
+          if (k0 + n > L) {
 #pragma unroll
-          for (int c0 = 0; c0 < kBN; c0 += 32) {
-            const uint32_t vis = visible32(key0 + c0, L, anc);
+            for (int c0 = 0; c0 < n; c0 += 32) {
+              const uint32_t vis = visible32(k0 + c0, L, anc);
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (!((vis >> c) & 1u)) v[c0 + c] = __float_as_uint(-INFINITY);
+              for (int c = 0; c < 32; ++c)
+                if (!((vis >> c) & 1u)) x[c0 + c] = __float_as_uint(-INFINITY);
+            }
           }
+        };
+        // row max of n values as four independent partial maxima of three-input steps
+        auto row_max = [&](const uint32_t* x, int n) {
+          float pm[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) pm[u] = fmaxf(__uint_as_float(x[2 * u]), __uint_as_float(x[2 * u + 1]));
+#pragma unroll
+          for (int c = 8; c < n; c += 8)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              pm[u] = fmax3(pm[u], __uint_as_float(x[c + 2 * u]), __uint_as_float(x[c + 2 * u + 1]));
+          return fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+        };
+        // 128 values of the row (bf16 cache), or the upper half of it (4-bit cache:
+        // the lower half is read for its maximum here and again for its probabilities)
+        constexpr int kW = kQ4 ? kBN / 2 : kBN;
+        uint32_t v[kW];
+        float mx;
+        if constexpr (kQ4) {
+          tmem_ld64(tS, v);
+          mask_keys(v, 64, key0);
+          const float mx0 = row_max(v, 64);
+          tmem_ld64(tS + 64, v);
+          mask_keys(v, 64, key0 + 64);
+          mx = fmaxf(mx0, row_max(v, 64));
+        } else {
+          tmem_ld128(tS, v);
+          mask_keys(v, kBN, key0);
+          mx = row_max(v, kBN);
         }
-        // row max as four independent partial maxima of three-input steps
-        float pm[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) pm[u] = __uint_as_float(v[u]);
-#pragma unroll
-        for (int c = 4; c < kBN; c += 8)
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            pm[u] = fmax3(pm[u], __uint_as_float(v[c + 2 * u]), __uint_as_float(v[c + 2 * u + 1]));
-        const float mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
         const float m_new = fmaxf(m_run, mx * sl2);
         const bool grow = m_new > m_run + kRescaleLog2;
         const float alpha = grow ? ex2_approx(m_run - m_new) : 1.f;  // 0 when m_run = -inf
@@ -760,16 +931,29 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
         // scaling and the row sum run two lanes per instruction
         const uint64_t sl2x2 = f2_pack(sl2, sl2), negm2 = f2_pack(-m_use, -m_use);
         uint64_t ps2[2] = {0ull, 0ull};
+        auto exps = [&](uint32_t* x, int n) {
 #pragma unroll
-        for (int c = 0; c < kBN; c += 2) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), sl2x2, negm2), x0, x1);
-          const float e0 = ex2_approx(x0);
-          const float e1 = ex2_approx(x1);
-          ps2[(c >> 1) & 1] = f2_add(ps2[(c >> 1) & 1], f2_pack(e0, e1));
-          v[c >> 1] = pack_bf16x2(e0, e1);
+          for (int c = 0; c < n; c += 2) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(x[c]), __uint_as_float(x[c + 1])), sl2x2, negm2), x0, x1);
+            const float e0 = ex2_approx(x0);
+            const float e1 = ex2_approx(x1);
+            ps2[(c >> 1) & 1] = f2_add(ps2[(c >> 1) & 1], f2_pack(e0, e1));
+            x[c >> 1] = pack_bf16x2(e0, e1);
+          }
+        };
+        if constexpr (kQ4) {
+          // P of keys 64-127 into columns 64-95, then of keys 0-63 into columns 0-31
+          exps(v, 64);
+          tmem_st32(tS + 64, v);
+          tmem_ld64(tS, v);
+          mask_keys(v, 64, key0);
+          exps(v, 64);
+          tmem_st32(tS, v);
+        } else {
+          exps(v, kBN);
+          tmem_st64(tS, v);
         }
-        tmem_st64(tS, v);
         float ps[4];
         f2_unpack(ps2[0], ps[0], ps[1]);
         f2_unpack(ps2[1], ps[2], ps[3]);
@@ -930,9 +1114,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
       if (entry == 0 && bits == 0) continue;
       any_timeout |= (bits & TV_DEV_TIMEOUT) != 0;
       uint4* dst = reinterpret_cast<uint4*>(p.out + (int64_t)b * per_req);
-      for (int64_t i = tid; i < per_req / 8; i += kThreads) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      for (int64_t i = tid; i < per_req / 8; i += kNThreads) dst[i] = make_uint4(0u, 0u, 0u, 0u);
       if (p.lse)
-        for (int64_t i = tid; i < (int64_t)p.n_max * p.Hq; i += kThreads) p.lse[(int64_t)b * p.n_max * p.Hq + i] = 0.f;
+        for (int64_t i = tid; i < (int64_t)p.n_max * p.Hq; i += kNThreads) p.lse[(int64_t)b * p.n_max * p.Hq + i] = 0.f;
       __syncthreads();
       if (tid == 0) {
         p.status[b] = entry | bits;
@@ -943,7 +1127,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attn_kernel(const __grid_c
       // a split that gave up never took its ticket: clear them all for the next call
       __syncthreads();
       const int64_t n_tick = (int64_t)p.B * p.Hkv * p.mp_max * kNT;
-      for (int64_t i = tid; i < n_tick; i += kThreads) p.ws_tickets[i] = 0;
+      for (int64_t i = tid; i < n_tick; i += kNThreads) p.ws_tickets[i] = 0;
     }
     if (tid == 0) *p.ws_exit = 0;
   }
@@ -995,21 +1179,31 @@ static bool make_map4(CUtensorMap* m, const void* base, const uint64_t dims[4], 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool kQ4>
 static int launch(const AttnParams& ap, int grid, cudaStream_t st) {
-  TV_CUDA_CHECK(ensure_smem_attr((const void*)verify_attn_kernel<D>, Smem<D>::kAlloc));
-  TV_CUDA_CHECK(launch_pdl(verify_attn_kernel<D>, dim3(grid), dim3(kThreads), (size_t)Smem<D>::kAlloc, st, ap));
+  using S = Smem<D, kQ4>;
+  TV_CUDA_CHECK(ensure_smem_attr((const void*)verify_attn_kernel<D, kQ4>, S::kAlloc));
+  TV_CUDA_CHECK(launch_pdl(verify_attn_kernel<D, kQ4>, dim3(grid), dim3(kQ4 ? kThreadsQ4 : kThreads),
+                           (size_t)S::kAlloc, st, ap));
   TV_CUDA_CHECK(cudaGetLastError());
   return TV_OK;
 }
 
 // Argument checks and parameter set-up shared by the entry points.
+// With q4 set, k_cache and v_cache are the code arrays and the params arrays
+// come in k_params / v_params; no tensor map is made for them.
 static int prepare(const void* q, const void* k_cache, const void* v_cache, int64_t num_pages,
                    const int32_t* page_table, int max_pages, const int32_t* prefix_len, const int32_t* n_nodes,
                    const uint64_t* anc_mask, int B, int n_max, int Hq, int Hkv, int D, int page_size, float scale,
-                   void* out, float* lse, int32_t* status, AttnParams* ap) {
+                   void* out, float* lse, int32_t* status, AttnParams* ap, bool q4 = false,
+                   const void* k_params = nullptr, const void* v_params = nullptr) {
   TV_REQUIRE(q && k_cache && v_cache && page_table && prefix_len && n_nodes && anc_mask && out && status,
              TV_ERR_INVALID_ARG, "tv_tree_verify_attn: NULL pointer");
+  TV_REQUIRE(!q4 || (k_params && v_params), TV_ERR_INVALID_ARG, "tv_tree_verify_attn_q4: NULL params pointer");
+  TV_REQUIRE(!q4 || (aligned16(k_params) && aligned16(v_params)), TV_ERR_INVALID_ARG,
+             "tv_tree_verify_attn_q4: params must be 16-byte aligned");
+  TV_REQUIRE(!q4 || B <= kMaxBatchQ4, TV_ERR_UNSUPPORTED, "tv_tree_verify_attn_q4: B = %d not in [0, %d]", B,
+             kMaxBatchQ4);
   TV_REQUIRE(page_size == kPageSize, TV_ERR_UNSUPPORTED, "tv_tree_verify_attn: page_size %d != 16", page_size);
   TV_REQUIRE(D == 64 || D == 128, TV_ERR_UNSUPPORTED, "tv_tree_verify_attn: D = %d not in {64, 128}", D);
   TV_REQUIRE(Hq >= 1 && Hkv >= 1 && Hq % Hkv == 0, TV_ERR_UNSUPPORTED,
@@ -1034,13 +1228,19 @@ static int prepare(const void* q, const void* k_cache, const void* v_cache, int6
       const uint32_t box[4] = {64, (uint32_t)G, (uint32_t)q_box_nodes, 1};
       TV_REQUIRE(make_map4(&ap->tmQ, q, dims, str, box), TV_ERR_CUDA, "tv_tree_verify_attn: tensor map for q failed");
     }
-    {
+    if (!q4) {
       const uint64_t dims[4] = {(uint64_t)D, (uint64_t)kPageSize, (uint64_t)Hkv, (uint64_t)num_pages};
       const uint64_t str[3] = {(uint64_t)D * 2, (uint64_t)kPageSize * D * 2, (uint64_t)Hkv * kPageSize * D * 2};
       const uint32_t box[4] = {64, (uint32_t)kPageSize, 1, 1};
       TV_REQUIRE(make_map4(&ap->tmK, k_cache, dims, str, box) && make_map4(&ap->tmV, v_cache, dims, str, box),
                  TV_ERR_CUDA, "tv_tree_verify_attn: tensor map for the KV cache failed");
     }
+  }
+  if (q4) {
+    ap->k_codes = static_cast<const uint8_t*>(k_cache);
+    ap->v_codes = static_cast<const uint8_t*>(v_cache);
+    ap->k_params = static_cast<const uint8_t*>(k_params);
+    ap->v_params = static_cast<const uint8_t*>(v_params);
   }
   ap->page_table = page_table;
   ap->prefix_len = prefix_len;
@@ -1099,7 +1299,30 @@ extern "C" int tv_tree_verify_attn(const void* q, const void* k_cache, const voi
   TV_REQUIRE(tv::aligned16(ws), TV_ERR_INVALID_ARG, "tv_tree_verify_attn: workspace must be 16-byte aligned");
   bind_workspace(&ap, wl, static_cast<uint8_t*>(ws));
   cudaStream_t st = tv::as_stream(stream);
-  return D == 128 ? launch<128>(ap, grid, st) : launch<64>(ap, grid, st);
+  return D == 128 ? launch<128, false>(ap, grid, st) : launch<64, false>(ap, grid, st);
+}
+
+extern "C" int tv_tree_verify_attn_q4(const void* q, const uint8_t* k_codes, const void* k_params,
+                                      const uint8_t* v_codes, const void* v_params, int64_t num_pages,
+                                      const int32_t* page_table, int max_pages, const int32_t* prefix_len,
+                                      const int32_t* n_nodes, const uint64_t* anc_mask, int B, int n_max, int Hq,
+                                      int Hkv, int D, int page_size, float scale, void* out, float* lse, void* ws,
+                                      size_t ws_bytes, int32_t* status, void* stream) {
+  using namespace tv::attn;
+  tv::clear_error();
+  AttnParams ap;
+  const int rc = prepare(q, k_codes, v_codes, num_pages, page_table, max_pages, prefix_len, n_nodes, anc_mask, B,
+                         n_max, Hq, Hkv, D, page_size, scale, out, lse, status, &ap, true, k_params, v_params);
+  if (rc != TV_OK) return rc;
+  if (B == 0) return TV_OK;
+  const int grid = tv::current_sm_count();
+  const WsLayout wl = ws_layout(B, n_max, Hq, Hkv, D, grid);
+  TV_REQUIRE(ws != nullptr && ws_bytes >= wl.total, TV_ERR_WORKSPACE,
+             "tv_tree_verify_attn_q4: workspace %zu bytes < %zu", ws_bytes, wl.total);
+  TV_REQUIRE(tv::aligned16(ws), TV_ERR_INVALID_ARG, "tv_tree_verify_attn_q4: workspace must be 16-byte aligned");
+  bind_workspace(&ap, wl, static_cast<uint8_t*>(ws));
+  cudaStream_t st = tv::as_stream(stream);
+  return D == 128 ? launch<128, true>(ap, grid, st) : launch<64, true>(ap, grid, st);
 }
 
 // ---------------------------------------------------------------- built-in scratch variant
@@ -1164,5 +1387,5 @@ extern "C" int tv_tree_verify_attn_noalloc(const void* q, const void* k_cache, c
   // clear the counters and error bits the kernel expects to start at zero
   TV_CUDA_CHECK(cudaMemsetAsync(ws, 0, wl.part_lse, st));
   bind_workspace(&ap, wl, static_cast<uint8_t*>(ws));
-  return D == 128 ? launch<128>(ap, grid, st) : launch<64>(ap, grid, st);
+  return D == 128 ? launch<128, false>(ap, grid, st) : launch<64, false>(ap, grid, st);
 }

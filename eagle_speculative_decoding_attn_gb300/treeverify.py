@@ -53,6 +53,8 @@ _SIGNATURES = {
     "tv_tree_expand": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, _P, _P]),
     "tv_kv_prune_pages": (_I, [_P, _I, _P, _I64, _P, _P, _P, _I, _I, _P, _I64, _P, _P, _P]),
     "tv_kv_quantize_q4": (_I, [_P, _I64, _I, _P, _P, _P]),
+    "tv_tree_verify_attn_q4": (_I, [_P, _P, _P, _P, _P, _I64, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
+                                    _P, _P, _SZ, _P, _P]),
     "tv_selftest_wait_timeout": (_I, [_P, _P]),
     "tv_last_error": (ctypes.c_char_p, []),
     "tv_version": (ctypes.c_char_p, []),
@@ -310,6 +312,40 @@ def kv_quantize_q4(x: torch.Tensor, *, codes=None, params=None):
     rc = load_library().tv_kv_quantize_q4(_ptr(x), rows, D, _ptr(codes), _ptr(params), _stream(x.device))
     _check(rc, "tv_kv_quantize_q4")
     return codes, params
+
+
+def tree_verify_attn_q4(q: torch.Tensor, k_codes: torch.Tensor, k_params: torch.Tensor, v_codes: torch.Tensor,
+                        v_params: torch.Tensor, page_table: torch.Tensor, prefix_len: torch.Tensor,
+                        n_nodes: torch.Tensor, anc_mask: torch.Tensor, scale: float, status: torch.Tensor, *,
+                        out=None, lse=None, want_lse=True, workspace=None):
+    """Tree-masked paged attention over a 4-bit cache: codes uint8
+    [num_pages, Hkv, 16, D/2] and params float16 [num_pages, Hkv, 16, 2*D/32]
+    for K and for V (the format of ``kv_quantize_q4``); everything else as
+    ``tree_verify_attn``, whose workspace it shares."""
+    B, n_max, Hq, D = q.shape
+    num_pages, Hkv, P, Dh = k_codes.shape
+    dev = q.device
+    if q.dtype != torch.bfloat16:
+        raise TreeVerifyError("q must be bfloat16")
+    if Dh * 2 != D or tuple(v_codes.shape) != tuple(k_codes.shape):
+        raise TreeVerifyError("k_codes / v_codes shapes do not match q")
+    for t, nm in ((k_codes, "k_codes"), (v_codes, "v_codes")):
+        _expect(t, torch.uint8, (num_pages, Hkv, P, D // 2), nm)
+    for t, nm in ((k_params, "k_params"), (v_params, "v_params")):
+        _expect(t, torch.float16, (num_pages, Hkv, P, 2 * D // 32), nm)
+    _expect(page_table, torch.int32, page_table.shape, "page_table")
+    _expect(anc_mask, torch.int64, (B, n_max), "anc_mask")
+    out = torch.empty_like(q) if out is None else out
+    if lse is None and want_lse:
+        lse = torch.empty((B, n_max, Hq), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_attn_workspace(B, n_max, Hq, Hkv, D, dev)
+    rc = load_library().tv_tree_verify_attn_q4(
+        _ptr(q), _ptr(k_codes), _ptr(k_params), _ptr(v_codes), _ptr(v_params), num_pages, _ptr(page_table),
+        page_table.shape[1], _ptr(prefix_len), _ptr(n_nodes), _ptr(anc_mask), B, n_max, Hq, Hkv, D, P,
+        float(scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev))
+    _check(rc, "tv_tree_verify_attn_q4")
+    return out, lse
 
 
 def version() -> str:

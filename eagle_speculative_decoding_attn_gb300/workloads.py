@@ -245,6 +245,13 @@ class Workload:
         qb = int(np.sum(self.n_nodes)) * self.Hq * self.D * 2
         return kv + qb
 
+    def attn_bytes_q4(self) -> int:
+        """attn_bytes with K and V in the 4-bit format: D/2 code bytes and D/32
+        (scale, zero) fp16 pairs per row."""
+        kv = int(np.sum(self.prefix_len.astype(np.int64) + self.n_nodes)) * self.Hkv * (self.D // 2 + self.D // 8) * 2
+        qb = int(np.sum(self.n_nodes)) * self.Hq * self.D * 2
+        return kv + qb
+
     def attn_flops(self) -> int:
         tot = 0
         for b in range(self.B):

@@ -351,6 +351,31 @@ int tv_kv_prune_pages(int32_t* page_table, int max_pages, int32_t* refcount, int
 int tv_kv_quantize_q4(const void* x, int64_t rows, int D, uint8_t* codes, void* params, void* stream);
 
 /*
+ * tv_tree_verify_attn_q4 — tv_tree_verify_attn over a paged KV cache held in
+ * the 4-bit format of tv_kv_quantize_q4 (troisinh.com "EAGLE - Draft head
+ * ...": EAGLE pairs with an INT4 KV cache).  The result is that of
+ * tv_tree_verify_attn on the decoded cache: every K and V value is first
+ * decoded to bf16(fp32(code * scale + zero)) with its row's (scale, zero) of
+ * its 32-dim group; the kernel decodes each page in shared memory as it
+ * streams, and the cache is read at about 0.31 (D = 128) of the bf16 bytes.
+ *
+ *  q          bf16 [B, n_max, Hq, D]                    (16-byte aligned)
+ *  k_codes    uint8 [num_pages, Hkv, 16, D / 2]         (16-byte aligned)
+ *  k_params   fp16  [num_pages, Hkv, 16, 2 * D / 32]    (16-byte aligned)
+ *  v_codes, v_params  the same for V
+ *  every other argument, the outputs, the workspace (tv_tree_verify_attn_workspace
+ *  of the same sizes) and the status bits as for tv_tree_verify_attn.
+ *
+ * Returns TV_ERR_UNSUPPORTED for D not in {64,128}, page_size != 16,
+ * Hq % Hkv != 0, 128 % G != 0 or B > 256.  One kernel launch.
+ */
+int tv_tree_verify_attn_q4(const void* q, const uint8_t* k_codes, const void* k_params, const uint8_t* v_codes,
+                           const void* v_params, int64_t num_pages, const int32_t* page_table, int max_pages,
+                           const int32_t* prefix_len, const int32_t* n_nodes, const uint64_t* anc_mask, int B,
+                           int n_max, int Hq, int Hkv, int D, int page_size, float scale, void* out, float* lse,
+                           void* ws, size_t ws_bytes, int32_t* status, void* stream);
+
+/*
  * tv_selftest_wait_timeout — self-test of the bounded waits every kernel uses
  * (no counterpart in the pages).  One CTA waits on an mbarrier that nothing
  * ever completes; after the wait limit (1 s) it ORs TV_DEV_TIMEOUT into
