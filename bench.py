@@ -737,12 +737,42 @@ def main():
         com_graph.replay()
     y1.record(stream)
     torch.cuda.synchronize()
+    # the attention over each copy's first-layer cache encoded in the 4-bit format
+    q4c = []
+    for cp in copies:
+        kc, kp = tvb.kv_quantize_q4(cp["k"][0])
+        vc, vp = tvb.kv_quantize_q4(cp["v"][0])
+        q4c.append((kc, kp, vc, vp))
+
+    def attn_q4_call(cp, c4):
+        tvb.tree_verify_attn_q4(cp["q"], *c4, shared["page_table"], shared["prefix_len"], shared["n_nodes"],
+                                cp["anc"], w.scale, cp["status"], out=cp["out"], lse=cp["lse"], workspace=cp["ws"])
+
+    for cp, c4 in zip(copies, q4c):
+        attn_q4_call(cp, c4)
+    torch.cuda.synchronize()
+    q4_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(q4_graph, stream=side):
+            for cp, c4 in zip(copies, q4c):
+                attn_q4_call(cp, c4)
+    torch.cuda.synchronize()
+    q4_graph.replay()
+    z0, z1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    z0.record(stream)
+    for _ in range(reps):
+        q4_graph.replay()
+    z1.record(stream)
+    torch.cuda.synchronize()
+    q4_ok = all(bool((cp["status"] == 0).all().item()) for cp in copies)
+    del q4c, q4_graph
     expand = time_expand(args, W, tvb, torch, np, dev, stream, B, n_max, V, cfg)
     clk = clocks.stop()
     attn_us = a0.elapsed_time(a1) * 1000.0 / (reps * R)
     ac_us = c0.elapsed_time(c1) * 1000.0 / (reps * R)
     accept_us = x0.elapsed_time(x1) * 1000.0 / (reps * R)
     commit_us = y0.elapsed_time(y1) * 1000.0 / (reps * R)
+    attn_q4_us = z0.elapsed_time(z1) * 1000.0 / (reps * R)
     # bytes of the accept and commit rooflines: logits rows (all nodes; the accepted
     # path's nodes only, the lower bound) and the moved K/V rows of every layer
     acc_len = copies[0]["acc"][0].cpu().numpy().astype(np.int64)
@@ -954,6 +984,10 @@ def main():
                    "bytes": commit_bytes, "bytes_one_layer": commit_bytes // max(layers, 1),
                    "hbm_us": commit_bytes / (hbm * 1e3)},
         "nodes_per_s_attn_accept_commit": nodes_total / ((attn_us + accept_us + commit_us) * 1e-6),
+        "attn_q4": {"us": attn_q4_us, "status_ok": q4_ok, "bytes": w.attn_bytes_q4(),
+                    "tbps": w.attn_bytes_q4() / attn_q4_us / 1e6,
+                    "roofline_frac": max(w.attn_bytes_q4() / (hbm * 1e9), t_tc) / (attn_q4_us * 1e-6),
+                    "cache": "the same first-layer K/V encoded by tv_kv_quantize_q4, same rotation"},
         "expand": dict(expand, us_per_level=expand_us / expand["levels"],
                        hbm_us=expand["bytes"] / (hbm * 1e3), hbm_frac=expand["bytes"] / (hbm * 1e3) / expand_us),
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,

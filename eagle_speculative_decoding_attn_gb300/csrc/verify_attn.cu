@@ -377,14 +377,22 @@ __device__ void merge_items(const AttnParams& p, const Item& it, int mtile, int 
   }
 }
 
-template <int D>
+template <int D, bool kQ4>
 __device__ __forceinline__ void merge_tile(const AttnParams& p, const Item& it, int mtile, int n_rows, int r) {
   // (splits per round trip, 16-byte loads per split): about 128 registers of loads
-  // and accumulators either way
-  if (it.n_splits <= 2) merge_items<D, 2, (D >= 128 ? 8 : 4)>(p, it, mtile, n_rows, r);
-  else if (it.n_splits <= 4) merge_items<D, 4, 4>(p, it, mtile, n_rows, r);
-  else if (it.n_splits <= 6) merge_items<D, 6, 4>(p, it, mtile, n_rows, r);
-  else merge_items<D, 8, 2>(p, it, mtile, n_rows, r);
+  // and accumulators either way; half of that where the launch leaves 128 registers
+  // a thread (4-bit cache)
+  if constexpr (kQ4) {
+    if (it.n_splits <= 2) merge_items<D, 2, (D >= 128 ? 4 : 2)>(p, it, mtile, n_rows, r);
+    else if (it.n_splits <= 4) merge_items<D, 4, 2>(p, it, mtile, n_rows, r);
+    else if (it.n_splits <= 6) merge_items<D, 6, 2>(p, it, mtile, n_rows, r);
+    else merge_items<D, 8, 1>(p, it, mtile, n_rows, r);
+  } else {
+    if (it.n_splits <= 2) merge_items<D, 2, (D >= 128 ? 8 : 4)>(p, it, mtile, n_rows, r);
+    else if (it.n_splits <= 4) merge_items<D, 4, 4>(p, it, mtile, n_rows, r);
+    else if (it.n_splits <= 6) merge_items<D, 6, 4>(p, it, mtile, n_rows, r);
+    else merge_items<D, 8, 2>(p, it, mtile, n_rows, r);
+  }
 }
 
 // Decodes key row r of a 4-bit code slot into a bf16 K or V stage, laid out as
@@ -671,8 +679,7 @@ __global__ void __launch_bounds__(kQ4 ? kThreadsQ4 : kThreads, 1)
         const uint64_t b = dv0 + (uint64_t)((s * S::kKVTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(d, tmem + t * 128 + kk * 8 + ((kQ4 && kk >= 4) ? 32 : 0), b + (uint64_t)((kk * 2048) >> 4), idesc_pv,
-                 (acc || kk > 0) ? 1u : 0u);
+          mma_ts(d, tmem + t * 128 + kk * 8, b + (uint64_t)((kk * 2048) >> 4), idesc_pv, (acc || kk > 0) ? 1u : 0u);
       };
       ItemIter it;
       iter_init(it, pv, cta);
@@ -884,8 +891,8 @@ __global__ void __launch_bounds__(kQ4 ? kThreadsQ4 : kThreads, 1)
               pm[u] = fmax3(pm[u], __uint_as_float(x[c + 2 * u]), __uint_as_float(x[c + 2 * u + 1]));
           return fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
         };
-        // 128 values of the row (bf16 cache), or the upper half of it (4-bit cache:
-        // the lower half is read for its maximum here and again for its probabilities)
+        // 128 values of the row (bf16 cache), or 64 at a time for the maximum (4-bit
+        // cache: the row is read again in chunks of 32 for its probabilities)
         constexpr int kW = kQ4 ? kBN / 2 : kBN;
         uint32_t v[kW];
         float mx;
@@ -943,13 +950,16 @@ __global__ void __launch_bounds__(kQ4 ? kThreadsQ4 : kThreads, 1)
           }
         };
         if constexpr (kQ4) {
-          // P of keys 64-127 into columns 64-95, then of keys 0-63 into columns 0-31
-          exps(v, 64);
-          tmem_st32(tS + 64, v);
-          tmem_ld64(tS, v);
-          mask_keys(v, 64, key0);
-          exps(v, 64);
-          tmem_st32(tS, v);
+          // chunk c of 32 keys: its P (16 packed columns) goes to columns 16c.., all
+          // of which were read before (the layout the bf16 path writes in one step)
+#pragma unroll 1
+          for (int c0 = 0; c0 < kBN; c0 += 32) {
+            uint32_t x[32];
+            tmem_ld32(tS + c0, x);
+            mask_keys(x, 32, key0 + c0);
+            exps(x, 32);
+            tmem_st16(tS + c0 / 2, x);
+          }
         } else {
           exps(v, kBN);
           tmem_st64(tS, v);
@@ -1083,7 +1093,7 @@ __global__ void __launch_bounds__(kQ4 ? kThreadsQ4 : kThreads, 1)
         if (ticket_sh[t] == item.n_splits - 1) {
           __threadfence();
           const int n_rows = min(kBM, N * G - (item.mp * kNT + mtile) * kBM);  // valid rows of the M tile
-          merge_tile<D>(p, item, mtile, n_rows, r);
+          merge_tile<D, kQ4>(p, item, mtile, n_rows, r);
           if (r == 0) p.ws_tickets[tick_idx] = 0;  // ready for the next call
         }
       }
