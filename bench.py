@@ -213,6 +213,20 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def packed_views(buf, specs):
+    """Views of a flat uint8 tensor as the (name, dtype, shape) arrays of `specs`,
+    each starting on a 256-byte boundary; returns ({name: view}, total bytes).
+    With buf None only the size is computed."""
+    import numpy as np
+    views, off = {}, 0
+    for name, dtype, shape in specs:
+        n = int(np.prod(shape)) * dtype.itemsize
+        if buf is not None:
+            views[name] = buf[off:off + n].view(dtype).view(shape)
+        off = (off + n + 255) // 256 * 256
+    return views, off
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -614,6 +628,12 @@ def main():
                   page_table=g(w.page_table), tokens=g(w.tokens), u_accept=g(w.u_accept), u_sample=g(w.u_sample))
     k0, v0, q0, t0 = bf(w.k_bits), bf(w.v_bits), bf(w.q_bits), g(w.target_logits)
     d0 = g(w.draft_logits) if sampling else None
+    # the step's results (accept and commit outputs) in one buffer per copy, so that
+    # one device-to-host copy reads them back
+    res_specs = [("accept_len", torch.int32, (B,)), ("path_nodes", torch.int32, (B, n_max)),
+                 ("out_tokens", torch.int32, (B, n_max + 1)), ("slots", torch.int64, (B, n_max)),
+                 ("new_len", torch.int32, (B,))]
+    _, res_bytes = packed_views(None, res_specs)
     copies = []
     for _ in range(R):
         copies.append(dict(
@@ -626,11 +646,10 @@ def main():
             depth=torch.empty((B, n_max), dtype=torch.int32, device=dev),
             status=torch.empty((B,), dtype=torch.int32, device=dev),
             out=torch.empty_like(q0), lse=torch.empty((B, n_max, Hq), dtype=torch.float32, device=dev),
-            acc=(torch.empty((B,), dtype=torch.int32, device=dev),
-                 torch.empty((B, n_max), dtype=torch.int32, device=dev),
-                 torch.empty((B, n_max + 1), dtype=torch.int32, device=dev)),
-            com=(torch.empty((B, n_max), dtype=torch.int64, device=dev),
-                 torch.empty((B,), dtype=torch.int32, device=dev))))
+            res=torch.empty(res_bytes, dtype=torch.uint8, device=dev)))
+        rv, _ = packed_views(copies[-1]["res"], res_specs)
+        copies[-1]["acc"] = (rv["accept_len"], rv["path_nodes"], rv["out_tokens"])
+        copies[-1]["com"] = (rv["slots"], rv["new_len"])
     del k0, v0
 
     def mask_call(cp):
@@ -791,19 +810,25 @@ def main():
                        prefix_len=w.prefix_len, page_table=w.page_table, tokens=w.tokens)
         if sampling:
             host_in.update(draft=w.draft_logits, u_accept=w.u_accept, u_sample=w.u_sample)
-        pinned = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host_in.items()}
-        dev_in = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in pinned.items()}
-        h2d_bytes = sum(v.numel() * v.element_size() for v in pinned.values())
-        cp0 = copies[0]
-        res_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory()
-                    for t in (cp0["acc"][0], cp0["acc"][1], cp0["acc"][2], cp0["com"][1], cp0["com"][0])]
-        d2h = sum(t.numel() * t.element_size() for t in res_host)
-
-        dev_ins = [dev_in] + [{k2: torch.empty_like(v) for k2, v in dev_in.items()} for _ in range(R - 1)]
+        # every input of a step packed in one pinned buffer and one device buffer per
+        # rotated copy: one host-to-device copy a step (and one copy back of the results)
+        in_specs = [(k, torch.from_numpy(np.ascontiguousarray(v)).dtype, v.shape) for k, v in host_in.items()]
+        _, in_bytes = packed_views(None, in_specs)
+        pinned_buf = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+        pinned, _ = packed_views(pinned_buf, in_specs)
+        for k, v in host_in.items():
+            pinned[k].copy_(torch.from_numpy(np.ascontiguousarray(v)))
+        h2d_bytes = in_bytes  # the copied buffer, 256-byte padding between arrays included
+        dev_bufs = [torch.empty(in_bytes, dtype=torch.uint8, device=dev) for _ in range(R)]
+        dev_ins = [packed_views(b, in_specs)[0] for b in dev_bufs]
+        res_host_buf = torch.empty(res_bytes, dtype=torch.uint8).pin_memory()
+        res_host_v, _ = packed_views(res_host_buf, res_specs)
+        res_names = ["accept_len", "path_nodes", "out_tokens", "new_len", "slots"]
+        res_host = [res_host_v[n] for n in res_names]
+        d2h = res_bytes
 
         def h2d(k):
-            for kk in pinned:
-                dev_ins[k % R][kk].copy_(pinned[kk], non_blocking=True)
+            dev_bufs[k % R].copy_(pinned_buf, non_blocking=True)
 
         def compute(k):
             cpk = copies[k % R]
@@ -818,8 +843,7 @@ def main():
                                   dev_in.get("u_sample"), st, outputs=cpk["acc"], workspace=cpk["aws"])
             com = tvb.kv_commit_path(cpk["k"], cpk["v"], dev_in["page_table"], dev_in["prefix_len"],
                                      dev_in["n_nodes"], acc[0], acc[1], st, outputs=cpk["com"])
-            for hdst, dsrc in zip(res_host, [acc[0], acc[1], acc[2], com[1], com[0]]):
-                hdst.copy_(dsrc, non_blocking=True)
+            res_host_buf.copy_(cpk["res"], non_blocking=True)
 
         def e2e_step(k):
             h2d(k)
@@ -867,36 +891,30 @@ def main():
         last = copies[(K2 - 1) % R]
         landed = all(torch.equal(h, d.cpu()) for h, d in zip(
             res_host, [last["acc"][0], last["acc"][1], last["acc"][2], last["com"][1], last["com"][0]]))
-        # (c) pipelined: the host->device copy of step i+1 runs on a copy stream while step i
-        # computes (each rotated copy has its own input buffers; a copy waits for the
-        # compute that last read its buffers)
+        # (c) pipelined: one CUDA graph per step holds the host->device copy of the next
+        # step's inputs on a copy stream (forked from and joined back into the graph)
+        # beside this step's compute; each rotated copy has its own input buffers, so
+        # the copy never writes what the compute reads, and consecutive graphs run in
+        # order, so step k+1 reads what graph k copied. The host issues one replay a step.
         copy_stream = torch.cuda.Stream(dev)
-        h2d_graphs, comp_graphs = [], []
+        pipe_graphs = []
         with torch.cuda.stream(side):
             for k in range(R):
-                g1, g2 = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g1, stream=side):
-                    h2d(k)
-                with torch.cuda.graph(g2, stream=side):
+                gph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gph, stream=side):
+                    copy_stream.wait_stream(side)      # fork
+                    with torch.cuda.stream(copy_stream):
+                        h2d(k + 1)
                     compute(k)
-                h2d_graphs.append(g1)
-                comp_graphs.append(g2)
+                    side.wait_stream(copy_stream)      # join
+                pipe_graphs.append(gph)
         torch.cuda.synchronize()
-        copied = [torch.cuda.Event() for _ in range(R)]
-        done = [torch.cuda.Event() for _ in range(R)]
-        for e in done:
-            e.record(stream)
+        h2d(0)
+        torch.cuda.synchronize()
 
         def pipelined(n):
             for i in range(n):
-                k = i % R
-                copy_stream.wait_event(done[k])
-                with torch.cuda.stream(copy_stream):
-                    h2d_graphs[k].replay()
-                    copied[k].record(copy_stream)
-                stream.wait_event(copied[k])
-                comp_graphs[k].replay()
-                done[k].record(stream)
+                pipe_graphs[i % R].replay()
         pipelined(min(Wm, 5))
         barrier()
         for t in res_host:
@@ -917,8 +935,9 @@ def main():
                "steps": K2, "results_landed_on_host": bool(landed),
                "note": "per step: queries, tree, logits and uniforms copied from pinned host memory, mask + "
                        "attention + accept + commit through the library, results copied back to pinned host "
-                       "memory; CUDA graphs, the copy of the next step overlapping this step's compute on a "
-                       "second stream; KV cache resident in HBM; wall clock and events, the larger",
+                       "memory; one CUDA graph per step, holding the copy of the next step's inputs on a second "
+                       "stream beside this step's compute; KV cache resident in HBM; wall clock and events, the "
+                       "larger",
                "serial_graph": {"value": nodes_b / (graph_ms / 1000.0), "ms_per_step": graph_ms,
                                 "note": "copy, compute and copy back in one CUDA graph per step, no overlap"},
                "eager": {"value": nodes_b / (eager_ms / 1000.0), "ms_per_step": eager_ms,
