@@ -305,14 +305,16 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kAccThreads, 1)
   float* wt = dyn;             // sampling: current target weights of this slice
   float* wq = dyn + p.chunk;   // sampling: draft weights of this slice
 
-  griddep_wait();
+  // Everything up to the outputs reads only inputs (tree, logits, uniforms, the
+  // mask kernel's words, which precede the previous kernel), so it runs while the
+  // previous kernel finishes; status, which that kernel may write, is read and
+  // written after the wait before the outputs.
   // ---- tree setup and validation (every CTA redundantly, identical results):
   // one node per thread, then thread 0 builds the child lists from shared memory
   const int N = p.n_nodes[b];
-  const int st_in = p.status[b];
   const bool n_ok = N >= 1 && N <= n_max;
   bool sbad = false, tbad = false;
-  if (st_in == 0 && n_ok && tid < N) {
+  if (n_ok && tid < N) {
     const int pi = p.parents[(int64_t)b * n_max + tid];
     const int ti = p.tokens[(int64_t)b * n_max + tid];
     sh.par[tid] = pi;
@@ -327,7 +329,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kAccThreads, 1)
   }
   const bool any_s = __syncthreads_or(sbad) != 0;
   const bool any_t = __syncthreads_or(tbad) != 0;
-  const int bad = st_in != 0 ? -1 : (!n_ok || any_s) ? TV_DEV_BAD_TREE : (any_t ? TV_DEV_BAD_TOKEN : 0);
+  const int bad = (!n_ok || any_s) ? TV_DEV_BAD_TREE : (any_t ? TV_DEV_BAD_TOKEN : 0);
   if (bad == 0 && tid < kMaxNodes) {  // warps 0 and 1, whole
     // children of node tid, then the exclusive scan of the counts over the nodes
     int cnt = 0;
@@ -360,384 +362,388 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kAccThreads, 1)
     sh.kids[sh.kid_off[pj] + before] = tid;
   }
   __syncthreads();
-  if (sh.bad != 0) {
-    if (rank == 0) {
-      if (tid == 0) {
-        p.accept_len[b] = 0;
-        if (sh.bad > 0) atomicOr(p.status + b, sh.bad);
-      }
-      for (int k = tid; k < n_max; k += kAccThreads) p.path_nodes[(int64_t)b * n_max + k] = -1;
-      for (int k = tid; k <= n_max; k += kAccThreads) p.out_tokens[(int64_t)b * (n_max + 1) + k] = -1;
-    }
-    return;  // uniform across the cluster: every CTA computed the same flag
-  }
-
-  const bool vec4 = (V & 3) == 0;
   int best = 0;
   int bonus = -1;
+  if (sh.bad == 0) {  // uniform across the cluster: every CTA computed the same flag
+    const bool vec4 = (V & 3) == 0;
 
-  if (!p.sampling) {
-    // ================================================ greedy: level-synchronous walk
-    int nf = 1;
-    if (tid == 0) sh.front[0] = 0;
-    __syncthreads();
-    while (nf > 0) {
-      for (int f = 0; f < nf; ++f) {
-        const int node = sh.front[f];
-        const float* row = p.target + ((int64_t)b * n_max + node) * V;
-        float bv = -FLT_MAX;
-        int bi = INT_MAX;
-        if (vec4) {
-          const float4* r4 = reinterpret_cast<const float4*>(row + lo);
-          for (int j = tid; j < (len >> 2); j += kAccThreads) {
-            const float4 x = __ldg(r4 + j);
-            const int base = lo + 4 * j;
-            argmax_take(bv, bi, x.x, base);
-            argmax_take(bv, bi, x.y, base + 1);
-            argmax_take(bv, bi, x.z, base + 2);
-            argmax_take(bv, bi, x.w, base + 3);
-          }
-        } else {
-          for (int j = tid; j < len; j += kAccThreads) argmax_take(bv, bi, __ldg(row + lo + j), lo + j);
-        }
-        block_argmax(bv, bi, sh);
-        if (tid == 0) {
-          ClSlot* s = ex.publish(sh);
-          s->f[0] = sh.bf;
-          s->i[0] = sh.bi;
-        }
-        ex.exchange(sh);
-        float gv = -FLT_MAX;
-        int gi = INT_MAX;
-        for (int r = 0; r < CL; ++r) {
-          const ClSlot* s = ex.got(sh, r);
-          argmax_take(gv, gi, s->f[0], s->i[0]);
-        }
-        ex.flip();
-        if (tid == 0) sh.am[node] = gi;  // identical in every CTA
-      }
+    if (!p.sampling) {
+      // ================================================ greedy: level-synchronous walk
+      int nf = 1;
+      if (tid == 0) sh.front[0] = 0;
       __syncthreads();
-      if (tid == 0) {
-        // next frontier: children of frontier nodes whose token is the parent's argmax
-        int cnt = 0, lowest = INT_MAX;
+      while (nf > 0) {
         for (int f = 0; f < nf; ++f) {
           const int node = sh.front[f];
-          for (int k = sh.kid_off[node]; k < sh.kid_off[node + 1]; ++k) {
-            const int c = sh.kids[k];
-            if (sh.tok[c] == sh.am[node]) {
-              sh.nxt[cnt++] = c;
-              lowest = min(lowest, c);
+          const float* row = p.target + ((int64_t)b * n_max + node) * V;
+          float bv = -FLT_MAX;
+          int bi = INT_MAX;
+          if (vec4) {
+            const float4* r4 = reinterpret_cast<const float4*>(row + lo);
+            for (int j = tid; j < (len >> 2); j += kAccThreads) {
+              const float4 x = __ldg(r4 + j);
+              const int base = lo + 4 * j;
+              argmax_take(bv, bi, x.x, base);
+              argmax_take(bv, bi, x.y, base + 1);
+              argmax_take(bv, bi, x.z, base + 2);
+              argmax_take(bv, bi, x.w, base + 3);
             }
+          } else {
+            for (int j = tid; j < len; j += kAccThreads) argmax_take(bv, bi, __ldg(row + lo + j), lo + j);
           }
-        }
-        for (int k = 0; k < cnt; ++k) sh.front[k] = sh.nxt[k];
-        sh.cnt = cnt;
-        sh.lowest = lowest;
-      }
-      __syncthreads();
-      nf = sh.cnt;
-      if (nf > 0) best = sh.lowest;  // all next-frontier nodes share one depth
-      __syncthreads();
-    }
-    bonus = sh.am[best];
-  } else {
-    // ================================================ sampling: walk from the root
-    int node = 0;
-    uint32_t load_phase = 0;
-    for (;;) {
-      // this thread's accesses to the slices precede the next copy into them (the
-      // last exchange was a barrier; no CTA reads another CTA's slices)
-      fence_proxy_async_smem();
-      const float* trow = p.target + ((int64_t)b * n_max + node) * V + lo;
-      const float* drow = p.draft + ((int64_t)b * n_max + node) * V + lo;
-      if (vec4) {
-        // 16-byte aligned slices: two bulk copies into shared memory
-        if (tid == 0) {
-          mbar_arrive_expect_tx(&sh.load_bar, 8u * (uint32_t)len);
-          if (len > 0) {
-            bulk_g2s(wt, trow, 4u * (uint32_t)len, &sh.load_bar);
-            bulk_g2s(wq, drow, 4u * (uint32_t)len, &sh.load_bar);
+          block_argmax(bv, bi, sh);
+          if (tid == 0) {
+            ClSlot* s = ex.publish(sh);
+            s->f[0] = sh.bf;
+            s->i[0] = sh.bi;
           }
-        }
-        if (!mbar_wait(&sh.load_bar, load_phase, &sh.timed_out)) sh.timed_out = 1;
-        load_phase ^= 1u;
-      } else {
-        for (int j = tid; j < len; j += kAccThreads) {
-          wt[j] = __ldg(trow + j);
-          wq[j] = __ldg(drow + j);
+          ex.exchange(sh);
+          float gv = -FLT_MAX;
+          int gi = INT_MAX;
+          for (int r = 0; r < CL; ++r) {
+            const ClSlot* s = ex.got(sh, r);
+            argmax_take(gv, gi, s->f[0], s->i[0]);
+          }
+          ex.flip();
+          if (tid == 0) sh.am[node] = gi;  // identical in every CTA
         }
         __syncthreads();
-      }
-      float mt = -FLT_MAX, mq = -FLT_MAX;
-      for (int j = tid; j < len; j += kAccThreads) {
-        mt = fmaxf(mt, wt[j]);
-        mq = fmaxf(mq, wq[j]);
-      }
-      block_max2(mt, mq, sh);
-      if (tid == 0) {
-        ClSlot* s = ex.publish(sh);
-        s->f[0] = sh.cf[0];
-        s->f[1] = sh.cf[1];
-      }
-      ex.exchange(sh);
-      float Mt = -FLT_MAX, Mq = -FLT_MAX;
-      for (int r = 0; r < CL; ++r) {
-        const ClSlot* s = ex.got(sh, r);
-        Mt = fmaxf(Mt, s->f[0]);
-        Mq = fmaxf(Mq, s->f[1]);
-      }
-      ex.flip();
-      // exponentiate in place: w = 2^((z - max) * log2(e)/T); sums in double-float
-      // (four terms in fp32, then into the double-float sum)
-      Df st{0.f, 0.f}, sq{0.f, 0.f};
-      for (int j0 = tid; j0 < len; j0 += 4 * kAccThreads) {
-        float gt = 0.f, gq = 0.f;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int j = j0 + u * kAccThreads;
-          if (j < len) {
-            const float et = exp2f((wt[j] - Mt) * p.k2);
-            const float eq = exp2f((wq[j] - Mq) * p.k2);
-            wt[j] = et;
-            wq[j] = eq;
-            gt += et;
-            gq += eq;
+        if (tid == 0) {
+          // next frontier: children of frontier nodes whose token is the parent's argmax
+          int cnt = 0, lowest = INT_MAX;
+          for (int f = 0; f < nf; ++f) {
+            const int node = sh.front[f];
+            for (int k = sh.kid_off[node]; k < sh.kid_off[node + 1]; ++k) {
+              const int c = sh.kids[k];
+              if (sh.tok[c] == sh.am[node]) {
+                sh.nxt[cnt++] = c;
+                lowest = min(lowest, c);
+              }
+            }
           }
+          for (int k = 0; k < cnt; ++k) sh.front[k] = sh.nxt[k];
+          sh.cnt = cnt;
+          sh.lowest = lowest;
         }
-        st = df_add1(st, gt);
-        sq = df_add1(sq, gq);
+        __syncthreads();
+        nf = sh.cnt;
+        if (nf > 0) best = sh.lowest;  // all next-frontier nodes share one depth
+        __syncthreads();
       }
-      block_sum2(st, sq, sh);
-      const int k_beg = sh.kid_off[node], k_end = sh.kid_off[node + 1];
-      int f_owner = 0, f_off = 0;
-      if (k_beg < k_end) {
-        const int x = sh.tok[sh.kids[k_beg]];
-        f_owner = x / p.chunk;
-        f_off = x - f_owner * p.chunk;
-      }
-      if (tid == 0) {
-        ClSlot* s = ex.publish(sh);
-        s->d[0] = sh.bd[0];
-        s->d[1] = sh.bd[1];
-        if (k_beg < k_end && rank == f_owner) {
-          s->f[0] = wt[f_off];
-          s->f[1] = wq[f_off];
+      bonus = sh.am[best];
+    } else {
+      // ================================================ sampling: walk from the root
+      int node = 0;
+      uint32_t load_phase = 0;
+      for (;;) {
+        // this thread's accesses to the slices precede the next copy into them (the
+        // last exchange was a barrier; no CTA reads another CTA's slices)
+        fence_proxy_async_smem();
+        const float* trow = p.target + ((int64_t)b * n_max + node) * V + lo;
+        const float* drow = p.draft + ((int64_t)b * n_max + node) * V + lo;
+        if (vec4) {
+          // 16-byte aligned slices: two bulk copies into shared memory
+          if (tid == 0) {
+            mbar_arrive_expect_tx(&sh.load_bar, 8u * (uint32_t)len);
+            if (len > 0) {
+              bulk_g2s(wt, trow, 4u * (uint32_t)len, &sh.load_bar);
+              bulk_g2s(wq, drow, 4u * (uint32_t)len, &sh.load_bar);
+            }
+          }
+          if (!mbar_wait(&sh.load_bar, load_phase, &sh.timed_out)) sh.timed_out = 1;
+          load_phase ^= 1u;
+        } else {
+          for (int j = tid; j < len; j += kAccThreads) {
+            wt[j] = __ldg(trow + j);
+            wq[j] = __ldg(drow + j);
+          }
+          __syncthreads();
         }
-      }
-      ex.exchange(sh);
-      Df St{0.f, 0.f}, Sq{0.f, 0.f};
-      for (int r = 0; r < CL; ++r) {  // rank order: identical in every CTA
-        const ClSlot* s = ex.got(sh, r);
-        St = df_add(St, s->d[0]);
-        Sq = df_add(Sq, s->d[1]);
-      }
-      float pv0 = 0.f, qv0 = 0.f;
-      if (k_beg < k_end) {
-        pv0 = ex.got(sh, f_owner)->f[0];
-        qv0 = ex.got(sh, f_owner)->f[1];
-      }
-      ex.flip();
-      float Sw = St.hi;   // normaliser of the current target weights wt
-      float SqF = Sq.hi;  // normaliser of the current draft weights wq
-      // the tested child's numerators: the owner CTA published them in the exchange
-      // (no CTA reads another CTA's slices during the walk)
-      float pv = pv0, qv = qv0;
-      // a residual step whose slice update is deferred to the next pass:
-      // wt = max(0, wt * pend_isw - wq * pend_isq), its normaliser already in Sw
-      bool pending = false;
-      float pend_isw = 0.f, pend_isq = 0.f;
-      // without replacement: the rejected token whose draft weight is zeroed in the
-      // next pass, after that pass's deferred update has used it (slice offset, or -1)
-      int pend_zero = -1;
-      int accepted = -1;
-      for (int k = k_beg; k < k_end; ++k) {
-        const int c = sh.kids[k];
-        const float u = sh.ua[c];
-        if (u * (SqF > 0.f ? qv / SqF : 0.f) < pv / Sw) {
-          accepted = c;
-          break;
+        float mt = -FLT_MAX, mq = -FLT_MAX;
+        for (int j = tid; j < len; j += kAccThreads) {
+          mt = fmaxf(mt, wt[j]);
+          mq = fmaxf(mq, wq[j]);
         }
-        // rejected: the residual max(0, p - q), normalised (p kept if it sums to 0);
-        // without replacement also q without the rejected token, renormalised.  One
-        // pass applies the deferred update and sums the new residual (and the
-        // remaining draft weights); products and differences are rounded one by one
-        // so every pass agrees.
-        const float cur_isw = 1.f / Sw;
-        const float cur_isq = SqF > 0.f ? 1.f / SqF : 0.f;
-        const int xk = sh.tok[c];
-        const int xk_off = (p.wor && xk >= lo && xk < hi) ? xk - lo : -1;
-        Df z{0.f, 0.f}, zq{0.f, 0.f};
-        if (p.wor)
-          residual_pass<true>(wt, wq, len, pending, pend_isw, pend_isq, pend_zero, cur_isw, cur_isq, xk_off, z, zq);
-        else
-          residual_pass<false>(wt, wq, len, pending, pend_isw, pend_isq, pend_zero, cur_isw, cur_isq, xk_off, z, zq);
-        block_sum2(z, zq, sh);
-        const bool more = k + 1 < k_end;
-        int nx_owner = 0, nx_off = 0, nx_tok = -1;
-        if (more) {
-          nx_tok = sh.tok[sh.kids[k + 1]];
-          nx_owner = nx_tok / p.chunk;
-          nx_off = nx_tok - nx_owner * p.chunk;
+        block_max2(mt, mq, sh);
+        if (tid == 0) {
+          ClSlot* s = ex.publish(sh);
+          s->f[0] = sh.cf[0];
+          s->f[1] = sh.cf[1];
+        }
+        ex.exchange(sh);
+        float Mt = -FLT_MAX, Mq = -FLT_MAX;
+        for (int r = 0; r < CL; ++r) {
+          const ClSlot* s = ex.got(sh, r);
+          Mt = fmaxf(Mt, s->f[0]);
+          Mq = fmaxf(Mq, s->f[1]);
+        }
+        ex.flip();
+        // exponentiate in place: w = 2^((z - max) * log2(e)/T); sums in double-float
+        // (four terms in fp32, then into the double-float sum)
+        Df st{0.f, 0.f}, sq{0.f, 0.f};
+        for (int j0 = tid; j0 < len; j0 += 4 * kAccThreads) {
+          float gt = 0.f, gq = 0.f;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = j0 + u * kAccThreads;
+            if (j < len) {
+              const float et = exp2f((wt[j] - Mt) * p.k2);
+              const float eq = exp2f((wq[j] - Mq) * p.k2);
+              wt[j] = et;
+              wq[j] = eq;
+              gt += et;
+              gq += eq;
+            }
+          }
+          st = df_add1(st, gt);
+          sq = df_add1(sq, gq);
+        }
+        block_sum2(st, sq, sh);
+        const int k_beg = sh.kid_off[node], k_end = sh.kid_off[node + 1];
+        int f_owner = 0, f_off = 0;
+        if (k_beg < k_end) {
+          const int x = sh.tok[sh.kids[k_beg]];
+          f_owner = x / p.chunk;
+          f_off = x - f_owner * p.chunk;
         }
         if (tid == 0) {
           ClSlot* s = ex.publish(sh);
           s->d[0] = sh.bd[0];
           s->d[1] = sh.bd[1];
-          if (more && rank == nx_owner) {
-            const float w = wt[nx_off];
-            const float qw = wq[nx_off];
-            s->f[0] = w;                                                   // p numerator if kept
-            s->f[1] = (p.wor && nx_tok == xk) ? 0.f : qw;                  // next child's q numerator
-            s->i[0] = __float_as_int(
-                fmaxf(0.f, __fsub_rn(__fmul_rn(w, cur_isw), __fmul_rn(qw, cur_isq))));  // residual numerator
+          if (k_beg < k_end && rank == f_owner) {
+            s->f[0] = wt[f_off];
+            s->f[1] = wq[f_off];
           }
         }
         ex.exchange(sh);
-        Df Z{0.f, 0.f}, Zq{0.f, 0.f};
-        for (int r = 0; r < CL; ++r) {
-          Z = df_add(Z, ex.got(sh, r)->d[0]);
-          Zq = df_add(Zq, ex.got(sh, r)->d[1]);
+        Df St{0.f, 0.f}, Sq{0.f, 0.f};
+        for (int r = 0; r < CL; ++r) {  // rank order: identical in every CTA
+          const ClSlot* s = ex.got(sh, r);
+          St = df_add(St, s->d[0]);
+          Sq = df_add(Sq, s->d[1]);
         }
-        float nw = 0.f, nq = 0.f, nr = 0.f;
-        if (more) {
-          const ClSlot* o = ex.got(sh, nx_owner);
-          nw = o->f[0];
-          nq = o->f[1];
-          nr = __int_as_float(o->i[0]);
-        }
-        ex.flip();
-        if (df_pos(Z)) {
-          pending = true;
-          pend_isw = cur_isw;
-          pend_isq = cur_isq;
-          Sw = Z.hi;
-          pv = nr;
-        } else {
-          pending = false;
-          pv = nw;
-        }
-        if (p.wor) {
-          pend_zero = xk_off;
-          SqF = Zq.hi;
-        }
-        qv = nq;
-      }
-      if (accepted >= 0) {
-        node = accepted;
-        continue;
-      }
-      if (pending) {  // the bonus draw reads the current p: apply the deferred update
-        for (int j = tid; j < len; j += kAccThreads)
-          wt[j] = fmaxf(0.f, __fsub_rn(__fmul_rn(wt[j], pend_isw), __fmul_rn(wq[j], pend_isq)));
-        __syncthreads();
-      }
-      // ---- bonus token: inverse CDF of wt with u_sample[node] (double-float prefix sums)
-      {
-        const int per = (len + kAccThreads - 1) / kAccThreads;
-        const int a0 = min(len, tid * per), a1 = min(len, a0 + per);
-        // this thread's range sum, starting at an offset rotated by the lane so that
-        // the 32 lanes hit 32 different banks (the ranges are `per` words apart)
-        Df tsum{0.f, 0.f};
-        {
-          const int cnt = a1 - a0;
-          int jj = cnt > 0 ? (tid & 31) % cnt : 0;
-          for (int n = 0; n < cnt; ++n) {
-            tsum = df_add1(tsum, wt[a0 + jj]);
-            jj = (jj + 1 == cnt) ? 0 : jj + 1;
-          }
-        }
-        // exclusive scan over the block's threads
-        const int lane = tid & 31, warp = tid >> 5;
-        Df incl = tsum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const Df y = df_shfl_up(incl, o);
-          if (lane >= o) incl = df_add(incl, y);
-        }
-        Df prev = df_shfl_up(incl, 1);
-        if (lane == 0) prev = Df{0.f, 0.f};
-        if (lane == 31) sh.wd[warp][0] = incl;
-        __syncthreads();
-        if (tid == 0) {
-          Df run{0.f, 0.f};
-          for (int w = 0; w < kAccWarps; ++w) {
-            const Df t = sh.wd[w][0];
-            sh.wd[w][1] = run;
-            run = df_add(run, t);
-          }
-          sh.bd[0] = run;
-        }
-        __syncthreads();
-        sh.thr_excl[tid] = df_add(sh.wd[warp][1], prev);
-        const Df s_r = sh.bd[0];
-        if (tid == 0) {
-          ClSlot* s = ex.publish(sh);
-          s->d[0] = s_r;
-        }
-        ex.exchange(sh);
-        Df pre[CL], srk[CL];
-        Df S{0.f, 0.f};
-        for (int r = 0; r < CL; ++r) {
-          pre[r] = S;
-          srk[r] = ex.got(sh, r)->d[0];
-          S = df_add(S, srk[r]);
+        float pv0 = 0.f, qv0 = 0.f;
+        if (k_beg < k_end) {
+          pv0 = ex.got(sh, f_owner)->f[0];
+          qv0 = ex.got(sh, f_owner)->f[1];
         }
         ex.flip();
-        const Df t = df_mul1(S, p.u_sample[(int64_t)b * n_max + node]);
-        int rstar = -1, rlast = -1;
-        for (int r = 0; r < CL; ++r) {
-          if (df_pos(srk[r])) rlast = r;
-          if (rstar < 0 && df_gt(df_add(pre[r], srk[r]), t)) rstar = r;
-        }
-        const bool fallback_rank = rstar < 0;
-        if (fallback_rank) rstar = rlast;
-        int found = -1;
-        if (rank == rstar) {
-          // thread whose range crosses t (or the last non-empty one on fallback)
-          const Df base = df_add(pre[rank], sh.thr_excl[tid]);
-          const bool nonempty = tsum.hi > 0.f;
-          const bool crosses = !fallback_rank && nonempty && df_gt(df_add(base, tsum), t) && !df_gt(base, t);
+        float Sw = St.hi;   // normaliser of the current target weights wt
+        float SqF = Sq.hi;  // normaliser of the current draft weights wq
+        // the tested child's numerators: the owner CTA published them in the exchange
+        // (no CTA reads another CTA's slices during the walk)
+        float pv = pv0, qv = qv0;
+        // a residual step whose slice update is deferred to the next pass:
+        // wt = max(0, wt * pend_isw - wq * pend_isq), its normaliser already in Sw
+        bool pending = false;
+        float pend_isw = 0.f, pend_isq = 0.f;
+        // without replacement: the rejected token whose draft weight is zeroed in the
+        // next pass, after that pass's deferred update has used it (slice offset, or -1)
+        int pend_zero = -1;
+        int accepted = -1;
+        for (int k = k_beg; k < k_end; ++k) {
+          const int c = sh.kids[k];
+          const float u = sh.ua[c];
+          if (u * (SqF > 0.f ? qv / SqF : 0.f) < pv / Sw) {
+            accepted = c;
+            break;
+          }
+          // rejected: the residual max(0, p - q), normalised (p kept if it sums to 0);
+          // without replacement also q without the rejected token, renormalised.  One
+          // pass applies the deferred update and sums the new residual (and the
+          // remaining draft weights); products and differences are rounded one by one
+          // so every pass agrees.
+          const float cur_isw = 1.f / Sw;
+          const float cur_isq = SqF > 0.f ? 1.f / SqF : 0.f;
+          const int xk = sh.tok[c];
+          const int xk_off = (p.wor && xk >= lo && xk < hi) ? xk - lo : -1;
+          Df z{0.f, 0.f}, zq{0.f, 0.f};
+          if (p.wor)
+            residual_pass<true>(wt, wq, len, pending, pend_isw, pend_isq, pend_zero, cur_isw, cur_isq, xk_off, z, zq);
+          else
+            residual_pass<false>(wt, wq, len, pending, pend_isw, pend_isq, pend_zero, cur_isw, cur_isq, xk_off, z, zq);
+          block_sum2(z, zq, sh);
+          const bool more = k + 1 < k_end;
+          int nx_owner = 0, nx_off = 0, nx_tok = -1;
+          if (more) {
+            nx_tok = sh.tok[sh.kids[k + 1]];
+            nx_owner = nx_tok / p.chunk;
+            nx_off = nx_tok - nx_owner * p.chunk;
+          }
           if (tid == 0) {
-            sh.bi = INT_MAX;
-            sh.wi[0] = -1;
-          }
-          __syncthreads();
-          if (crosses) atomicMin(&sh.bi, tid);
-          if (nonempty) atomicMax(&sh.wi[0], tid);
-          __syncthreads();
-          int kstar = sh.bi;
-          const bool fb = (kstar == INT_MAX);
-          if (fb) kstar = sh.wi[0];
-          if (tid == kstar) {
-            Df acc = base;
-            int j_found = -1, j_last = -1;
-            for (int j = a0; j < a1; ++j) {
-              if (wt[j] > 0.f) j_last = j;
-              acc = df_add1(acc, wt[j]);
-              if (!fb && j_found < 0 && df_gt(acc, t) && wt[j] > 0.f) j_found = j;
+            ClSlot* s = ex.publish(sh);
+            s->d[0] = sh.bd[0];
+            s->d[1] = sh.bd[1];
+            if (more && rank == nx_owner) {
+              const float w = wt[nx_off];
+              const float qw = wq[nx_off];
+              s->f[0] = w;                                                   // p numerator if kept
+              s->f[1] = (p.wor && nx_tok == xk) ? 0.f : qw;                  // next child's q numerator
+              s->i[0] = __float_as_int(
+                  fmaxf(0.f, __fsub_rn(__fmul_rn(w, cur_isw), __fmul_rn(qw, cur_isq))));  // residual numerator
             }
-            sh.wi[1] = lo + (j_found >= 0 ? j_found : j_last);
+          }
+          ex.exchange(sh);
+          Df Z{0.f, 0.f}, Zq{0.f, 0.f};
+          for (int r = 0; r < CL; ++r) {
+            Z = df_add(Z, ex.got(sh, r)->d[0]);
+            Zq = df_add(Zq, ex.got(sh, r)->d[1]);
+          }
+          float nw = 0.f, nq = 0.f, nr = 0.f;
+          if (more) {
+            const ClSlot* o = ex.got(sh, nx_owner);
+            nw = o->f[0];
+            nq = o->f[1];
+            nr = __int_as_float(o->i[0]);
+          }
+          ex.flip();
+          if (df_pos(Z)) {
+            pending = true;
+            pend_isw = cur_isw;
+            pend_isq = cur_isq;
+            Sw = Z.hi;
+            pv = nr;
+          } else {
+            pending = false;
+            pv = nw;
+          }
+          if (p.wor) {
+            pend_zero = xk_off;
+            SqF = Zq.hi;
+          }
+          qv = nq;
+        }
+        if (accepted >= 0) {
+          node = accepted;
+          continue;
+        }
+        if (pending) {  // the bonus draw reads the current p: apply the deferred update
+          for (int j = tid; j < len; j += kAccThreads)
+            wt[j] = fmaxf(0.f, __fsub_rn(__fmul_rn(wt[j], pend_isw), __fmul_rn(wq[j], pend_isq)));
+          __syncthreads();
+        }
+        // ---- bonus token: inverse CDF of wt with u_sample[node] (double-float prefix sums)
+        {
+          const int per = (len + kAccThreads - 1) / kAccThreads;
+          const int a0 = min(len, tid * per), a1 = min(len, a0 + per);
+          // this thread's range sum, starting at an offset rotated by the lane so that
+          // the 32 lanes hit 32 different banks (the ranges are `per` words apart)
+          Df tsum{0.f, 0.f};
+          {
+            const int cnt = a1 - a0;
+            int jj = cnt > 0 ? (tid & 31) % cnt : 0;
+            for (int n = 0; n < cnt; ++n) {
+              tsum = df_add1(tsum, wt[a0 + jj]);
+              jj = (jj + 1 == cnt) ? 0 : jj + 1;
+            }
+          }
+          // exclusive scan over the block's threads
+          const int lane = tid & 31, warp = tid >> 5;
+          Df incl = tsum;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const Df y = df_shfl_up(incl, o);
+            if (lane >= o) incl = df_add(incl, y);
+          }
+          Df prev = df_shfl_up(incl, 1);
+          if (lane == 0) prev = Df{0.f, 0.f};
+          if (lane == 31) sh.wd[warp][0] = incl;
+          __syncthreads();
+          if (tid == 0) {
+            Df run{0.f, 0.f};
+            for (int w = 0; w < kAccWarps; ++w) {
+              const Df t = sh.wd[w][0];
+              sh.wd[w][1] = run;
+              run = df_add(run, t);
+            }
+            sh.bd[0] = run;
           }
           __syncthreads();
-          found = sh.wi[1];
+          sh.thr_excl[tid] = df_add(sh.wd[warp][1], prev);
+          const Df s_r = sh.bd[0];
+          if (tid == 0) {
+            ClSlot* s = ex.publish(sh);
+            s->d[0] = s_r;
+          }
+          ex.exchange(sh);
+          Df pre[CL], srk[CL];
+          Df S{0.f, 0.f};
+          for (int r = 0; r < CL; ++r) {
+            pre[r] = S;
+            srk[r] = ex.got(sh, r)->d[0];
+            S = df_add(S, srk[r]);
+          }
+          ex.flip();
+          const Df t = df_mul1(S, p.u_sample[(int64_t)b * n_max + node]);
+          int rstar = -1, rlast = -1;
+          for (int r = 0; r < CL; ++r) {
+            if (df_pos(srk[r])) rlast = r;
+            if (rstar < 0 && df_gt(df_add(pre[r], srk[r]), t)) rstar = r;
+          }
+          const bool fallback_rank = rstar < 0;
+          if (fallback_rank) rstar = rlast;
+          int found = -1;
+          if (rank == rstar) {
+            // thread whose range crosses t (or the last non-empty one on fallback)
+            const Df base = df_add(pre[rank], sh.thr_excl[tid]);
+            const bool nonempty = tsum.hi > 0.f;
+            const bool crosses = !fallback_rank && nonempty && df_gt(df_add(base, tsum), t) && !df_gt(base, t);
+            if (tid == 0) {
+              sh.bi = INT_MAX;
+              sh.wi[0] = -1;
+            }
+            __syncthreads();
+            if (crosses) atomicMin(&sh.bi, tid);
+            if (nonempty) atomicMax(&sh.wi[0], tid);
+            __syncthreads();
+            int kstar = sh.bi;
+            const bool fb = (kstar == INT_MAX);
+            if (fb) kstar = sh.wi[0];
+            if (tid == kstar) {
+              Df acc = base;
+              int j_found = -1, j_last = -1;
+              for (int j = a0; j < a1; ++j) {
+                if (wt[j] > 0.f) j_last = j;
+                acc = df_add1(acc, wt[j]);
+                if (!fb && j_found < 0 && df_gt(acc, t) && wt[j] > 0.f) j_found = j;
+              }
+              sh.wi[1] = lo + (j_found >= 0 ? j_found : j_last);
+            }
+            __syncthreads();
+            found = sh.wi[1];
+          }
+          if (tid == 0) {
+            ClSlot* s = ex.publish(sh);
+            s->i[0] = found;
+          }
+          ex.exchange(sh);
+          int tokv = -1;
+          for (int r = 0; r < CL; ++r) tokv = max(tokv, ex.got(sh, r)->i[0]);
+          ex.flip();
+          bonus = tokv;
         }
-        if (tid == 0) {
-          ClSlot* s = ex.publish(sh);
-          s->i[0] = found;
-        }
-        ex.exchange(sh);
-        int tokv = -1;
-        for (int r = 0; r < CL; ++r) tokv = max(tokv, ex.got(sh, r)->i[0]);
-        ex.flip();
-        bonus = tokv;
+        best = node;
+        break;
       }
-      best = node;
-      break;
     }
-  }
 
-  // ---- outputs (rank 0)
-  if (rank == 0 && tid == 0) {
+  }  // sh.bad == 0
+
+  // ---- outputs (rank 0), after the previous kernel: a request flagged on entry,
+  // or with an invalid tree, gets an empty path
+  griddep_wait();
+  const int st_in = p.status[b];
+  const int bad_out = st_in != 0 ? -1 : sh.bad;
+  if (bad_out != 0) {
+    if (rank == 0) {
+      if (tid == 0) {
+        p.accept_len[b] = 0;
+        if (bad_out > 0) atomicOr(p.status + b, bad_out);
+      }
+      for (int k = tid; k < n_max; k += kAccThreads) p.path_nodes[(int64_t)b * n_max + k] = -1;
+      for (int k = tid; k <= n_max; k += kAccThreads) p.out_tokens[(int64_t)b * (n_max + 1) + k] = -1;
+    }
+  } else if (rank == 0 && tid == 0) {
     if (sh.timed_out) atomicOr(p.status + b, TV_DEV_TIMEOUT);
     int len_path = 0;
     for (int j = best; j != 0; j = sh.par[j]) sh.path[len_path++] = j;
@@ -812,9 +818,11 @@ __global__ void __launch_bounds__(kArgThreads) greedy_onepass_kernel(const OnePa
   const int sl = blockIdx.x, node = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   const int n_max = p.n_max, V = p.V;
-  griddep_wait();
+  // the slices read only inputs (logits, node counts), so they run while the
+  // previous kernel finishes; status, which it may write, is read by the last CTA
+  // after the wait below
   const int N = p.n_nodes[b];
-  const bool req_ok = p.status[b] == 0 && N >= 1 && N <= n_max;
+  const bool req_ok = N >= 1 && N <= n_max;
 
   // ---- this slice's partial argmax (lowest index on ties)
   float bv = -FLT_MAX;
@@ -851,6 +859,7 @@ __global__ void __launch_bounds__(kArgThreads) greedy_onepass_kernel(const OnePa
   }
   __syncthreads();
   if (!last_sh) return;
+  griddep_wait();
   __threadfence();
 
   // ---- the last CTA of request b: validate, then resolve the walk

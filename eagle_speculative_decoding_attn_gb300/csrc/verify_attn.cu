@@ -513,6 +513,10 @@ __global__ void __launch_bounds__(kQ4 ? kThreadsQ4 : kThreads, 1)
   }
   // everything above is on chip; global memory only after the previous kernel
   griddep_wait();
+  // the next kernel may be scheduled now: its CTAs take SMs as this grid's CTAs
+  // exit (an SM running this kernel has no registers left for another CTA), and
+  // it waits for this grid before reading anything this kernel writes
+  griddep_launch_dependents();
   if (warp == 3) {
     // ---- plan: per-request tiles and costs, exclusive scan of the costs
     int64_t carry = 0;
