@@ -305,10 +305,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kAccThreads, 1)
   float* wt = dyn;             // sampling: current target weights of this slice
   float* wq = dyn + p.chunk;   // sampling: draft weights of this slice
 
-  // Everything up to the outputs reads only inputs (tree, logits, uniforms, the
-  // mask kernel's words, which precede the previous kernel), so it runs while the
-  // previous kernel finishes; status, which that kernel may write, is read and
-  // written after the wait before the outputs.
+  // Everything up to the outputs reads only inputs (tree, tokens, logits,
+  // uniforms) and writes nothing global, so it runs while the previous kernel
+  // finishes; status, which that kernel may write, is read and written after the
+  // wait before the outputs.
   // ---- tree setup and validation (every CTA redundantly, identical results):
   // one node per thread, then thread 0 builds the child lists from shared memory
   const int N = p.n_nodes[b];

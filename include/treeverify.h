@@ -39,6 +39,16 @@
  *    status is non-zero and OR in their own bits.
  *  - Return value: TV_OK (0) or a negative TV_ERR_* code; tv_last_error()
  *    gives a message for the calling thread's last failure.
+ *  - Launch order: every kernel is launched with programmatic dependent
+ *    launch and waits for the preceding kernel in the stream before it reads
+ *    anything that kernel may write (and before it writes anything that kernel
+ *    may read).  tv_tree_build_mask and tv_tree_verify_attn(_q4) let the next
+ *    kernel in the stream be scheduled before they finish; a kernel of the
+ *    caller's that follows one of them and is itself launched with the
+ *    programmatic-launch attribute must wait (griddepcontrol.wait /
+ *    cudaGridDependencySynchronize) before reading their outputs.  Kernels
+ *    launched without that attribute, and host synchronisation, are
+ *    unaffected.
  */
 #ifndef TREEVERIFY_H_
 #define TREEVERIFY_H_
