@@ -87,7 +87,7 @@ struct AttnParams {
   int32_t* ws_exit;     // CTA exit counter (zero between calls)
   uint4* part_o;        // [2 * gridDim][D/8][256] 8 x fp16: column group major, rows contiguous
   float* part_lse;      // [2 * gridDim][256] log-sum-exp of each partial row
-  float* part_scale;    // [2 * gridDim][256] max |O| of each partial row (its fp16 values are O / max)
+  float* part_scale;    // [2 * gridDim][256] c of each partial row: its fp16 values are O / c (c = 1, or max |O|)
   // 4-bit cache only: codes [pages][Hkv][16][D/2] bytes, params [pages][Hkv][16][D/16] fp16
   const uint8_t* k_codes;
   const uint8_t* k_params;
@@ -287,7 +287,8 @@ __device__ __forceinline__ int split_slot(const Item& it, int sp) { return sp ==
 // partial rows by their log-sum-exp weights: out = sum_s w_s O_s with
 // w_s = exp(lse_s - m) / sum_s' exp(lse_s' - m), m = max_s lse_s, and
 // lse = m + ln sum_s exp(lse_s - m).  A partial row is stored as fp16 values
-// of O_s / c_s with c_s = max |O_s| (kept in fp32), so w_s c_s multiplies them.
+// of O_s / c_s with c_s = 1, or c_s = max |O_s| for a row with a value past the
+// fp16 range (c_s kept in fp32), so w_s c_s multiplies them.
 // The work items are (row, column slice) pairs spread over the whole
 // warpgroup, consecutive threads on consecutive rows so the partial reads
 // coalesce; one item loads the log-sum-exps, scales and slices of up to kMB
@@ -1037,43 +1038,52 @@ __global__ void __launch_bounds__(kQ4 ? kThreadsQ4 : kThreads, 1)
           for (int c = 0; c < 32; ++c) y[c] = __uint_as_float(o[c]) * inv_l;
         }
       };
-      float row_scale = 0.f;
-      if (!direct) {
-        // a partial row is stored as fp16 values of O / max |O|
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          float y[32];
-          row_chunk(c0, y);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) row_scale = fmaxf(row_scale, fabsf(y[c]));
-        }
-      }
-      const float to_half = row_scale > 0.f ? 1.f / row_scale : 0.f;
+      // a partial row is stored as fp16 values of O / c: c = 1, or c = max |O| for a row
+      // with a value past the fp16 range (found on the way; that row is stored again)
       uint4* pslot = p.part_o + (int64_t)item.my_slot * (D / 8) * kRowsPerSlot + prow;
+      auto half_store = [&](const float* y, int c0, float sc) {
+        uint4* dst = pslot + (c0 / 8) * kRowsPerSlot;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t hw[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __half2 h = __floats2half2_rn(y[8 * q + 2 * e] * sc, y[8 * q + 2 * e + 1] * sc);
+            hw[e] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+          dst[q * kRowsPerSlot] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        }
+      };
+      float amax = 0.f;
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         float y[32];
         row_chunk(c0, y);
-        if (row_ok) {
-          if (direct) {
+        if (direct) {
+          if (row_ok) {
             uint4* dst = reinterpret_cast<uint4*>(p.out + orow_idx * D + c0);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               dst[q] = make_uint4(pack_bf16x2(y[8 * q], y[8 * q + 1]), pack_bf16x2(y[8 * q + 2], y[8 * q + 3]),
                                   pack_bf16x2(y[8 * q + 4], y[8 * q + 5]), pack_bf16x2(y[8 * q + 6], y[8 * q + 7]));
-          } else {
-            uint4* dst = pslot + (c0 / 8) * kRowsPerSlot;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t hw[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const __half2 h = __floats2half2_rn(y[8 * q + 2 * e] * to_half, y[8 * q + 2 * e + 1] * to_half);
-                hw[e] = *reinterpret_cast<const uint32_t*>(&h);
-              }
-              dst[q * kRowsPerSlot] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            }
           }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) amax = fmaxf(amax, fabsf(y[c]));
+          if (row_ok) half_store(y, c0, 1.f);
+        }
+      }
+      constexpr float kHalfMax = 65504.f;
+      float row_scale = 1.f;
+      if (!direct && __any_sync(0xffffffffu, amax > kHalfMax)) {
+        const bool over = amax > kHalfMax;
+        if (over) row_scale = amax;
+        const float to_half = 1.f / row_scale;
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float y[32];
+          row_chunk(c0, y);
+          if (row_ok && over) half_store(y, c0, to_half);
         }
       }
       tc_fence_before();

@@ -221,3 +221,36 @@ def test_attn_many_small_requests():
     ref_out, ref_lse, ref_st = _oracle(w)
     assert np.array_equal(st, ref_st) and (st == 0).all()
     compare_attn(out, lse, ref_out, ref_lse, w, output_rounding=True)
+
+
+def test_attn_split_partials_past_fp16_range():
+    """Split partials are stored in fp16; a row with a value past the fp16 range
+    is stored again as O / max |O|.  One KV head over a 6000-key prefix splits
+    across ~30 CTAs; the V row of tree node 5 carries an offset of 1e9, so the
+    rows of node 5 and its descendants have partials and outputs past the fp16
+    range while the other rows of the same warps do not.  An output dominated by
+    one V value carries that key's probability rounded to bf16 (up to 2^-8
+    relative), the bf16 output's rounding (up to 2^-8) and the fp16 partial's
+    (2^-11 of its largest value): the bound is 1e-2 + (2^-7 + 2^-10) |ref|."""
+    dev = require_gpu()
+    rng = np.random.Generator(np.random.PCG64(91))
+    parents = W.random_recursive_tree(rng, 40)
+    L, j = 6000, 5
+    w = W.make_custom(B=1, Hq=8, Hkv=1, D=128, prefix_len=[L], parents_list=[parents], seed=92)
+    v = oracle.bf16_to_f64(w.v_bits)
+    pos = L + j
+    v[w.page_table[0, pos // 16], 0, pos % 16] += 1.0e9
+    w.v_bits = W.to_bf16_bits(v.astype(np.float32))
+    out, lse, st = DevWorkload(w, dev, logits=False).attn()
+    assert (st == 0).all()
+    ref_out, ref_lse, _ = _oracle(w)
+    n = int(w.n_nodes[0])
+    big = np.abs(ref_out[0, :n]).max(axis=-1) > 65504.0
+    assert big.any() and (~big).any()                      # both paths are taken
+    got, ref = out[0, :n], ref_out[0, :n]
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref)
+    rel = err[big] / np.abs(ref[big])
+    assert np.all(err <= 1e-2 + (2.0 ** -7 + 2.0 ** -10) * np.abs(ref)), \
+        f"large rows: max relative error {rel.max():.3e}; other rows: max error {err[~big].max():.3e}"
+    assert np.abs(lse[0, :n] - ref_lse[0, :n]).max() <= 2e-3
