@@ -726,7 +726,6 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kAccThreads, 1)
         break;
       }
     }
-
   }  // sh.bad == 0
 
   // ---- outputs (rank 0), after the previous kernel: a request flagged on entry,

@@ -600,22 +600,15 @@ __global__ void __launch_bounds__(kQ4 ? kThreadsQ4 : kThreads, 1)
         const int L = p.prefix_len[item.b], N = p.n_nodes[item.b];
         const int32_t* pt = p.page_table + (int64_t)item.b * p.max_pages;
         for (int tile = item.tile_begin; tile < item.tile_end && ok; ++tile, ++kv_it) {
-          const int s = kv_it % kStages;
-          const uint32_t ph = (kv_it / kStages) & 1u;
           const int key0 = tile * kBN;
           const int npg = min(kPagesPerTile, (L + N - key0 + kPageSize - 1) / kPageSize);
-          const uint32_t bytes = (uint32_t)(npg * kPageSize * D * 2);
           int pages[kPagesPerTile];
 #pragma unroll
           for (int pg = 0; pg < kPagesPerTile; ++pg) pages[pg] = pg < npg ? pt[key0 / kPageSize + pg] : 0;
-          // an out-of-range page id reads the TMA fill value (zeros); the request is
-          // reported and zero-filled at exit
           if constexpr (kQ4) {
             // codes and params of each half tile into its code slot (bulk copies of the
             // contiguous per-page blocks); an out-of-range page id reads page 0 instead
             // (the request is reported and zero-filled at exit)
-            (void)s;
-            (void)bytes;
             const uint8_t* codes = is_k ? p.k_codes : p.v_codes;
             const uint8_t* prm = is_k ? p.k_params : p.v_params;
             constexpr uint32_t kPgCodes = kPageSize * S::kCodeRow, kPgParams = kPageSize * S::kParamRow;
@@ -637,6 +630,11 @@ __global__ void __launch_bounds__(kQ4 ? kThreadsQ4 : kThreads, 1)
               }
             }
           } else {
+            // an out-of-range page id reads the TMA fill value (zeros); the request is
+            // reported and zero-filled at exit
+            const int s = kv_it % kStages;
+            const uint32_t ph = (kv_it / kStages) & 1u;
+            const uint32_t bytes = (uint32_t)(npg * kPageSize * D * 2);
             uint64_t* empty = is_k ? &bar_ke[s] : &bar_ve[s];
             uint64_t* full = is_k ? &bar_kf[s] : &bar_vf[s];
             uint8_t* dst = (is_k ? sK : sV) + s * S::kKVTile;
