@@ -66,8 +66,9 @@ constexpr uint32_t kRegsControl = 88;
 constexpr uint32_t kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax == kThreads * 168, "register split must match the launch");
 // 4-bit cache: 512 threads at 128 registers each, no re-split (the compiler's
-// limit is the launch's 128 registers for every role, so the softmax works on
-// half an S row at a time)
+// limit is the launch's 128 registers for every role, so the softmax reads the
+// S row in 64-column halves for its maximum and in 32-column chunks for the
+// probabilities)
 constexpr int kQ4Group = 32;                   // dims sharing one (scale, zero) pair
 constexpr int kHalfKeys = kBN / 2;             // keys of one code slot (half a KV tile)
 
