@@ -59,3 +59,41 @@ def test_product_path_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in src and "from oracle" not in src, f
+
+
+def _declarations():
+    """{name: (return type, [parameter types])} of every call in the header."""
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    out = {}
+    for m in re.finditer(r"([A-Za-z_][A-Za-z0-9_ ]*?\**)\s*\b(tv_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", txt):
+        ret, name, params = m.group(1).strip(), m.group(2), m.group(3).strip()
+        types = []
+        if params and params != "void":
+            for prm in params.split(","):
+                prm = " ".join(prm.split())
+                # drop the parameter's name: the last identifier
+                t = re.sub(r"\b[A-Za-z_][A-Za-z0-9_]*\s*$", "", prm).strip()
+                types.append(t)
+        out[name] = (ret, types)
+    return out
+
+
+def _ctype_of(c_type):
+    if "*" in c_type:
+        return ctypes.c_char_p if c_type.replace(" ", "") == "constchar*" else ctypes.c_void_p
+    base = c_type.replace("const", "").strip()
+    return {"int": ctypes.c_int, "int64_t": ctypes.c_int64, "size_t": ctypes.c_size_t,
+            "float": ctypes.c_float}[base]
+
+
+def test_binding_argument_types_match_the_header():
+    from eagle_speculative_decoding_attn_gb300 import treeverify as tvb
+    decl = _declarations()
+    assert set(decl) == set(tvb._SIGNATURES)
+    for name, (ret, params) in decl.items():
+        restype, argtypes = tvb._SIGNATURES[name]
+        assert len(argtypes) == len(params), f"{name}: {len(argtypes)} binding arguments, header has {len(params)}"
+        for i, (c_type, a) in enumerate(zip(params, argtypes)):
+            assert a is _ctype_of(c_type), f"{name} argument {i}: header {c_type!r}, binding {a}"
+        assert restype is _ctype_of(ret), f"{name} return: header {ret!r}, binding {restype}"
