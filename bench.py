@@ -213,6 +213,13 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def workload_config(cfg, world):
+    """The `config` keys naming the workload, the same on both arms' lines."""
+    return {"workload": f"{cfg.name}: B={cfg.B}, Hq={cfg.Hq}, Hkv={cfg.Hkv}, D={cfg.D}, prefix={cfg.prefix}, "
+                        f"nodes={cfg.n_nodes}, V={cfg.V}, T={cfg.temperature}, commit layers={cfg.n_layers_commit}",
+            "global_batch": cfg.B * world, "parallelism": f"replicas x{world}"}
+
+
 def packed_views(buf, specs):
     """Views of a flat uint8 tensor as the (name, dtype, shape) arrays of `specs`,
     each starting on a 256-byte boundary; returns ({name: view}, total bytes).
@@ -985,11 +992,9 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded numpy PCG64; random bf16 KV/Q ~ N(0,1), Gaussian fp32 logits)",
-        "config": {"workload": f"{cfg.name}: B={B}, Hq={Hq}, Hkv={Hkv}, D={D}, prefix={cfg.prefix}, "
-                               f"nodes={cfg.n_nodes}, V={V}, T={w.temperature}, commit layers={layers}",
-                   "global_batch": B * world, "parallelism": f"replicas x{world}",
-                   "l2": f"{R} rotated input copies ({R * per_copy / 1e6:.0f} MB read per rotation) > 3x L2",
-                   "step": "mask + attention + accept + commit, one CUDA graph replay"},
+        "config": dict(workload_config(cfg, world),
+                       l2=f"{R} rotated input copies ({R * per_copy / 1e6:.0f} MB read per rotation) > 3x L2",
+                       step="mask + attention + accept + commit, one CUDA graph replay"),
         "attn_us": attn_us,
         "attn_tbps": abytes / attn_s / 1e12,
         "attn_roofline_frac": max(t_hbm, t_tc) / attn_s,
@@ -1037,6 +1042,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     import numpy as np
+    from eagle_speculative_decoding_attn_gb300 import workloads as W
     steps = max(1, min(args.steps, 3))
     warm = 1 if args.warmup > 0 else 0
     for _ in range(warm):
@@ -1050,7 +1056,7 @@ def run_reference(args, world, rank):
     print(json.dumps({"impl": "reference", "metric": METRIC, "value": value, "unit": "nodes/s", "n_gpus": world,
                       "steps": steps, "warmup": warm, "ms_per_step": sps * 1000.0, "higher_is_better": True,
                       "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                      "config": {"workload": args.config},
+                      "config": workload_config(W.CONFIG_BY_NAME[args.config], world),
                       "cpu_baseline": {"value": value, "unit": "nodes/s", "cores": res["cores"], "kind": "oracle",
                                        "sample": res["desc"] + "; attention rows spread over the cores"},
                       "e2e": {"value": value, "unit": "nodes/s", "h2d_bytes_per_step": 0,
