@@ -35,8 +35,9 @@
  *    launch.  Data errors found on the device never trap: they are OR-ed into
  *    the per-request int32 `status` word as TV_DEV_* bits and that request's
  *    outputs are written as documented (zeros / -1).  tv_tree_build_mask
- *    writes `status`; the other calls read it on entry, skip requests whose
- *    status is non-zero and OR in their own bits.
+ *    writes `status`; the other calls read it as the calls before them left
+ *    it, treat requests whose status is non-zero as skipped (the documented
+ *    outputs of a skipped request) and OR in their own bits.
  *  - Return value: TV_OK (0) or a negative TV_ERR_* code; tv_last_error()
  *    gives a message for the calling thread's last failure.
  *  - Launch order: every kernel is launched with programmatic dependent
