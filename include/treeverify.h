@@ -41,15 +41,19 @@
  *  - Return value: TV_OK (0) or a negative TV_ERR_* code; tv_last_error()
  *    gives a message for the calling thread's last failure.
  *  - Launch order: every kernel is launched with programmatic dependent
- *    launch and waits for the preceding kernel in the stream before it reads
- *    anything that kernel may write (and before it writes anything that kernel
- *    may read).  tv_tree_build_mask and tv_tree_verify_attn(_q4) let the next
- *    kernel in the stream be scheduled before they finish; a kernel of the
- *    caller's that follows one of them and is itself launched with the
- *    programmatic-launch attribute must wait (griddepcontrol.wait /
- *    cudaGridDependencySynchronize) before reading their outputs.  Kernels
- *    launched without that attribute, and host synchronisation, are
- *    unaffected.
+ *    launch and waits for the preceding kernel in the stream before it writes
+ *    anything, and before it reads anything that a call of this library
+ *    writes (status, masks, accept outputs, caches).  tv_tree_accept reads its
+ *    own inputs (logits, tokens, parents, n_nodes, uniforms) before that wait,
+ *    which no call of this library writes.  tv_tree_build_mask and
+ *    tv_tree_verify_attn(_q4) let the next kernel in the stream be scheduled
+ *    before they finish.  So a kernel of the caller's that is launched with
+ *    the programmatic-launch attribute must wait (griddepcontrol.wait /
+ *    cudaGridDependencySynchronize) before reading the outputs of a call it
+ *    follows, and one that precedes tv_tree_accept and signals its
+ *    dependents early must have written the accept's inputs before it
+ *    signals.  Kernels launched without that attribute, and host
+ *    synchronisation, are unaffected.
  */
 #ifndef TREEVERIFY_H_
 #define TREEVERIFY_H_
