@@ -42,10 +42,10 @@
  *    gives a message for the calling thread's last failure.
  *  - Launch order: every kernel is launched with programmatic dependent
  *    launch and waits for the preceding kernel in the stream before it writes
- *    anything, and before it reads anything that a call of this library
+ *    any output, and before it reads anything that a call of this library
  *    writes (status, masks, accept outputs, caches).  tv_tree_accept reads its
- *    own inputs (logits, tokens, parents, n_nodes, uniforms) before that wait,
- *    which no call of this library writes.  tv_tree_build_mask and
+ *    own inputs (logits, tokens, parents, n_nodes, uniforms) and fills its own
+ *    workspace before that wait; no call of this library writes those inputs.  tv_tree_build_mask and
  *    tv_tree_verify_attn(_q4) let the next kernel in the stream be scheduled
  *    before they finish.  So a kernel of the caller's that is launched with
  *    the programmatic-launch attribute must wait (griddepcontrol.wait /
