@@ -45,6 +45,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include "tv_common.cuh"
+#include "attn_plan.cuh"
 
 namespace tv {
 namespace attn {
@@ -125,134 +126,6 @@ struct Smem {
   static_assert(kAlloc + 2048 <= 227 * 1024, "shared memory over the per-CTA limit");
 };
 
-// ---------------------------------------------------------------- plan
-__device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
-__device__ __forceinline__ int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
-// ceil(a / c) for a cost per tile c in {2, 3}, 0 when a <= 0
-__device__ __forceinline__ int64_t ceil_div_c(int64_t a, int c) {
-  if (a <= 0) return 0;
-  return c == 2 ? (a + 1) >> 1 : (a + 2) / 3;
-}
-
-struct PlanView {
-  const int64_t* start;  // cost position of each request's first group; start[B] = W
-  const int32_t* T;      // KV tiles of each request (0 = request skipped)
-  const int32_t* MT;     // M tiles of each request
-  int B, Hkv;
-  int64_t W;             // total cost (< 2^40, so k * W fits in 64 bits)
-  int C;                 // CTAs that receive work
-  bool narrow;           // (C + 1) * W < 2^32: 32-bit division suffices
-  // first cost position of CTA k, and the CTA owning cost position x
-  __device__ int64_t cut(int k) const {
-    if (narrow) return ((uint32_t)k * (uint32_t)W + (uint32_t)(C - 1)) / (uint32_t)C;
-    return ((int64_t)k * W + C - 1) / C;
-  }
-  __device__ int owner(int64_t x) const {
-    if (narrow) return (int)min((uint32_t)(C - 1), ((uint32_t)x * (uint32_t)C) / (uint32_t)W);
-    return (int)imin64(C - 1, x * C / W);
-  }
-};
-
-struct Item {
-  int b, g, mp, nt;           // request, KV head, M-tile pair, active M tiles
-  int tile_begin, tile_end;   // KV tiles of this item
-  int k0, n_splits;           // first CTA of the group, number of splits
-  int slot0;                  // partial slot of split 0
-  int my_slot;                // partial slot of this CTA's split
-};
-
-// Iterates this CTA's items in the global (request, KV head, pair, tile) order.
-// A tile belongs to the CTA whose cost range holds the tile's first cost unit;
-// a tile of a group with nt active M tiles costs nt + 1 units.
-struct ItemIter {
-  int b, j;           // request and group index within it (j = g * MP + mp)
-  int64_t gstart;     // cost position of the current group's first tile
-  int c_prev;         // cost per tile of the group before the current one (0: none)
-  int produced;
-  int64_t lo, hi;     // this CTA's cost range
-};
-
-__device__ void iter_init(ItemIter& it, const PlanView& pv, int cta) {
-  it.produced = 0;
-  it.lo = pv.cut(cta);
-  it.hi = pv.cut(cta + 1);
-  it.c_prev = 0;
-  // largest b with start[b] <= lo (it has a non-zero cost), then its group
-  int lo_b = 0, hi_b = pv.B;
-  while (hi_b - lo_b > 1) {
-    const int mid = (lo_b + hi_b) >> 1;
-    if (pv.start[mid] <= it.lo) lo_b = mid; else hi_b = mid;
-  }
-  int b = lo_b;
-  while (b < pv.B && pv.T[b] == 0) ++b;
-  it.b = b;
-  it.j = 0;
-  it.gstart = b < pv.B ? pv.start[b] : pv.W;
-  if (b < pv.B) {
-    const int T = pv.T[b], MT = pv.MT[b], MP = (MT + 1) / 2;
-    const int64_t per_g = (int64_t)T * (MT + MP);
-    const int64_t off = it.lo - pv.start[b];
-    if (off > 0) {
-      // 32-bit divisions when every cost position fits in 32 bits
-      const int g = (int)imin64(pv.Hkv - 1, pv.narrow ? (int64_t)((uint32_t)off / (uint32_t)per_g) : off / per_g);
-      const int64_t off2 = off - g * per_g;
-      const int mp = (int)imin64(MP - 1, pv.narrow ? (int64_t)((uint32_t)off2 / (uint32_t)(3 * T))
-                                                   : off2 / (3ll * T));
-      it.j = g * MP + mp;
-      it.gstart = pv.start[b] + g * per_g + (int64_t)mp * 3 * T;
-    }
-    if (it.j > 0) {
-      const int mpp = (it.j - 1) % MP;
-      it.c_prev = min(2, MT - 2 * mpp) + 1;
-    } else {
-      int bp = b - 1;
-      while (bp >= 0 && pv.T[bp] == 0) --bp;
-      if (bp >= 0) {
-        const int MTp = pv.MT[bp], MPp = (MTp + 1) / 2;
-        it.c_prev = min(2, MTp - 2 * (MPp - 1)) + 1;
-      }
-    }
-  }
-}
-
-__device__ bool iter_next(ItemIter& it, const PlanView& pv, int cta, Item& o) {
-  for (;;) {
-    if (it.b >= pv.B || it.gstart >= it.hi) return false;
-    const int T = pv.T[it.b];
-    const int MT = pv.MT[it.b], MP = (MT + 1) / 2;
-    if (T == 0 || it.j >= pv.Hkv * MP) {
-      ++it.b;
-      it.j = 0;
-      continue;
-    }
-    const int g = it.j / MP, mp = it.j - g * MP;
-    const int nt = min(2, MT - 2 * mp);
-    const int c = nt + 1;
-    const int64_t gs = it.gstart;
-    const int64_t i_lo = imin64(T, ceil_div_c(it.lo - gs, c));
-    const int64_t i_hi = imin64(T, ceil_div_c(it.hi - gs, c));
-    const int c_prev = it.c_prev;
-    it.gstart += (int64_t)T * c;
-    it.c_prev = c;
-    ++it.j;
-    if (i_lo >= i_hi) continue;
-    o.b = it.b;
-    o.g = g;
-    o.mp = mp;
-    o.nt = nt;
-    o.tile_begin = (int)i_lo;
-    o.tile_end = (int)i_hi;
-    o.k0 = pv.owner(gs);
-    o.n_splits = pv.owner(gs + (int64_t)(T - 1) * c) - o.k0 + 1;
-    // split 0's slot: 2*k0 when the group is CTA k0's first item, else 2*k0 + 1;
-    // every later split is its CTA's first item
-    const bool first_of_k0 = (c_prev == 0) || pv.owner(gs - c_prev) < o.k0;
-    o.slot0 = 2 * o.k0 + (first_of_k0 ? 0 : 1);
-    o.my_slot = 2 * cta + (it.produced == 0 ? 0 : 1);
-    ++it.produced;
-    return true;
-  }
-}
 
 // Visibility of the 32 keys [base, base + 32) for a row with ancestor word anc.
 __device__ __forceinline__ uint32_t visible32(int base, int L, uint64_t anc) {
@@ -282,7 +155,6 @@ __device__ __forceinline__ int request_shape_bits(int L, int N, int n_max, int m
   return 0;
 }
 
-__device__ __forceinline__ int split_slot(const Item& it, int sp) { return sp == 0 ? it.slot0 : 2 * (it.k0 + sp); }
 
 // The last split of a (group, M tile) combines every split's normalised
 // partial rows by their log-sum-exp weights: out = sum_s w_s O_s with
