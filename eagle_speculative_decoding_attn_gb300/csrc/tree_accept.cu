@@ -967,7 +967,10 @@ namespace {
 template <int CL>
 int active_clusters(int dev) {
   static int known[64] = {};  // per device: clusters of CL that fit at once, plus 1 (0 = not yet known)
-  if (known[dev] == 0) {
+  static unsigned long long ctx_of[64] = {};  // the context the attributes were set in
+  unsigned long long ctx = 0;
+  if (tv::current_context_id(&ctx) != cudaSuccess) return -1;
+  if (known[dev] == 0 || ctx == 0 || ctx_of[dev] != ctx) {
     const void* f = (const void*)tv::tree_accept_kernel<CL>;
     if (cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return -1;
     if (tv::ensure_smem_attr(f, 2ull * tv::kMaxChunk * sizeof(float)) != cudaSuccess) return -1;
@@ -981,6 +984,7 @@ int active_clusters(int dev) {
       n = 0;
     }
     known[dev] = n + 1;
+    if (tv::current_context_id(&ctx_of[dev]) != cudaSuccess) ctx_of[dev] = 0;
   }
   return known[dev] - 1;
 }

@@ -1,6 +1,7 @@
 // Host-side helpers shared by every entry point: thread-local error text,
 // version string, cached device properties.
 #include <cstdarg>
+#include <cudaTypedefs.h>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -35,19 +36,45 @@ int current_sm_count() {
   return cached[dev];
 }
 
+cudaError_t current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_ctx = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_ctx = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+  });
+  *id = 0;
+  if (!get_ctx || !get_id) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return cudaErrorUnknown;
+  if (ctx == nullptr) return cudaSuccess;
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
+
 cudaError_t ensure_smem_attr(const void* func, size_t bytes) {
   static std::mutex mu;
-  static std::map<std::pair<int, const void*>, size_t> done;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::map<std::pair<unsigned long long, const void*>, size_t> done;
+  unsigned long long ctx = 0;
+  cudaError_t e = current_context_id(&ctx);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  auto key = std::make_pair(dev, func);
-  auto it = done.find(key);
-  if (it != done.end() && it->second >= bytes) return cudaSuccess;
+  if (ctx != 0) {
+    auto it = done.find(std::make_pair(ctx, func));
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+  }
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess) done[key] = bytes;
-  return e;
+  if (e != cudaSuccess) return e;
+  if (ctx == 0 && current_context_id(&ctx) != cudaSuccess) return cudaSuccess;  // not cached: set again next time
+  if (ctx != 0) done[std::make_pair(ctx, func)] = bytes;
+  return cudaSuccess;
 }
 
 }  // namespace tv

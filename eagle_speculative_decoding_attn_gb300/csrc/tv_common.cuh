@@ -39,7 +39,12 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // SM count of the current device (cached per device id).
 int current_sm_count();
 
-// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (device, kernel).
+// Unique id of the calling thread's current CUDA context (0: none yet).  The
+// library keys what it caches per context on it, so that a device reset (which
+// ends the context and loads the kernels again in a new one) is noticed.
+cudaError_t current_context_id(unsigned long long* id);
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (context, kernel).
 cudaError_t ensure_smem_attr(const void* func, size_t bytes);
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }

@@ -734,7 +734,10 @@ __global__ void __launch_bounds__(kQ4 ? kThreadsQ4 : kThreads, 1)
       const int node = mrow / G;
       const int hh = mrow - node * G;
       const bool row_ok = node < N;
-      const uint64_t anc = row_ok ? p.anc_mask[(int64_t)item.b * p.n_max + node] : 0ull;
+      // only bits of the request's own nodes count: a stray bit j >= N in the caller's
+      // word would otherwise expose position L + j, which holds no node of this tree
+      const uint64_t valid_bits = N >= 64 ? ~0ull : ((1ull << N) - 1ull);
+      const uint64_t anc = row_ok ? p.anc_mask[(int64_t)item.b * p.n_max + node] & valid_bits : 0ull;
       float m_run = -INFINITY, l_run = 0.f;
       for (int k = 0; k < n_units; ++k) {
         const int j = dual ? 2 * k + t : k;                       // stage of this unit
@@ -1230,23 +1233,33 @@ namespace attn {
 constexpr size_t kFixedScratchBytes = size_t(48) << 20;  // 48 MiB
 static __device__ __align__(256) uint8_t g_fixed_scratch[kFixedScratchBytes];
 
-// Device address of g_fixed_scratch on the current device.  In host code the
-// array's name only stands in for the symbol, so the address is looked up once
-// per device (with that device current) and cached.
+// Device address of g_fixed_scratch in the current context.  In host code the
+// array's name only stands in for the symbol, so its address is looked up with
+// the device current and cached per device together with the id of the context
+// it was found in.  A device reset (or any other new context on the device)
+// loads the library's module again, possibly at another address: a changed
+// context id makes the next call look the address up again instead of using the
+// old context's pointer.
 static int fixed_scratch_address(void** out) {
   static std::mutex mu;
   static void* addr[64] = {};
+  static unsigned long long ctx_of[64] = {};
   int dev = 0;
   TV_CUDA_CHECK(cudaGetDevice(&dev));
   TV_REQUIRE(dev >= 0 && dev < 64, TV_ERR_UNSUPPORTED, "tv_tree_verify_attn_noalloc: device id %d >= 64", dev);
+  unsigned long long ctx_id = 0;
+  TV_REQUIRE(current_context_id(&ctx_id) == cudaSuccess, TV_ERR_CUDA,
+             "tv_tree_verify_attn_noalloc: the current context could not be queried");
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  if (ctx_id == 0 || addr[dev] == nullptr || ctx_of[dev] != ctx_id) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_fixed_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_fixed_scratch);  // sets up the context if needed
     TV_REQUIRE(e == cudaSuccess && p != nullptr, TV_ERR_CUDA,
                "tv_tree_verify_attn_noalloc: cudaGetSymbolAddress of the built-in scratch failed: %s",
                cudaGetErrorString(e));
+    TV_REQUIRE(current_context_id(&ctx_id) == cudaSuccess && ctx_id != 0, TV_ERR_CUDA, "tv_tree_verify_attn_noalloc: no current CUDA context");
     addr[dev] = p;
+    ctx_of[dev] = ctx_id;
   }
   *out = addr[dev];
   return TV_OK;

@@ -177,6 +177,8 @@ size_t tv_tree_verify_attn_workspace(int B, int n_max, int Hq, int Hkv, int D, i
  *   lse = ln sum_t exp(s_t)
  *
  * where L = prefix_len[b] and A(i) = ancestors of i plus i (anc_mask[b][i]).
+ * Bits j >= n_nodes[b] of a node's word are ignored (only the request's own
+ * tree positions L..L+N-1 can be made visible).
  * The tree's own K/V must already sit at logical positions L..L+N-1 of the
  * request's pages; logical position t lives in physical page
  * page_table[b][t / 16], row t % 16.
@@ -213,8 +215,15 @@ int tv_tree_verify_attn(const void* q, const void* k_cache, const void* v_cache,
  * compiled into the library; every device that loads the library holds it
  * until the process exits.
  *  - The first call on each device looks up the array's device address (with
- *    that device current) and caches it; make that first call before any
- *    stream capture.
+ *    that device current) and caches it together with the id of the current
+ *    context; make that first call before any stream capture.  A call in a new
+ *    context on the device (after cudaDeviceReset, say) looks the address up
+ *    again, so that first call after a reset should also precede any capture.
+ *  - The scratch need is 2 * SMs * 256 * (2 * D + 8) bytes of split partials
+ *    plus 8 bytes per (request, KV head, M-tile pair) of split tickets: about
+ *    20.6 MB at D = 128 on 152 SMs for every workload shape this library is
+ *    measured on (the largest ticket area among them is 4 KB), well inside
+ *    48 MiB.
  *  - Sizes whose scratch need exceeds 48 MiB return TV_ERR_UNSUPPORTED with a
  *    message; use tv_tree_verify_attn with a workspace for those.
  *  - Every call shares the one array and clears its counters at the start

@@ -254,3 +254,37 @@ def test_attn_split_partials_past_fp16_range():
     assert np.all(err <= 1e-2 + (2.0 ** -7 + 2.0 ** -10) * np.abs(ref)), \
         f"large rows: max relative error {rel.max():.3e}; other rows: max error {err[~big].max():.3e}"
     assert np.abs(lse[0, :n] - ref_lse[0, :n]).max() <= 2e-3
+
+
+def test_attn_stray_mask_bits_ignored():
+    """Bits j >= n_nodes of a node's ancestor word name no node of the tree.
+    The attention ignores them: with every such bit set (and the cache slots
+    they would name filled with large keys) the outputs equal those of the
+    clean words bit for bit."""
+    dev = require_gpu()
+    rng = np.random.Generator(np.random.PCG64(46))
+    trees = [W.random_recursive_tree(rng, 20), W.chain_tree(5), W.random_recursive_tree(rng, 63)]
+    w = W.make_custom(B=3, Hq=16, Hkv=4, D=128, prefix_len=[100, 37, 500], parents_list=trees, seed=47,
+                      n_max=64)
+    k2 = w.k_bits.copy()
+    for b in range(w.B):
+        L, N = int(w.prefix_len[b]), int(w.n_nodes[b])
+        cap = 16 * int((w.page_table[b] >= 0).sum())
+        for pos in range(L + N, cap):          # slots past the tree in the request's own pages
+            k2[w.page_table[b, pos // 16], :, pos % 16] = W.to_bf16_bits(np.full((w.Hkv, w.D), 8.0, np.float32))
+    dw = DevWorkload(w, dev, logits=False)
+    kd = bf16_dev(k2, dev)
+    out0, lse0, st0 = dw.attn(k=kd)
+    anc, _, status = dw.mask()
+    words = anc.cpu().numpy().view(np.uint64).copy()
+    for b in range(w.B):
+        N = int(w.n_nodes[b])
+        stray = np.uint64(0) if N >= 64 else ~np.uint64((1 << N) - 1)
+        words[b, :N] |= stray
+    anc2 = to_dev(words.view(np.int64), dev)
+    out1, lse1, st1 = dw.attn(status=status, anc=anc2, k=kd)
+    assert (st0 == 0).all() and (st1 == 0).all()
+    for b in range(w.B):
+        n = int(w.n_nodes[b])
+        assert np.array_equal(out0[b, :n], out1[b, :n]), b
+        assert np.array_equal(lse0[b, :n], lse1[b, :n]), b

@@ -157,3 +157,79 @@ def test_quantize_codes_match_float32_definition():
             c = min(15, max(0, c))
             got = (codes[r, d // 2] >> (4 * (d % 2))) & 15
             assert got == c
+
+
+def _fp16_round_exact(fr):
+    """The float16 nearest to the rational fr (ties to even mantissa), found by
+    exact comparison with the neighbours of a first guess."""
+    from fractions import Fraction
+    g = np.float16(float(fr))
+    cands = {g, np.nextafter(g, np.float16(np.inf)), np.nextafter(g, np.float16(-np.inf))}
+    best = None
+    for c in cands:
+        if not np.isfinite(c):
+            continue
+        d = abs(Fraction(float(c)) - fr)
+        even = (int(np.array(c, np.float16).view(np.uint16)) & 1) == 0
+        key = (d, not even)
+        if best is None or key < best[0]:
+            best = (key, c)
+    return best[1]
+
+
+def test_quantize_against_exact_rational_rounding():
+    """The encoder's integer decisions against exact arithmetic (Python
+    fractions), independent of its float32 steps.
+
+    Parameters: zero is the float16 nearest to the group minimum and scale the
+    float16 nearest to (max - min) / 15, both rounded exactly here.  Codes: the
+    nearest integer (ties to even) to the exact rational (x - zero) / scale,
+    clamped to [0, 15], for the stored (scale, zero).  The float32 form rounds
+    x - zero, 1 / scale and their product once each (relative error at most
+    3 * 2^-24 of a quotient <= 15.5), so a code may differ from the exact one
+    only where the exact quotient lies within 16 * 3 * 2^-24 of a half-integer;
+    every differing code is checked to be such a case and the count is bounded."""
+    from fractions import Fraction
+    rng = np.random.default_rng(21)
+    rows = [rng.standard_normal((600, 128)).astype(np.float32),                       # the workloads' N(0, 1)
+            (rng.standard_normal((200, 128)) * rng.uniform(1e-3, 50, (200, 1))).astype(np.float32),
+            rng.integers(-8, 8, (50, 128)).astype(np.float32) * 0.5]                 # exact steps, many ties
+    x = np.concatenate(rows)
+    xb = _bits(x)
+    codes, params = oracle.quantize_q4(xb)
+    xv = oracle.bf16_to_f64(xb)
+    n_rows, D = xv.shape
+    q = np.empty((n_rows, D), np.int64)
+    q[:, 0::2], q[:, 1::2] = codes & 15, codes >> 4
+    slack = Fraction(16 * 3, 2 ** 24)
+    n_codes = n_diff = n_param_diff = 0
+    for r in range(n_rows):
+        for grp in range(D // 32):
+            vals = [Fraction(float(v)) for v in xv[r, 32 * grp: 32 * grp + 32]]
+            mn, mx = min(vals), max(vals)
+            s_ex = _fp16_round_exact((mx - mn) / 15)
+            z_ex = _fp16_round_exact(mn)
+            s_got, z_got = params[r, 2 * grp], params[r, 2 * grp + 1]
+            assert z_got == z_ex, (r, grp)
+            if s_got != s_ex:
+                # float32 then float16 (double rounding) may differ from one exact rounding
+                # only next to a float16 tie
+                n_param_diff += 1
+                assert abs(float(s_got) - float(s_ex)) <= float(np.spacing(np.float16(s_ex))), (r, grp)
+            s, z = Fraction(float(s_got)), Fraction(float(z_got))
+            for d in range(32):
+                n_codes += 1
+                got = int(q[r, 32 * grp + d])
+                if s == 0:
+                    assert got == 0
+                    continue
+                t = (vals[d] - z) / s
+                exact = min(15, max(0, round(t)))          # round() of a Fraction: ties to even
+                if got != exact:
+                    n_diff += 1
+                    half = Fraction(2 * min(got, exact) + 1, 2)
+                    assert abs(got - exact) == 1 and abs(t - half) <= slack, (r, grp, d, float(t))
+    assert n_codes == n_rows * D
+    assert n_diff <= n_codes // 10000, n_diff
+    assert n_param_diff <= (n_rows * D // 32) // 1000, n_param_diff
+    print(f"exact-rounding pin: {n_diff} of {n_codes} codes and {n_param_diff} scales differ (all at ties)")
