@@ -14,7 +14,7 @@
 
 #ifdef __CUDACC__
 #define TV_PLAN_INL __host__ __device__ __forceinline__
-#define TV_PLAN_FN __host__ __device__
+#define TV_PLAN_FN __host__ __device__ inline
 #else
 #define TV_PLAN_INL inline
 #define TV_PLAN_FN inline

@@ -276,6 +276,12 @@ size_t tv_tree_accept_workspace(int B, int n_max, int V);
  * rejection against the renormalised draft keeps the output distribution
  * exactly the target's under such drafting, as the fixed-q rule does under
  * i.i.d. drafting.
+ * Which rule is lossless depends only on how the children were drafted: a tree
+ * grown by sampled top-k expansion (distinct sibling tokens, e.g. the Gumbel
+ * top-k of the draft row) needs this flag; children drawn independently from
+ * q (repeats allowed) need flags = 0.  Neither rule is lossless for the
+ * other's drafting, and a deterministic top-k (argmax) expansion is lossless
+ * under neither.
  *
  *  target_logits float [B, n_max, V]; draft_logits float [B, n_max, V] (row n =
  *    the distribution n's children were drawn from; may be NULL when greedy)

@@ -96,6 +96,23 @@ def test_attn_large_configs_sampled(name):
         assert np.isfinite(out[b, : int(w.n_nodes[b])]).all()
 
 
+@pytest.mark.parametrize("name,which", [("llama3_70b", "longest"), ("llama3_70b", "shortest"), ("long", "first")])
+def test_attn_full_request_every_row(name, which):
+    """Every (node, query head) row of one whole request of a G = 8 workload at
+    the plain bound: all eight KV heads, both M-tile pairs of each, and every
+    split of the request's key range with its merge (the sampled comparison
+    above covers a few rows of every request; this covers one request whole)."""
+    dev = require_gpu()
+    w = W.make_workload(name, with_logits=False)
+    out, lse, st = DevWorkload(w, dev, logits=False).attn()
+    assert (st == 0).all()
+    b = {"longest": int(np.argmax(w.prefix_len)), "shortest": int(np.argmin(w.prefix_len)), "first": 0}[which]
+    rows = [(b, i, h) for i in range(int(w.n_nodes[b])) for h in range(w.Hq)]
+    ref_out, ref_lse, _ = _oracle(w, rows=rows)
+    mx, mean = compare_attn(out, lse, ref_out, ref_lse, w, rows=rows)
+    print(f"{name} request {b} (prefix {int(w.prefix_len[b])}): {len(rows)} rows, max err {mx:.2e}, mean {mean:.2e}")
+
+
 def test_attn_page_shuffle_bit_exact():
     dev = require_gpu()
     rng = np.random.Generator(np.random.PCG64(44))
