@@ -891,7 +891,7 @@ static int launch(const AttnParams& ap, int grid, cudaStream_t st) {
 // fewer rows per KV head (MHA, small trees) run one CTA per SM with its own
 // 256-row M-tile pairs.  Head dim 64 always runs one CTA per SM.
 static int launch_bf16(const AttnParams& ap, int D, int n_max, int grid, cudaStream_t st) {
-  if (D == 128 && n_max * ap.G >= 2 * 2 * kBM) return launch_pair(ap, grid, st);
+  if (D == 128 && n_max * ap.G >= 2 * 2 * kBM && n_max * ap.G <= 8 * kBM) return launch_pair(ap, grid, st);
   return D == 128 ? launch<128, false>(ap, grid, st) : launch<64, false>(ap, grid, st);
 }
 

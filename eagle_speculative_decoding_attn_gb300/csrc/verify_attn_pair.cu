@@ -29,8 +29,11 @@
 //    reference max that a chain's first stage sets and later stages keep while
 //    their probabilities stay below 2^32 (checked on the row sum, no max pass);
 //    a stage that would pass it raises the reference and rescales O (rare).
-//  * Work division: the plan of verify_attn.cu over clusters; a group is
-//    (request, KV head, 256-row block), split groups merge per CTA half.
+//  * Work division: block c of every KV head runs on the clusters of lane c;
+//    within a lane the plan of verify_attn.cu splits the (request, KV head,
+//    KV tile) sequence evenly over its clusters, so the lanes read each K/V
+//    tile at about the same time (one read from DRAM, the others from L2).
+//    Split groups merge per CTA half.
 //  * Every wait is bounded (about one second); on a timeout the kernel unwinds
 //    and reports TV_DEV_TIMEOUT for the request, as the one-CTA kernel does.
 #include <algorithm>
@@ -45,6 +48,7 @@ constexpr int kPStages = 4;         // K and V ring depth (half tiles)
 constexpr int kPThreads = 384;      // 12 warps
 constexpr int kPHalfKeys = 64;      // keys of this CTA's K half tile
 constexpr uint32_t kWgArrivals = 8; // one arrival per warp of a softmax warpgroup, from both CTAs
+constexpr int kMaxLanes = 4;        // 256-row blocks per KV head (n_max * G <= 1024)
 
 struct PairSmem {
   static constexpr int kQTile = kBM * kPD * 2;          // [2 dim blocks][128 rows][128 B]
@@ -61,9 +65,12 @@ struct PairSmem {
   static_assert(kAlloc + 4096 <= 227 * 1024, "shared memory over the per-CTA limit");
 };
 
-// Partial slot of this CTA for the plan's slot s (plan slots count clusters;
-// each CTA of the pair keeps its own rows in its own slot).
-__device__ __forceinline__ int pair_ws_slot(int s, uint32_t rank) { return ((s >> 1) * 2 + (int)rank) * 2 + (s & 1); }
+// Partial slot of this CTA for slot s of its lane's plan (plan slots count the
+// lane's clusters from lane_base; each CTA of the pair keeps its own rows in its
+// own slot).
+__device__ __forceinline__ int pair_ws_slot(int lane_base, int s, uint32_t rank) {
+  return ((lane_base + (s >> 1)) * 2 + (int)rank) * 2 + (s & 1);
+}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     verify_attn_pair_kernel(const __grid_constant__ AttnParams p) {
@@ -79,7 +86,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
   __shared__ int64_t plan_W;
-  __shared__ int plan_C;
+  __shared__ int plan_C, plan_lane, plan_base;
   __shared__ int ticket_sh[kNT];
   __shared__ int last_cta_sh;
   __shared__ int last_b_sh;
@@ -128,23 +135,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   griddep_wait();
   griddep_launch_dependents();
   if (warp == 3) {
-    // ---- plan over clusters: per-request tiles and 256-row blocks (two "M tiles" of
-    // the one-CTA plan per block, so every tile of every group costs the same)
+    // ---- plan.  Block c (query rows 256c .. 256c + 255) of every (request, KV head)
+    // belongs to lane c; each lane gets a share of the clusters proportional to its
+    // cost, and within a lane the clusters split the (request, KV head, KV tile)
+    // sequence evenly (the one-CTA plan with one 256-row "M-tile pair" per KV head).
+    // The lanes walk the same sequence at the same pace, so the blocks of one KV
+    // head read each K/V tile at about the same time and all but one read come
+    // from L2.
+    // pass 1: lane costs (every tile costs 3 units, as a pair of M tiles does)
+    int64_t wl[kMaxLanes];
+#pragma unroll
+    for (int l = 0; l < kMaxLanes; ++l) wl[l] = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int b = base + lane;
+      int64_t cost = 0;
+      int chains = 0;
+      if (b < p.B) {
+        const int L = p.prefix_len[b], N = p.n_nodes[b];
+        const bool skip = p.status[b] != 0 || request_shape_bits(L, N, p.n_max, p.max_pages) != 0;
+        if (!skip) {
+          cost = (int64_t)p.Hkv * ((L + N + kBN - 1) / kBN) * 3;
+          chains = (N * p.G + 2 * kBM - 1) / (2 * kBM);
+        }
+      }
+#pragma unroll
+      for (int l = 0; l < kMaxLanes; ++l) {
+        int64_t c = (l < p.mp_max && chains > l) ? cost : 0;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+        wl[l] += c;
+      }
+    }
+    // clusters of each lane: one for every lane with work, the rest by cost
+    int64_t w_all = 0;
+    int nz = 0;
+#pragma unroll
+    for (int l = 0; l < kMaxLanes; ++l) {
+      w_all += wl[l];
+      nz += wl[l] > 0;
+    }
+    const int spare = max(0, n_cl - nz);
+    int my_lane = -1, lane_base = 0, lane_cl = 0, first = 0;
+#pragma unroll
+    for (int l = 0; l < kMaxLanes; ++l) {
+      const int cnt = wl[l] > 0 ? 1 + (int)(spare * wl[l] / imax64(1, w_all)) : 0;
+      if (my_lane < 0 && cl >= first && cl < first + cnt) {
+        my_lane = l;
+        lane_base = first;
+        lane_cl = cnt;
+      }
+      first += cnt;
+    }
+    // pass 2: this lane's plan (requests whose rows reach block my_lane)
     int64_t carry = 0;
     for (int base = 0; base < p.B; base += 32) {
       const int b = base + lane;
       int64_t cost = 0;
       if (b < p.B) {
         const int L = p.prefix_len[b], N = p.n_nodes[b];
-        const bool skip = p.status[b] != 0 || request_shape_bits(L, N, p.n_max, p.max_pages) != 0;
-        int T = 0, MT = 0;
-        if (!skip) {
-          T = (L + N + kBN - 1) / kBN;
-          MT = 2 * ((N * p.G + 2 * kBM - 1) / (2 * kBM));
-          cost = (int64_t)p.Hkv * T * (MT + MT / 2);
-        }
+        const bool skip = my_lane < 0 || p.status[b] != 0 || request_shape_bits(L, N, p.n_max, p.max_pages) != 0 ||
+                          (N * p.G + 2 * kBM - 1) / (2 * kBM) <= my_lane;
+        const int T = skip ? 0 : (L + N + kBN - 1) / kBN;
+        cost = (int64_t)p.Hkv * T * 3;
         rq_T[b] = T;
-        rq_MT[b] = MT;
+        rq_MT[b] = 2;
       }
       int64_t incl = cost;
 #pragma unroll
@@ -158,7 +212,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     if (lane == 0) {
       rq_start[p.B] = carry;
       plan_W = carry;
-      plan_C = (int)imax64(1, imin64(n_cl, carry / 3));
+      plan_C = (int)imax64(1, imin64(lane_cl, carry / 3));
+      plan_lane = my_lane;
+      plan_base = lane_base;
     }
   }
   tc_fence_before();
@@ -176,7 +232,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   pv.W = plan_W;
   pv.C = plan_C;
   pv.narrow = (int64_t)(plan_C + 1) * plan_W < (int64_t(1) << 32);
-  const bool has_work = pv.W > 0 && cl < pv.C;
+  const int lane_id = plan_lane;          // this cluster's 256-row block index
+  const int wk = cl - plan_base;          // this cluster's worker index within its lane
+  const bool has_work = lane_id >= 0 && pv.W > 0 && wk < pv.C;
 
   uint8_t* sQ = smem + S::kQ;
   uint8_t* sK = smem + S::kK;
@@ -191,17 +249,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const bool is_k = warp == 0;
     if (elect_one_sync()) {
       ItemIter it;
-      iter_init(it, pv, cl);
+      iter_init(it, pv, wk);
       Item item;
       uint32_t kv_it = 0, n_item = 0;
       bool ok = true;
       auto leader = [&](uint64_t* bar) { return mapa_shared(smem_u32(bar), 0); };
-      while (ok && iter_next(it, pv, cl, item)) {
+      while (ok && iter_next(it, pv, wk, item)) {
         if (is_k) {
           // Q of the previous item is free once its last QK^T has completed
           if (n_item > 0) ok = mbar_wait(&bar_qe, (n_item - 1) & 1u, &abort_sh);
           if (!ok) break;
-          const int node0 = (item.mp * 2 * kBM + (int)rank * kBM) / G;
+          const int node0 = (lane_id * 2 * kBM + (int)rank * kBM) / G;
           if (rank == 0) mbar_arrive_expect_tx(&bar_q, (uint32_t)(2 * 2 * p.q_box_nodes * G * 128));
           for (int db = 0; db < 2; ++db)
             tma_load_4d_pair(sQ + db * (kBM * 128), &p.tmQ, leader(&bar_q), db * 64, item.g * G, node0, item.b);
@@ -266,13 +324,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       const uint64_t dk0 = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dv0 = sdesc_sw128(smem_u32(sV), kBN * 128, 1024);
       ItemIter it;
-      iter_init(it, pv, cl);
+      iter_init(it, pv, wk);
       Item item;
       uint32_t kv_it = 0, n_item = 0;
       uint32_t ph_p = 0;             // bit t: phase of bar_p[t]
       uint32_t uses[kNT] = {0, 0};   // items that used accumulator t so far
       bool ok = true;
-      while (ok && iter_next(it, pv, cl, item)) {
+      while (ok && iter_next(it, pv, wk, item)) {
         const int T = item.tile_end - item.tile_begin;
         int kf_next = 0, vf_next = 0;
         auto slot = [&](int j) { return (int)((kv_it + j) % kPStages); };
@@ -341,10 +399,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     // ------------------------------------------------------------ page-table check
     setmaxnreg_dec<kRegsControl>();
     ItemIter it;
-    iter_init(it, pv, cl);
+    iter_init(it, pv, wk);
     Item item;
     int prev_b = -1;
-    while (iter_next(it, pv, cl, item)) {
+    while (iter_next(it, pv, wk, item)) {
       if (item.b == prev_b) continue;
       prev_b = item.b;
       const int L = p.prefix_len[item.b], N = p.n_nodes[item.b];
@@ -367,7 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const uint32_t tO1 = tmem + lane_base + 256 + D;     // chain 1's O (read by warpgroup 0)
     const float sl2 = p.scale_log2;
     ItemIter it;
-    iter_init(it, pv, cl);
+    iter_init(it, pv, wk);
     Item item;
     uint32_t kv_it = 0;
     uint32_t ph_s = 0, ph_o = 0, ph_ml = 0, ph_wg = 0;
@@ -399,7 +457,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           pm[u] = fmax3(pm[u], __uint_as_float(x[c + 2 * u]), __uint_as_float(x[c + 2 * u + 1]));
       return fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
     };
-    while (ok && iter_next(it, pv, cl, item)) {
+    while (ok && iter_next(it, pv, wk, item)) {
       const int T = item.tile_end - item.tile_begin;
       const bool dual = T >= 2;
       // the item's partial last tile (if any) completes a phase of CTA 1's barrier of
@@ -418,7 +476,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       // only bits of the request's own nodes count: a stray bit j >= N in the caller's
       // word would otherwise expose position L + j, which holds no node of this tree
       const uint64_t valid_bits = N >= 64 ? ~0ull : ((1ull << N) - 1ull);
-      const int mrow0 = item.mp * 2 * kBM + (int)rank * kBM;  // first row of this CTA's half of the group
+      const int mrow0 = lane_id * 2 * kBM + (int)rank * kBM;  // first row of this CTA's half of the group
       const int mrow = mrow0 + r;
       const int node = mrow / G;
       const int hh = mrow - node * G;
@@ -545,7 +603,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       const int h = item.g * G + hh;
       const int64_t orow_idx = ((int64_t)item.b * p.n_max + node) * p.Hq + h;
       const bool direct = item.n_splits == 1;
-      const int my_slot = pair_ws_slot(item.my_slot, rank);
+      const int my_slot = pair_ws_slot(plan_base, item.my_slot, rank);
       // the normalised row (both chains in dual mode), in chunks of 32 columns
       auto row_chunk = [&](int c0, float* y) {
         uint32_t o[32];
@@ -621,7 +679,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         __threadfence();
         ok = wg_sync();
         if (!ok) break;
-        const int tick_idx = (((item.b * p.Hkv + item.g) * p.mp_max + item.mp) * kNT) + (int)rank;
+        const int tick_idx = (((item.b * p.Hkv + item.g) * p.mp_max + lane_id) * kNT) + (int)rank;
         if (r == 0) ticket_sh[0] = atomicAdd(p.ws_tickets + tick_idx, 1);
         ok = wg_sync();
         if (!ok) break;
@@ -629,7 +687,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           __threadfence();
           const int n_rows = min(kBM, N * G - mrow0);
           if (n_rows > 0) {
-            auto slot_of = [&](int sp) { return pair_ws_slot(split_slot(item, sp), rank); };
+            auto slot_of = [&](int sp) { return pair_ws_slot(plan_base, split_slot(item, sp), rank); };
             if (item.n_splits <= 2) merge_items<D, 2, 8, kBM>(p, item, mrow0, 0, n_rows, r, slot_of);
             else if (item.n_splits <= 4) merge_items<D, 4, 4, kBM>(p, item, mrow0, 0, n_rows, r, slot_of);
             else if (item.n_splits <= 6) merge_items<D, 6, 4, kBM>(p, item, mrow0, 0, n_rows, r, slot_of);
