@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--profile-accept", type=int, default=0,
                     help="profiler capture mode: N tree_accept calls on the chosen config (its greedy or sampling "
                          "mode) and exit")
+    ap.add_argument("--profile-step", type=int, default=0,
+                    help="profiler capture mode: N eager steps (mask, attention, accept, commit) and exit")
     ap.add_argument("--profile-quant", type=int, default=0,
                     help="profiler capture mode: N 4-bit encodings of the chosen config's K cache layer and exit")
     ap.add_argument("--breakdown", action="store_true",
@@ -711,6 +713,38 @@ def profile_accept(args, W, tvb, dev):
                       "status": status.cpu().numpy().tolist()}))
 
 
+def profile_step(args, W, tvb, dev):
+    """A small self-contained command for profiler launch lists: N eager steps
+    (mask, attention, accept, commit over the config's layers) on the chosen
+    config."""
+    import numpy as np
+    import torch
+    cfg = W.CONFIG_BY_NAME[args.config]
+    w = W.make_workload(args.config)
+    g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    bf = lambda b: g(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16)
+    sampling = w.temperature > 0
+    parents, n_nodes, tokens, L, pt = g(w.parents), g(w.n_nodes), g(w.tokens), g(w.prefix_len), g(w.page_table)
+    target = g(w.target_logits)
+    draft = g(w.draft_logits) if sampling else None
+    ua = g(w.u_accept) if sampling else None
+    us = g(w.u_sample) if sampling else None
+    q = bf(w.q_bits)
+    k = bf(w.k_bits).unsqueeze(0).repeat(cfg.n_layers_commit, 1, 1, 1, 1).contiguous()
+    v = bf(w.v_bits).unsqueeze(0).repeat(cfg.n_layers_commit, 1, 1, 1, 1).contiguous()
+    ws = tvb.new_attn_workspace(w.B, w.n_max, w.Hq, w.Hkv, w.D, dev)
+    aws = tvb.new_accept_workspace(w.B, w.n_max, w.V, dev)
+    for _ in range(args.profile_step):
+        anc, depth, status = tvb.tree_build_mask(parents, n_nodes)
+        tvb.tree_verify_attn(q, k[0], v[0], pt, L, n_nodes, anc, w.scale, status, workspace=ws)
+        acc = tvb.tree_accept(target, draft, tokens, parents, n_nodes, anc, depth, w.temperature, ua, us, status,
+                              workspace=aws)
+        tvb.kv_commit_path(k, v, pt, L, n_nodes, acc[0], acc[1], status)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_step": args.config, "steps": args.profile_step,
+                      "status": status.cpu().numpy().tolist()}))
+
+
 def profile_quant(args, W, tvb, dev):
     """A small self-contained command for profiler captures: N 4-bit
     encodings of the chosen config's K cache (one layer)."""
@@ -766,6 +800,8 @@ def main():
         return profile_accept(args, W, tvb, dev)
     if args.profile_quant:
         return profile_quant(args, W, tvb, dev)
+    if args.profile_step:
+        return profile_step(args, W, tvb, dev)
 
     cfg = W.CONFIG_BY_NAME[args.config]
     w = W.make_workload(cfg)
