@@ -294,7 +294,11 @@ size_t tv_tree_accept_workspace(int B, int n_max, int V);
  *  out_tokens  int32 [B, n_max+1] out: tokens of n_1..n_a, the bonus, then -1
  *  ws, ws_bytes  workspace of at least tv_tree_accept_workspace(B, n_max, V)
  *                bytes (may be NULL when that is 0); TV_ERR_INVALID_ARG if smaller
- *  status      int32 [B]          in/out: TV_DEV_BAD_TOKEN
+ *  status      int32 [B]          in/out: TV_DEV_BAD_TOKEN, TV_DEV_TIMEOUT
+ *
+ * Sampling holds each request's two rows in registers across one cluster of
+ * at most 16 CTAs: V <= 262144 (TV_ERR_UNSUPPORTED above).  Greedy has no
+ * limit on V.
  */
 int tv_tree_accept(const float* target_logits, const float* draft_logits, const int32_t* tokens,
                    const int32_t* parents, const int32_t* n_nodes, const uint64_t* anc_mask,

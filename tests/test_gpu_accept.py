@@ -216,9 +216,9 @@ def test_accept_errors():
     assert int(a.cpu()[0]) == 0 and (pn.cpu().numpy() == -1).all() and (ot.cpu().numpy() == -1).all()
     with pytest.raises(tvb.TreeVerifyError):
         tvb.tree_accept(dw.target, None, dw.tokens, dw.parents, dw.n_nodes, anc, depth, 1.0, None, None, st)
-    # sampling keeps each CTA's vocabulary slice on chip: at most 26624 entries per
-    # CTA, with 16 CTAs per request for one request and 8 for a batch of 12
-    for B, V in ((1, 16 * 26624 + 64), (12, 8 * 26624 + 64)):
+    # sampling keeps each request's rows in registers: at most 16 CTAs of 512
+    # threads with 32 entries each
+    for B, V in ((1, 16 * 512 * 32 + 4), (12, 16 * 512 * 32 + 64)):
         big = torch.zeros((B, 2, V), dtype=torch.float32, device=dev)
         two = lambda t: t[:, :2].expand(B, 2).contiguous()
         with pytest.raises(tvb.TreeVerifyError):
