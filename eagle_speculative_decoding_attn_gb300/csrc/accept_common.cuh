@@ -12,65 +12,96 @@ struct AccTree {
   int kid_off[kMaxNodes + 1];  // children of node n: kids[kid_off[n] .. kid_off[n + 1])
   int kids[kMaxNodes];
   float ua[kMaxNodes];         // u_accept of each node (sampling)
-  int cnt;
-  int bad;
+  float us[kMaxNodes];         // u_sample of each node (sampling)
+  unsigned long long cmask[kMaxNodes];  // bit j: node j is a child of node n
 };
 
-// Loads request b's tree (one node per thread), validates it and builds the
-// child lists.  Every CTA that calls it computes the same result.  Returns 0,
+// One request's tree inputs as thread tid (< n_max) loaded them.
+struct AccTreeIn {
+  int N, par, tok;
+  float ua, us;
+};
+
+// Issues the loads of request b's node count and of node tid's parent, token,
+// u_accept and u_sample (the uniforms when given); the values are used later
+// by acc_tree_build.
+__device__ __forceinline__ AccTreeIn acc_tree_load(const int32_t* parents, const int32_t* tokens,
+                                                   const float* u_accept, const float* u_sample,
+                                                   const int32_t* n_nodes, int b, int n_max) {
+  const int tid = threadIdx.x;
+  AccTreeIn in{n_nodes[b], -2, 0, 0.f, 0.f};
+  if (tid < n_max) {
+    in.par = parents[(int64_t)b * n_max + tid];
+    in.tok = tokens[(int64_t)b * n_max + tid];
+    if (u_accept) in.ua = u_accept[(int64_t)b * n_max + tid];
+    if (u_sample) in.us = u_sample[(int64_t)b * n_max + tid];
+  }
+  return in;
+}
+
+// Validates the tree and builds the child lists (ascending child index).
+// Every CTA that calls it computes the same result.  Returns 0,
 // TV_DEV_BAD_TREE (n_nodes out of [1, n_max], a root that is not -1, a parent
 // not below its child) or TV_DEV_BAD_TOKEN (a non-root token outside [0, V)).
 // Needs at least 64 threads; ends with a block barrier.
-__device__ inline int acc_tree_setup(AccTree& t, const int32_t* parents, const int32_t* tokens,
-                                     const float* u_accept, const int32_t* n_nodes, int b, int n_max, int V) {
-  const int tid = threadIdx.x;
-  const int N = n_nodes[b];
+__device__ inline int acc_tree_build(AccTree& t, const AccTreeIn& in, int n_max, int V) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const int N = in.N;
   const bool n_ok = N >= 1 && N <= n_max;
-  bool sbad = false, tbad = false;
-  if (n_ok && tid < N) {
-    const int pi = parents[(int64_t)b * n_max + tid];
-    const int ti = tokens[(int64_t)b * n_max + tid];
-    t.par[tid] = pi;
-    t.tok[tid] = ti;
-    sbad = tid == 0 ? pi != -1 : (pi < 0 || pi >= tid);
-    tbad = tid >= 1 && (ti < 0 || ti >= V);
+  const bool live = n_ok && tid < N;
+  const bool sbad = live && (tid == 0 ? in.par != -1 : (in.par < 0 || in.par >= tid));
+  const bool tbad = live && tid >= 1 && (in.tok < 0 || in.tok >= V);
+  if (tid < kMaxNodes) {
+    t.par[tid] = live ? in.par : -2;
+    t.tok[tid] = in.tok;
+    t.ua[tid] = in.ua;
+    t.us[tid] = in.us;
   }
-  const bool any_s = __syncthreads_or(sbad) != 0;
-  const bool any_t = __syncthreads_or(tbad) != 0;
-  const int bad = (!n_ok || any_s) ? TV_DEV_BAD_TREE : (any_t ? TV_DEV_BAD_TOKEN : 0);
-  if (bad == 0 && tid < kMaxNodes) {  // warps 0 and 1, whole
-    // children of node tid, then the exclusive scan of the counts over the nodes
-    int cnt = 0;
-    if (tid < N)
-      for (int j = 1; j < N; ++j) cnt += t.par[j] == tid;
-    int incl = cnt;
+  int bad = 0;
+  if (__syncthreads_or(sbad || tbad)) bad = __syncthreads_or(sbad) ? TV_DEV_BAD_TREE : TV_DEV_BAD_TOKEN;
+  if (!n_ok) bad = TV_DEV_BAD_TREE;
+  if (bad) return bad;  // uniform
+  // child masks by ballot: warp w takes nodes w, w + nwarps, ...
+  {
+    const int p0 = lane >= 1 ? t.par[lane] : -2, p1 = t.par[lane + 32];
+    for (int n = warp; n < N; n += nwarps) {
+      const unsigned lo = __ballot_sync(0xffffffffu, p0 == n);
+      const unsigned hi = __ballot_sync(0xffffffffu, p1 == n);
+      if (lane == 0) t.cmask[n] = (unsigned long long)lo | ((unsigned long long)hi << 32);
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // offsets: exclusive scan of the child counts, nodes lane and lane + 32
+    const int c0 = lane < N ? __popcll(t.cmask[lane]) : 0;
+    const int c1 = lane + 32 < N ? __popcll(t.cmask[lane + 32]) : 0;
+    int i0 = c0, i1 = c1;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if ((tid & 31) >= o) incl += y;
+      const int y0 = __shfl_up_sync(0xffffffffu, i0, o);
+      const int y1 = __shfl_up_sync(0xffffffffu, i1, o);
+      if (lane >= o) {
+        i0 += y0;
+        i1 += y1;
+      }
     }
-    if (tid == 31) t.cnt = incl;  // warp 0's total
-    if (tid < N) {
-      t.kid_off[tid] = incl - cnt;
-      if (u_accept) t.ua[tid] = u_accept[(int64_t)b * n_max + tid];
+    const int tot0 = __shfl_sync(0xffffffffu, i0, 31);
+    t.kid_off[lane] = i0 - c0;
+    t.kid_off[lane + 32] = tot0 + i1 - c1;
+    if (lane == 31) t.kid_off[64] = tot0 + i1;
+    __syncwarp();
+    // child j goes after its lower-indexed siblings
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = lane + 32 * h;
+      if (j >= 1 && j < N) {
+        const int pj = t.par[j];
+        t.kids[t.kid_off[pj] + __popcll(t.cmask[pj] & ((1ull << j) - 1ull))] = j;
+      }
     }
   }
-  if (tid == 0) t.bad = bad;
   __syncthreads();
-  if (bad == 0 && tid < N) {
-    if (tid >= 32) t.kid_off[tid] += t.cnt;
-    if (tid == N - 1) t.kid_off[N] = N - 1;  // every non-root node is somebody's child
-  }
-  __syncthreads();
-  if (bad == 0 && tid >= 1 && tid < N) {
-    // ascending child index within each parent's list
-    const int pj = t.par[tid];
-    int before = 0;
-    for (int k = 1; k < tid; ++k) before += t.par[k] == pj;
-    t.kids[t.kid_off[pj] + before] = tid;
-  }
-  __syncthreads();
-  return bad;
+  return 0;
 }
 
 // Sampling acceptance with every CTA's vocabulary slice in registers

@@ -137,7 +137,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(kAccThreads, 1)
   // status, which that kernel may write, is read and written after the wait
   // before the outputs.  Tree setup and validation: every CTA redundantly,
   // identical results.
-  const int bad = acc_tree_setup(sh.tr, p.parents, p.tokens, nullptr, p.n_nodes, b, n_max, V);
+  const AccTreeIn tin = acc_tree_load(p.parents, p.tokens, nullptr, nullptr, p.n_nodes, b, n_max);
+  const int bad = acc_tree_build(sh.tr, tin, n_max, V);
   int best = 0;
   int bonus = -1;
   if (bad == 0) {  // uniform across the cluster: every CTA computed the same flag
