@@ -10,4 +10,5 @@ from .treeverify_oracle import (tree_build_mask, tree_verify_attn, tree_accept_g
                                 tree_is_valid, draft_entropy, branch_width, top_tokens,
                                 log_softmax_at, tree_expand_level, tree_build_dynamic,
                                 kv_prune_pages, dequantize_q4, tree_verify_attn_q4,
-                                f64_to_bf16_bits_via_f32, quantize_q4)
+                                f64_to_bf16_bits_via_f32, quantize_q4, q3_code_values, q3_pack,
+                                dequantize_q3, tree_verify_attn_q3, quantize_q3)

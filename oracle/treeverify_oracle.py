@@ -793,3 +793,95 @@ def quantize_q4(x_bits):
     params[..., 0::2] = scale
     params[..., 1::2] = zero
     return codes, params
+
+
+# --------------------------------------------------------------------------
+# low-bit KV: verify attention over a 3-bit cache
+# --------------------------------------------------------------------------
+def q3_code_values(codes, D):
+    """The integer codes 0..7 of a 3-bit row layout (uint8 [..., 3 * D / 8]),
+    as int64 [..., D].  Bytes [0, D/4) hold the low two bits of every code,
+    four per byte: byte j holds dims 4j .. 4j+3, dim 4j+i in bits 2i, 2i+1.
+    Bytes [D/4, 3D/8) hold the third bit of every code, eight per byte: byte
+    D/4 + j holds dims 8j .. 8j+7, dim 8j+i in bit i."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    lo = codes[..., : D // 4].astype(np.int64)
+    hi = codes[..., D // 4: 3 * D // 8].astype(np.int64)
+    c = np.empty(codes.shape[:-1] + (D,), dtype=np.int64)
+    for i in range(4):
+        c[..., i::4] = (lo >> (2 * i)) & 3
+    for i in range(8):
+        c[..., i::8] |= ((hi >> i) & 1) << 2
+    return c
+
+
+def q3_pack(c):
+    """Inverse of ``q3_code_values``: int codes 0..7 [..., D] -> uint8 [..., 3D/8]."""
+    c = np.asarray(c, dtype=np.int64)
+    D = c.shape[-1]
+    out = np.zeros(c.shape[:-1] + (3 * D // 8,), dtype=np.int64)
+    for i in range(4):
+        out[..., : D // 4] |= (c[..., i::4] & 3) << (2 * i)
+    for i in range(8):
+        out[..., D // 4:] |= ((c[..., i::8] >> 2) & 1) << i
+    return out.astype(np.uint8)
+
+
+def dequantize_q3(codes, params):
+    """Decode a 3-bit KV cache to bf16 rows (troisinh.com "EAGLE - Draft head
+    ...": its further-reading list names KV-cache quantisation to INT4/INT3).
+
+    codes  uint8 [..., 3 * D / 8] in the layout of ``q3_code_values``, codes 0..7;
+    params float16 [..., 2 * D / 32]: (scale, zero) of each group of 32 dims.
+    Value of dim d: bf16(fp32(code * scale + zero)) for the group of d (the
+    product and sum exact in fp64, one rounding to fp32, one to bf16), as for
+    the 4-bit format.  Returns bf16 bit patterns uint16 [..., D].
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    D = codes.shape[-1] * 8 // 3
+    c = q3_code_values(codes, D).astype(np.float64)
+    prm = np.asarray(params, dtype=np.float16).astype(np.float64)
+    n_groups = D // Q4_GROUP
+    scale = np.repeat(prm[..., 0:2 * n_groups:2], Q4_GROUP, axis=-1)
+    zero = np.repeat(prm[..., 1:2 * n_groups:2], Q4_GROUP, axis=-1)
+    return f64_to_bf16_bits_via_f32(c * scale + zero)
+
+
+def tree_verify_attn_q3(q_bits, k_codes, k_params, v_codes, v_params, page_table, prefix_len, n_nodes,
+                        parents, scale, page_size=16, rows=None):
+    """Tree-masked attention over a 3-bit paged cache: the cache decoded by
+    ``dequantize_q3`` (caches [num_pages, Hkv, page_size, 3 * D / 8] codes and
+    [num_pages, Hkv, page_size, 2 * D / 32] params), then ``tree_verify_attn``."""
+    return tree_verify_attn(q_bits, dequantize_q3(k_codes, k_params), dequantize_q3(v_codes, v_params),
+                            page_table, prefix_len, n_nodes, parents, scale, page_size=page_size, rows=rows)
+
+
+def quantize_q3(x_bits):
+    """Encode bf16 rows (uint16 bits [..., D]) in the 3-bit format that
+    ``dequantize_q3`` decodes.  Per row and group of 32 dims, in fp32 IEEE
+    arithmetic (round to nearest even at each step) with fp16 parameters, as
+    the 4-bit encoder with 8 levels:
+        zero  = fp16(min x)
+        scale = fp16((max x - min x) / 7)
+        inv   = fp32(1 / scale)
+        code  = clamp(rint((x - zero) * inv), 0, 7)   (0 when scale is 0)
+    Returns (codes uint8 [..., 3 * D / 8], params float16 [..., 2 * D / 32])."""
+    x = bf16_to_f64(x_bits).astype(np.float32)
+    D = x.shape[-1]
+    g = D // Q4_GROUP
+    xg = x.reshape(x.shape[:-1] + (g, Q4_GROUP))
+    mn = xg.min(axis=-1)
+    mx = xg.max(axis=-1)
+    zero = mn.astype(np.float16)
+    scale = ((mx - mn) / np.float32(7.0)).astype(np.float16)
+    z32 = zero.astype(np.float32)[..., None]
+    s32 = scale.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        inv = np.float32(1.0) / s32
+        q = np.rint((xg - z32) * inv)
+    q = np.where(s32 > 0, q, 0.0)
+    q = np.clip(q, 0, 7).astype(np.int64).reshape(x.shape)
+    params = np.empty(x.shape[:-1] + (2 * g,), dtype=np.float16)
+    params[..., 0::2] = scale
+    params[..., 1::2] = zero
+    return q3_pack(q), params
