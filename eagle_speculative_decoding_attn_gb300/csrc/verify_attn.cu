@@ -50,17 +50,18 @@ namespace tv {
 namespace attn {
 
 // dynamic shared-memory layout (1024-byte aligned base)
-template <int D, bool kQ4>
+template <int D, int kLB>
 struct Smem {
+  static constexpr bool kQ4 = kLB != 0;                   // a low-bit (4- or 3-bit) cache
   static constexpr int kDBlocks = D / 64;                 // 128-byte swizzle atoms along D
   static constexpr int kQTile = kBM * D * 2;
   static constexpr int kKVTile = kBN * D * 2;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kNT * kQTile;
   static constexpr int kV = kK + kStages * kKVTile;
-  // 4-bit cache: for K and for V two code slots of half a tile each, a slot
-  // holding the codes [64 keys][D/2] followed by the params [64 keys][D/16] fp16
-  static constexpr int kCodeRow = D / 2;
+  // low-bit cache: for K and for V two code slots of half a tile each, a slot
+  // holding the codes [64 keys][D/2 or 3D/8] followed by the params [64 keys][D/16] fp16
+  static constexpr int kCodeRow = kLB == 3 ? 3 * D / 8 : D / 2;
   static constexpr int kParamRow = D / 8;
   static constexpr int kSlotParams = kHalfKeys * kCodeRow;
   static constexpr int kSlot = kHalfKeys * (kCodeRow + kParamRow);
@@ -76,14 +77,14 @@ struct Smem {
 };
 
 
-template <int D, bool kQ4>
+template <int D, int kLB>
 __device__ __forceinline__ void merge_tile(const AttnParams& p, const Item& it, int mtile, int n_rows, int r) {
   // (splits per round trip, 16-byte loads per split): about 128 registers of loads
   // and accumulators either way; half of that where the launch leaves 128 registers
   // a thread (4-bit cache)
   const int mrow0 = (it.mp * kNT + mtile) * kBM, prow0 = mtile * kBM;
   auto slot_of = [&](int sp) { return split_slot(it, sp); };
-  if constexpr (kQ4) {
+  if constexpr (kLB != 0) {
     if (it.n_splits <= 2) merge_items<D, 2, (D >= 128 ? 4 : 2), kBM>(p, it, mrow0, prow0, n_rows, r, slot_of);
     else if (it.n_splits <= 4) merge_items<D, 4, 2, kBM>(p, it, mrow0, prow0, n_rows, r, slot_of);
     else if (it.n_splits <= 6) merge_items<D, 6, 2, kBM>(p, it, mrow0, prow0, n_rows, r, slot_of);
@@ -143,10 +144,69 @@ __device__ __forceinline__ void decode_row_q4(const uint8_t* codes, const uint8_
   }
 }
 
-template <int D, bool kQ4>
-__global__ void __launch_bounds__(kQ4 ? kThreadsQ4 : kThreads, 1)
+// Decodes key row r of a 3-bit code slot into a bf16 K or V stage (the layout
+// of decode_row_q4).  The row's codes: its low two bits four per byte (byte j:
+// dims 4j .. 4j+3, dim 4j+i in bits 2i and 2i+1), then its third bits eight per
+// byte (byte D/4 + j: dims 8j .. 8j+7, dim 8j+i in bit i); per group of 32 dims
+// two 32-bit words of low bits and one of third bits.  Four codes at a time are
+// spread into the bytes of a word: the low-bit pairs by shifts of 6, 12 and 18
+// (each lands at the bottom of its own byte), the third bits by a multiply with
+// 1 + 2^7 + 2^14 + 2^21 (bit k lands at bit 8k); then as in the 4-bit decode.
+template <int D>
+__device__ __forceinline__ void decode_row_q3(const uint8_t* codes, const uint8_t* params, uint8_t* stage, int r) {
+  constexpr int kGroups = D / kQ4Group;
+  uint32_t pw[kGroups];  // (scale, zero) of each group, scale in the low half
+  if constexpr (kGroups == 4) {
+    const uint4 t = *reinterpret_cast<const uint4*>(params);
+    pw[0] = t.x; pw[1] = t.y; pw[2] = t.z; pw[3] = t.w;
+  } else {
+    const uint2 t = *reinterpret_cast<const uint2*>(params);
+    pw[0] = t.x; pw[1] = t.y;
+  }
+  const uint2* lo2 = reinterpret_cast<const uint2*>(codes);
+  const uint32_t* hi4 = reinterpret_cast<const uint32_t*>(codes + D / 4);
+  const uint64_t neg_magic = f2_pack(-8388608.f, -8388608.f);
+#pragma unroll
+  for (int gi = 0; gi < kGroups; ++gi) {
+    const uint2 l = lo2[gi];
+    const uint32_t h = hi4[gi];
+    const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&pw[gi]));
+    const uint64_t s2 = f2_pack(sz.x, sz.x), z2 = f2_pack(sz.y, sz.y);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // dims 8q .. 8q + 7 of the group: one 16-byte chunk
+      const uint32_t l16 = (q < 2 ? l.x : l.y) >> (16 * (q & 1));
+      const uint32_t h8 = h >> (8 * q);
+      uint32_t cw[2];  // codes of dims 8q .. 8q+3 and 8q+4 .. 8q+7, one per byte
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t x = (l16 >> (8 * u)) & 0xFFu;
+        const uint32_t lo = (x | (x << 6) | (x << 12) | (x << 18)) & 0x03030303u;
+        const uint32_t hb = (((h8 >> (4 * u)) & 0xFu) * 0x00204081u) & 0x01010101u;
+        cw[u] = lo | (hb << 2);
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t w = cw[j >> 1];
+        const float ce = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u + 2 * (j & 1)));
+        const float co = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u + 2 * (j & 1) + 1));
+        float ve, vo;
+        f2_unpack(f2_fma(f2_add(f2_pack(ce, co), neg_magic), s2, z2), ve, vo);
+        o[j] = pack_bf16x2(ve, vo);
+      }
+      const int d0 = gi * kQ4Group + q * 8;
+      const int db = d0 / 64, ch = (d0 % 64) / 8;
+      *reinterpret_cast<uint4*>(stage + db * (kBN * 128) + r * 128 + ((ch ^ (r & 7)) << 4)) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+template <int D, int kLB>
+__global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
     verify_attn_kernel(const __grid_constant__ AttnParams p) {
-  using S = Smem<D, kQ4>;
+  using S = Smem<D, kLB>;
+  constexpr bool kQ4 = kLB != 0;  // a low-bit cache, decoded by warps 12-15
   constexpr int kNThreads = kQ4 ? kThreadsQ4 : kThreads;
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
@@ -513,8 +573,12 @@ __global__ void __launch_bounds__(kQ4 ? kThreadsQ4 : kThreads, 1)
           if (!ok) break;
           const int r = h * kHalfKeys + ri;  // key row of the tile
           if (r < npg * kPageSize)
-            decode_row_q4<D>(slots + h * S::kSlot + ri * S::kCodeRow,
-                             slots + h * S::kSlot + S::kSlotParams + ri * S::kParamRow, stage, r);
+          {
+            const uint8_t* crow = slots + h * S::kSlot + ri * S::kCodeRow;
+            const uint8_t* prow = slots + h * S::kSlot + S::kSlotParams + ri * S::kParamRow;
+            if constexpr (kLB == 3) decode_row_q3<D>(crow, prow, stage, r);
+            else decode_row_q4<D>(crow, prow, stage, r);
+          }
           mbar_arrive(is_k ? &bar_kce[h] : &bar_vce[h]);
         }
         if (!ok) break;
@@ -808,7 +872,7 @@ __global__ void __launch_bounds__(kQ4 ? kThreadsQ4 : kThreads, 1)
         if (ticket_sh[t] == item.n_splits - 1) {
           __threadfence();
           const int n_rows = min(kBM, N * G - (item.mp * kNT + mtile) * kBM);  // valid rows of the M tile
-          merge_tile<D, kQ4>(p, item, mtile, n_rows, r);
+          merge_tile<D, kLB>(p, item, mtile, n_rows, r);
           if (r == 0) p.ws_tickets[tick_idx] = 0;  // ready for the next call
         }
       }
@@ -875,11 +939,11 @@ static bool make_map4(CUtensorMap* m, const void* base, const uint64_t dims[4], 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool kQ4>
+template <int D, int kLB>
 static int launch(const AttnParams& ap, int grid, cudaStream_t st) {
-  using S = Smem<D, kQ4>;
-  TV_CUDA_CHECK(ensure_smem_attr((const void*)verify_attn_kernel<D, kQ4>, S::kAlloc));
-  TV_CUDA_CHECK(launch_pdl(verify_attn_kernel<D, kQ4>, dim3(grid), dim3(kQ4 ? kThreadsQ4 : kThreads),
+  using S = Smem<D, kLB>;
+  TV_CUDA_CHECK(ensure_smem_attr((const void*)verify_attn_kernel<D, kLB>, S::kAlloc));
+  TV_CUDA_CHECK(launch_pdl(verify_attn_kernel<D, kLB>, dim3(grid), dim3(kLB != 0 ? kThreadsQ4 : kThreads),
                            (size_t)S::kAlloc, st, ap));
   TV_CUDA_CHECK(cudaGetLastError());
   return TV_OK;
@@ -892,24 +956,26 @@ static int launch(const AttnParams& ap, int grid, cudaStream_t st) {
 // 256-row M-tile pairs.  Head dim 64 always runs one CTA per SM.
 static int launch_bf16(const AttnParams& ap, int D, int n_max, int grid, cudaStream_t st) {
   if (D == 128 && n_max * ap.G >= 2 * 2 * kBM && n_max * ap.G <= 8 * kBM) return launch_pair(ap, grid, st);
-  return D == 128 ? launch<128, false>(ap, grid, st) : launch<64, false>(ap, grid, st);
+  return D == 128 ? launch<128, 0>(ap, grid, st) : launch<64, 0>(ap, grid, st);
 }
 
 // Argument checks and parameter set-up shared by the entry points.
-// With q4 set, k_cache and v_cache are the code arrays and the params arrays
-// come in k_params / v_params; no tensor map is made for them.
+// With low_bits set (4 or 3), k_cache and v_cache are the code arrays and the
+// params arrays come in k_params / v_params; no tensor map is made for them.
 static int prepare(const void* q, const void* k_cache, const void* v_cache, int64_t num_pages,
                    const int32_t* page_table, int max_pages, const int32_t* prefix_len, const int32_t* n_nodes,
                    const uint64_t* anc_mask, int B, int n_max, int Hq, int Hkv, int D, int page_size, float scale,
-                   void* out, float* lse, int32_t* status, AttnParams* ap, bool q4 = false,
+                   void* out, float* lse, int32_t* status, AttnParams* ap, int low_bits = 0,
                    const void* k_params = nullptr, const void* v_params = nullptr) {
+  const bool q4 = low_bits != 0;
   TV_REQUIRE(q && k_cache && v_cache && page_table && prefix_len && n_nodes && anc_mask && out && status,
              TV_ERR_INVALID_ARG, "tv_tree_verify_attn: NULL pointer");
-  TV_REQUIRE(!q4 || (k_params && v_params), TV_ERR_INVALID_ARG, "tv_tree_verify_attn_q4: NULL params pointer");
+  TV_REQUIRE(!q4 || (k_params && v_params), TV_ERR_INVALID_ARG, "tv_tree_verify_attn_q%d: NULL params pointer",
+             low_bits);
   TV_REQUIRE(!q4 || (aligned16(k_params) && aligned16(v_params)), TV_ERR_INVALID_ARG,
-             "tv_tree_verify_attn_q4: params must be 16-byte aligned");
-  TV_REQUIRE(!q4 || B <= kMaxBatchQ4, TV_ERR_UNSUPPORTED, "tv_tree_verify_attn_q4: B = %d not in [0, %d]", B,
-             kMaxBatchQ4);
+             "tv_tree_verify_attn_q%d: params must be 16-byte aligned", low_bits);
+  TV_REQUIRE(!q4 || B <= kMaxBatchQ4, TV_ERR_UNSUPPORTED, "tv_tree_verify_attn_q%d: B = %d not in [0, %d]",
+             low_bits, B, kMaxBatchQ4);
   TV_REQUIRE(page_size == kPageSize, TV_ERR_UNSUPPORTED, "tv_tree_verify_attn: page_size %d != 16", page_size);
   TV_REQUIRE(D == 64 || D == 128, TV_ERR_UNSUPPORTED, "tv_tree_verify_attn: D = %d not in {64, 128}", D);
   TV_REQUIRE(Hq >= 1 && Hkv >= 1 && Hq % Hkv == 0, TV_ERR_UNSUPPORTED,
@@ -1009,27 +1075,54 @@ extern "C" int tv_tree_verify_attn(const void* q, const void* k_cache, const voi
   return launch_bf16(ap, D, n_max, grid, st);
 }
 
+namespace tv {
+namespace attn {
+// The low-bit entry points: argument checks, workspace, the decoding kernel.
+static int verify_attn_lowbit(int bits, const void* q, const uint8_t* k_codes, const void* k_params,
+                              const uint8_t* v_codes, const void* v_params, int64_t num_pages,
+                              const int32_t* page_table, int max_pages, const int32_t* prefix_len,
+                              const int32_t* n_nodes, const uint64_t* anc_mask, int B, int n_max, int Hq, int Hkv,
+                              int D, int page_size, float scale, void* out, float* lse, void* ws, size_t ws_bytes,
+                              int32_t* status, void* stream) {
+  clear_error();
+  AttnParams ap;
+  const int rc = prepare(q, k_codes, v_codes, num_pages, page_table, max_pages, prefix_len, n_nodes, anc_mask, B,
+                         n_max, Hq, Hkv, D, page_size, scale, out, lse, status, &ap, bits, k_params, v_params);
+  if (rc != TV_OK) return rc;
+  if (B == 0) return TV_OK;
+  const int grid = current_sm_count();
+  const WsLayout wl = ws_layout(B, n_max, Hq, Hkv, D, grid);
+  TV_REQUIRE(ws != nullptr && ws_bytes >= wl.total, TV_ERR_WORKSPACE,
+             "tv_tree_verify_attn_q%d: workspace %zu bytes < %zu", bits, ws_bytes, wl.total);
+  TV_REQUIRE(aligned16(ws), TV_ERR_INVALID_ARG, "tv_tree_verify_attn_q%d: workspace must be 16-byte aligned", bits);
+  bind_workspace(&ap, wl, static_cast<uint8_t*>(ws));
+  cudaStream_t st = as_stream(stream);
+  if (bits == 3) return D == 128 ? launch<128, 3>(ap, grid, st) : launch<64, 3>(ap, grid, st);
+  return D == 128 ? launch<128, 4>(ap, grid, st) : launch<64, 4>(ap, grid, st);
+}
+}  // namespace attn
+}  // namespace tv
+
 extern "C" int tv_tree_verify_attn_q4(const void* q, const uint8_t* k_codes, const void* k_params,
                                       const uint8_t* v_codes, const void* v_params, int64_t num_pages,
                                       const int32_t* page_table, int max_pages, const int32_t* prefix_len,
                                       const int32_t* n_nodes, const uint64_t* anc_mask, int B, int n_max, int Hq,
                                       int Hkv, int D, int page_size, float scale, void* out, float* lse, void* ws,
                                       size_t ws_bytes, int32_t* status, void* stream) {
-  using namespace tv::attn;
-  tv::clear_error();
-  AttnParams ap;
-  const int rc = prepare(q, k_codes, v_codes, num_pages, page_table, max_pages, prefix_len, n_nodes, anc_mask, B,
-                         n_max, Hq, Hkv, D, page_size, scale, out, lse, status, &ap, true, k_params, v_params);
-  if (rc != TV_OK) return rc;
-  if (B == 0) return TV_OK;
-  const int grid = tv::current_sm_count();
-  const WsLayout wl = ws_layout(B, n_max, Hq, Hkv, D, grid);
-  TV_REQUIRE(ws != nullptr && ws_bytes >= wl.total, TV_ERR_WORKSPACE,
-             "tv_tree_verify_attn_q4: workspace %zu bytes < %zu", ws_bytes, wl.total);
-  TV_REQUIRE(tv::aligned16(ws), TV_ERR_INVALID_ARG, "tv_tree_verify_attn_q4: workspace must be 16-byte aligned");
-  bind_workspace(&ap, wl, static_cast<uint8_t*>(ws));
-  cudaStream_t st = tv::as_stream(stream);
-  return D == 128 ? launch<128, true>(ap, grid, st) : launch<64, true>(ap, grid, st);
+  return tv::attn::verify_attn_lowbit(4, q, k_codes, k_params, v_codes, v_params, num_pages, page_table, max_pages,
+                                      prefix_len, n_nodes, anc_mask, B, n_max, Hq, Hkv, D, page_size, scale, out,
+                                      lse, ws, ws_bytes, status, stream);
+}
+
+extern "C" int tv_tree_verify_attn_q3(const void* q, const uint8_t* k_codes, const void* k_params,
+                                      const uint8_t* v_codes, const void* v_params, int64_t num_pages,
+                                      const int32_t* page_table, int max_pages, const int32_t* prefix_len,
+                                      const int32_t* n_nodes, const uint64_t* anc_mask, int B, int n_max, int Hq,
+                                      int Hkv, int D, int page_size, float scale, void* out, float* lse, void* ws,
+                                      size_t ws_bytes, int32_t* status, void* stream) {
+  return tv::attn::verify_attn_lowbit(3, q, k_codes, k_params, v_codes, v_params, num_pages, page_table, max_pages,
+                                      prefix_len, n_nodes, anc_mask, B, n_max, Hq, Hkv, D, page_size, scale, out,
+                                      lse, ws, ws_bytes, status, stream);
 }
 
 // ---------------------------------------------------------------- built-in scratch variant

@@ -55,6 +55,9 @@ _SIGNATURES = {
     "tv_kv_quantize_q4": (_I, [_P, _I64, _I, _P, _P, _P]),
     "tv_tree_verify_attn_q4": (_I, [_P, _P, _P, _P, _P, _I64, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
                                     _P, _P, _SZ, _P, _P]),
+    "tv_kv_quantize_q3": (_I, [_P, _I64, _I, _P, _P, _P]),
+    "tv_tree_verify_attn_q3": (_I, [_P, _P, _P, _P, _P, _I64, _P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
+                                    _P, _P, _SZ, _P, _P]),
     "tv_selftest_wait_timeout": (_I, [_P, _P]),
     "tv_last_error": (ctypes.c_char_p, []),
     "tv_version": (ctypes.c_char_p, []),
@@ -298,20 +301,65 @@ def kv_prune_pages(page_table: torch.Tensor, refcount: torch.Tensor, prefix_len:
     return free_list, free_count
 
 
-def kv_quantize_q4(x: torch.Tensor, *, codes=None, params=None):
-    """Encode bf16 rows [..., D] in the 4-bit cache format.  Returns (codes
-    uint8 [..., D/2], params float16 [..., 2*D/32])."""
+def _code_row(bits: int, D: int) -> int:
+    """Bytes of one row's codes in the 4-bit (D/2) or 3-bit (3D/8) format."""
+    return D // 2 if bits == 4 else 3 * D // 8
+
+
+def _kv_quantize(bits: int, x: torch.Tensor, codes, params):
+    name = f"tv_kv_quantize_q{bits}"
     if x.dtype != torch.bfloat16:
         raise TreeVerifyError(f"x: expected torch.bfloat16, got {x.dtype}")
     D = x.shape[-1]
     rows = x.numel() // D
     if codes is None:
-        codes = torch.empty(x.shape[:-1] + (D // 2,), dtype=torch.uint8, device=x.device)
+        codes = torch.empty(x.shape[:-1] + (_code_row(bits, D),), dtype=torch.uint8, device=x.device)
     if params is None:
         params = torch.empty(x.shape[:-1] + (2 * D // 32,), dtype=torch.float16, device=x.device)
-    rc = load_library().tv_kv_quantize_q4(_ptr(x), rows, D, _ptr(codes), _ptr(params), _stream(x.device))
-    _check(rc, "tv_kv_quantize_q4")
+    rc = getattr(load_library(), name)(_ptr(x), rows, D, _ptr(codes), _ptr(params), _stream(x.device))
+    _check(rc, name)
     return codes, params
+
+
+def kv_quantize_q4(x: torch.Tensor, *, codes=None, params=None):
+    """Encode bf16 rows [..., D] in the 4-bit cache format.  Returns (codes
+    uint8 [..., D/2], params float16 [..., 2*D/32])."""
+    return _kv_quantize(4, x, codes, params)
+
+
+def kv_quantize_q3(x: torch.Tensor, *, codes=None, params=None):
+    """Encode bf16 rows [..., D] in the 3-bit cache format.  Returns (codes
+    uint8 [..., 3*D/8], params float16 [..., 2*D/32])."""
+    return _kv_quantize(3, x, codes, params)
+
+
+def _verify_attn_lowbit(bits, q, k_codes, k_params, v_codes, v_params, page_table, prefix_len, n_nodes, anc_mask,
+                        scale, status, out, lse, want_lse, workspace):
+    name = f"tv_tree_verify_attn_q{bits}"
+    B, n_max, Hq, D = q.shape
+    num_pages, Hkv, P, Dc = k_codes.shape
+    dev = q.device
+    if q.dtype != torch.bfloat16:
+        raise TreeVerifyError("q must be bfloat16")
+    if Dc != _code_row(bits, D) or tuple(v_codes.shape) != tuple(k_codes.shape):
+        raise TreeVerifyError("k_codes / v_codes shapes do not match q")
+    for t, nm in ((k_codes, "k_codes"), (v_codes, "v_codes")):
+        _expect(t, torch.uint8, (num_pages, Hkv, P, Dc), nm)
+    for t, nm in ((k_params, "k_params"), (v_params, "v_params")):
+        _expect(t, torch.float16, (num_pages, Hkv, P, 2 * D // 32), nm)
+    _expect(page_table, torch.int32, page_table.shape, "page_table")
+    _expect(anc_mask, torch.int64, (B, n_max), "anc_mask")
+    out = torch.empty_like(q) if out is None else out
+    if lse is None and want_lse:
+        lse = torch.empty((B, n_max, Hq), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = new_attn_workspace(B, n_max, Hq, Hkv, D, dev)
+    rc = getattr(load_library(), name)(
+        _ptr(q), _ptr(k_codes), _ptr(k_params), _ptr(v_codes), _ptr(v_params), num_pages, _ptr(page_table),
+        page_table.shape[1], _ptr(prefix_len), _ptr(n_nodes), _ptr(anc_mask), B, n_max, Hq, Hkv, D, P,
+        float(scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev))
+    _check(rc, name)
+    return out, lse
 
 
 def tree_verify_attn_q4(q: torch.Tensor, k_codes: torch.Tensor, k_params: torch.Tensor, v_codes: torch.Tensor,
@@ -322,30 +370,20 @@ def tree_verify_attn_q4(q: torch.Tensor, k_codes: torch.Tensor, k_params: torch.
     [num_pages, Hkv, 16, D/2] and params float16 [num_pages, Hkv, 16, 2*D/32]
     for K and for V (the format of ``kv_quantize_q4``); everything else as
     ``tree_verify_attn``, whose workspace it shares."""
-    B, n_max, Hq, D = q.shape
-    num_pages, Hkv, P, Dh = k_codes.shape
-    dev = q.device
-    if q.dtype != torch.bfloat16:
-        raise TreeVerifyError("q must be bfloat16")
-    if Dh * 2 != D or tuple(v_codes.shape) != tuple(k_codes.shape):
-        raise TreeVerifyError("k_codes / v_codes shapes do not match q")
-    for t, nm in ((k_codes, "k_codes"), (v_codes, "v_codes")):
-        _expect(t, torch.uint8, (num_pages, Hkv, P, D // 2), nm)
-    for t, nm in ((k_params, "k_params"), (v_params, "v_params")):
-        _expect(t, torch.float16, (num_pages, Hkv, P, 2 * D // 32), nm)
-    _expect(page_table, torch.int32, page_table.shape, "page_table")
-    _expect(anc_mask, torch.int64, (B, n_max), "anc_mask")
-    out = torch.empty_like(q) if out is None else out
-    if lse is None and want_lse:
-        lse = torch.empty((B, n_max, Hq), dtype=torch.float32, device=dev)
-    if workspace is None:
-        workspace = new_attn_workspace(B, n_max, Hq, Hkv, D, dev)
-    rc = load_library().tv_tree_verify_attn_q4(
-        _ptr(q), _ptr(k_codes), _ptr(k_params), _ptr(v_codes), _ptr(v_params), num_pages, _ptr(page_table),
-        page_table.shape[1], _ptr(prefix_len), _ptr(n_nodes), _ptr(anc_mask), B, n_max, Hq, Hkv, D, P,
-        float(scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(status), _stream(dev))
-    _check(rc, "tv_tree_verify_attn_q4")
-    return out, lse
+    return _verify_attn_lowbit(4, q, k_codes, k_params, v_codes, v_params, page_table, prefix_len, n_nodes,
+                               anc_mask, scale, status, out, lse, want_lse, workspace)
+
+
+def tree_verify_attn_q3(q: torch.Tensor, k_codes: torch.Tensor, k_params: torch.Tensor, v_codes: torch.Tensor,
+                        v_params: torch.Tensor, page_table: torch.Tensor, prefix_len: torch.Tensor,
+                        n_nodes: torch.Tensor, anc_mask: torch.Tensor, scale: float, status: torch.Tensor, *,
+                        out=None, lse=None, want_lse=True, workspace=None):
+    """Tree-masked paged attention over a 3-bit cache: codes uint8
+    [num_pages, Hkv, 16, 3*D/8] and params float16 [num_pages, Hkv, 16, 2*D/32]
+    for K and for V (the format of ``kv_quantize_q3``); everything else as
+    ``tree_verify_attn``, whose workspace it shares."""
+    return _verify_attn_lowbit(3, q, k_codes, k_params, v_codes, v_params, page_table, prefix_len, n_nodes,
+                               anc_mask, scale, status, out, lse, want_lse, workspace)
 
 
 def version() -> str:

@@ -529,3 +529,19 @@ def make_q4_cache(rng: np.random.Generator, num_pages: int, Hkv: int, D: int):
     params[..., 0::2] = s.astype(np.float16)
     params[..., 1::2] = z.astype(np.float16)
     return codes, params
+
+
+def make_q3_cache(rng: np.random.Generator, num_pages: int, Hkv: int, D: int):
+    """A random 3-bit paged cache: codes uint8 [num_pages, Hkv, 16, 3*D/8]
+    (every bit uniform, so codes 0..7 are uniform) and params float16
+    [num_pages, Hkv, 16, 2 * D / 32]: per row and group of 32 dims a scale
+    ~ U(0.25, 0.60) and a zero ~ -3.5 * scale + N(0, 0.05), so decoded values
+    spread like N(0, 1) around 0."""
+    codes = rng.integers(0, 256, size=(num_pages, Hkv, PAGE_SIZE, 3 * D // 8), dtype=np.uint8)
+    g = D // Q4_GROUP
+    s = rng.uniform(0.25, 0.60, size=(num_pages, Hkv, PAGE_SIZE, g))
+    z = -3.5 * s + 0.05 * rng.standard_normal(size=s.shape)
+    params = np.empty((num_pages, Hkv, PAGE_SIZE, 2 * g), dtype=np.float16)
+    params[..., 0::2] = s.astype(np.float16)
+    params[..., 1::2] = z.astype(np.float16)
+    return codes, params

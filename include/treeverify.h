@@ -410,6 +410,46 @@ int tv_tree_verify_attn_q4(const void* q, const uint8_t* k_codes, const void* k_
                            void* ws, size_t ws_bytes, int32_t* status, void* stream);
 
 /*
+ * tv_kv_quantize_q3 — encode bf16 KV rows in a 3-bit cache format
+ * (troisinh.com "EAGLE - Draft head ...", further reading: KV-cache
+ * quantisation to INT4/INT3).  Per row and group of 32 dims: scale and zero
+ * in fp16 as for tv_kv_quantize_q4, codes 0..7.  A row's codes take 3 * D / 8
+ * bytes: first the low two bits of every code, four per byte (byte j: dims
+ * 4j .. 4j+3, dim 4j+i in bits 2i and 2i+1), then the third bits, eight per
+ * byte (byte D/4 + j: dims 8j .. 8j+7, dim 8j+i in bit i).  A value decodes to
+ * bf16(fp32(code * scale + zero)).  Encoding, in fp32 with round-to-nearest-
+ * even at each step: zero = fp16(min x), scale = fp16((max x - min x) / 7),
+ * inv = fp32(1 / scale), code = clamp(rint((x - zero) * inv), 0, 7), or 0 when
+ * scale is 0.  Inputs must be finite.
+ *
+ *  x       bf16 [rows, D] (any row layout), 16-byte aligned
+ *  D       a multiple of 32, at most 1024
+ *  codes   uint8 [rows, 3 * D / 8] out, 4-byte aligned
+ *  params  fp16 [rows, 2 * D / 32] out: (scale, zero) per group, 4-byte aligned
+ */
+int tv_kv_quantize_q3(const void* x, int64_t rows, int D, uint8_t* codes, void* params, void* stream);
+
+/*
+ * tv_tree_verify_attn_q3 — tv_tree_verify_attn over a paged KV cache held in
+ * the 3-bit format of tv_kv_quantize_q3: the result is that of
+ * tv_tree_verify_attn on the decoded cache (every K and V value first decoded
+ * to bf16(fp32(code * scale + zero))); the kernel decodes each page in shared
+ * memory as it streams, reading the cache at about 0.25 (D = 128) of the bf16
+ * bytes.
+ *
+ *  q          bf16 [B, n_max, Hq, D]                    (16-byte aligned)
+ *  k_codes    uint8 [num_pages, Hkv, 16, 3 * D / 8]     (16-byte aligned)
+ *  k_params   fp16  [num_pages, Hkv, 16, 2 * D / 32]    (16-byte aligned)
+ *  v_codes, v_params  the same for V
+ *  everything else as for tv_tree_verify_attn_q4.
+ */
+int tv_tree_verify_attn_q3(const void* q, const uint8_t* k_codes, const void* k_params, const uint8_t* v_codes,
+                           const void* v_params, int64_t num_pages, const int32_t* page_table, int max_pages,
+                           const int32_t* prefix_len, const int32_t* n_nodes, const uint64_t* anc_mask, int B,
+                           int n_max, int Hq, int Hkv, int D, int page_size, float scale, void* out, float* lse,
+                           void* ws, size_t ws_bytes, int32_t* status, void* stream);
+
+/*
  * tv_selftest_wait_timeout — self-test of the bounded waits every kernel uses
  * (no counterpart in the pages).  One CTA waits on an mbarrier that nothing
  * ever completes; after the wait limit (1 s) it ORs TV_DEV_TIMEOUT into
