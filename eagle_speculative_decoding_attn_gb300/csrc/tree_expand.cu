@@ -29,6 +29,7 @@
 // arrival are a serial latency chain that two resident CTAs did not hide.)
 #include <cfloat>
 #include <climits>
+#include <cmath>
 
 #include "tv_common.cuh"
 
@@ -58,20 +59,22 @@ struct ExpandParams {
   float* entropy;
   int32_t* width;
   int n_max, V, top_k, max_new, budget, max_frontier, n_slices;
+  float width_ln[kExpTop];  // width_ln[j] = ln(j + 1/2), rounded once from double: H at or above it gives > j children
   ExpPart* part;      // [B][max_frontier][n_slices]
   int32_t* tickets;   // [B] arrivals of this call (zero between calls)
   int32_t* status;
 };
 
 struct ExpShared {
-  float red_m[kExpWarps], red_s[kExpWarps], red_t[kExpWarps], wmax[kExpWarps];
+  int wmax_k[kExpWarps];  // order keys of the warps' largest logits
+  int wcnt[kExpWarps];    // candidates of each warp
+  float red_s[kExpWarps], red_t[kExpWarps];
   float wtop_v[kExpWarps][kExpTop];
   int wtop_i[kExpWarps][kExpTop];
   float top_v[kExpTop];
   int top_i[kExpTop];
   float cand_v[kSliceCand];
   int cand_i[kSliceCand];
-  int cand_n;
   int last;
   // merge of a request
   float row_c[kMaxNodes][kExpTop];
@@ -179,78 +182,102 @@ __device__ __forceinline__ void warp_mst(float& m, float& s, float& t) {
 // first; entries past hi are -inf.
 __device__ __forceinline__ int slice_j(int lo, int u, int c) { return lo + 4 * (u * kExpThreads + threadIdx.x) + c; }
 
-// Reduce one slice (x in registers) to its part and store it at dst (thread 0
-// writes it; it publishes the part with a fence before arriving).
-__device__ __forceinline__ void slice_reduce(ExpShared& sh, const float (&x)[kExpPerThread], bool work, int lo,
-                                             int hi, ExpPart* dst) {
+// Order key of a float: larger floats have larger (signed) keys.
+__device__ __forceinline__ int f2key(float f) {
+  const int i = __float_as_int(f);
+  return i ^ ((i >> 31) & 0x7fffffff);
+}
+__device__ __forceinline__ float key2f(int k) { return __int_as_float(k ^ ((k >> 31) & 0x7fffffff)); }
+
+// Sum over the warp, in every lane.
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Reduce one slice (x in registers: the row's logits lo .. hi - 1, at least
+// one) to its part: M = the slice's max, sum e^(x-M), sum e^(x-M)(x-M) and its
+// 8 largest logits with their token ids; thread 0 stores it at dst (and
+// publishes it with a fence before arriving).
+//
+// Each warp's largest logit is a distinct logit, so with 8 warps the slice's 8
+// best are all >= T, the smallest warp maximum: only logits >= T are
+// candidates.  Every thread reads M and T from the warps' maxima; the
+// candidates are placed by a scan of their counts (no atomics) and ranked
+// against each other (larger logit, then lower token id first).
+__device__ __forceinline__ void slice_reduce(ExpShared& sh, const float (&x)[kExpPerThread], const float* row,
+                                             int lo, int hi, ExpPart* dst) {
+  static_assert(kExpWarps == kExpTop, "the threshold is the smallest of 8 warp maxima");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float m = -INFINITY, s = 0.f, t = 0.f;
-  if (work) {
-    // four independent chains for the maximum and the two sums
-    float m4[4] = {x[0], x[1], x[2], x[3]};
+  float m4[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-    for (int k = 4; k < kExpPerThread; ++k) m4[k & 3] = fmaxf(m4[k & 3], x[k]);
-    m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-    float s4[4] = {0.f, 0.f, 0.f, 0.f}, t4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int k = 0; k < kExpPerThread; ++k) {
-      // d >= -200 keeps e * d finite: e is then 0 (also when the thread saw
-      // no logit and m = -inf, where x - m is NaN and fmaxf takes -200)
-      const float d = fmaxf(x[k] - m, -200.f);
-      const float e = ex2_approx(d * kLog2e);
-      s4[k & 3] += e;
-      t4[k & 3] = fmaf(e, d, t4[k & 3]);
-    }
-    s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-    t = (t4[0] + t4[1]) + (t4[2] + t4[3]);
-    if (s == 0.f) m = -INFINITY;
-  }
-  // Each warp's largest logit is a distinct logit, so with 8 warps the
-  // slice's 8 best are all >= tau, the smallest warp maximum: only logits
-  // >= tau are candidates (a warp without logits makes tau = -inf).  After
-  // the warp's (m, s, t) merge, m is that maximum.
-  warp_mst(m, s, t);
-  if (lane == 0) {
-    sh.red_m[warp] = m;
-    sh.red_s[warp] = s;
-    sh.red_t[warp] = t;
-    sh.wmax[warp] = m;
-  }
-  if (tid == 0) {  // the thread that reads the previous slice's list
+  for (int k = 4; k < kExpPerThread; ++k) m4[k & 3] = fmaxf(m4[k & 3], x[k]);
+  const int wk = __reduce_max_sync(0xffffffffu, f2key(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]))));
+  if (lane == 0) sh.wmax_k[warp] = wk;
+  __syncthreads();
+  if (tid == 0) {  // after the barrier: the previous slice's readers of the list are done
 #pragma unroll
     for (int k = 0; k < kExpTop; ++k) {
       sh.top_v[k] = -INFINITY;
       sh.top_i[k] = INT_MAX;
     }
   }
-  __syncthreads();
-  if (warp == 0) {  // the slice's (m, s, t)
-    m = lane < kExpWarps ? sh.red_m[lane] : -INFINITY;
-    s = lane < kExpWarps ? sh.red_s[lane] : 0.f;
-    t = lane < kExpWarps ? sh.red_t[lane] : 0.f;
-    warp_mst(m, s, t);
+  int kmax = INT_MIN, kmin = INT_MAX;
+#pragma unroll
+  for (int w = 0; w < kExpWarps; ++w) {
+    const int k = sh.wmax_k[w];
+    kmax = max(kmax, k);
+    kmin = min(kmin, k);
   }
-  float tau = INFINITY;
+  const float M = key2f(kmax), T = key2f(kmin);
+  // sums against M in base 2 (d >= -288 keeps e * d finite: e is then 0), and
+  // the thread's candidates
+  const float ml2 = M * kLog2e;
+  float s4[4] = {0.f, 0.f, 0.f, 0.f}, t4[4] = {0.f, 0.f, 0.f, 0.f};
+  int cnt = 0;
 #pragma unroll
-  for (int w = 0; w < kExpWarps; ++w) tau = fminf(tau, sh.wmax[w]);
-  if (work) {
+  for (int k = 0; k < kExpPerThread; ++k) {
+    const float d = fmaxf(fmaf(x[k], kLog2e, -ml2), -288.f);
+    const float e = ex2_approx(d);
+    s4[k & 3] += e;
+    t4[k & 3] = fmaf(e, d, t4[k & 3]);
+    cnt += x[k] >= T && slice_j(lo, k >> 2, k & 3) < hi;
+  }
+  const float s_w = warp_sum((s4[0] + s4[1]) + (s4[2] + s4[3]));
+  const float t_w = warp_sum((t4[0] + t4[1]) + (t4[2] + t4[3]));
+  int incl = cnt;  // inclusive scan of the counts over the warp
 #pragma unroll
-    for (int u = 0; u < kExpPerThread / 4; ++u)
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) {
+    sh.red_s[warp] = s_w;
+    sh.red_t[warp] = t_w;
+    sh.wcnt[warp] = incl;
+  }
+  __syncthreads();
+  int pos = incl - cnt, nc = 0;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int j = slice_j(lo, u, c);
-        if (j < hi && x[4 * u + c] >= tau) {
-          const int slot = atomicAdd(&sh.cand_n, 1);
-          if (slot < kSliceCand) {
-            sh.cand_v[slot] = x[4 * u + c];
-            sh.cand_i[slot] = j;
-          }
+  for (int w = 0; w < kExpWarps; ++w) {
+    const int c = sh.wcnt[w];
+    pos += w < warp ? c : 0;
+    nc += c;
+  }
+  if (nc <= kSliceCand) {
+    if (cnt > 0) {
+#pragma unroll
+      for (int k = 0; k < kExpPerThread; ++k) {
+        const int j = slice_j(lo, k >> 2, k & 3);
+        if (x[k] >= T && j < hi) {
+          sh.cand_v[pos] = x[k];
+          sh.cand_i[pos] = j;
+          ++pos;
         }
       }
-  }
-  __syncthreads();
-  const int nc = sh.cand_n;
-  if (nc <= kSliceCand) {
+    }
+    __syncthreads();
     // a candidate's rank among the candidates; ranks 0..7 are the slice's 8 best
     if (tid < nc) {
       const float v = sh.cand_v[tid];
@@ -264,19 +291,18 @@ __device__ __forceinline__ void slice_reduce(ExpShared& sh, const float (&x)[kEx
       }
     }
   } else {
-    // many logits equal to tau: exact per-thread lists instead
+    // many logits equal to T: exact per-thread lists instead, over the slice
+    // read again (rare; the registers of x are free by now)
     float tv_[kExpTop], ov[kExpTop];
     int ti_[kExpTop], oi[kExpTop];
     top_clear(tv_, ti_);
-    if (work) {
+#pragma unroll 1
+    for (int u = 0; u < kExpPerThread / 4; ++u)
 #pragma unroll
-      for (int u = 0; u < kExpPerThread / 4; ++u)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int j = slice_j(lo, u, c);
-          if (j < hi) top_insert(tv_, ti_, x[4 * u + c], j);
-        }
-    }
+      for (int c = 0; c < 4; ++c) {
+        const int j = slice_j(lo, u, c);
+        if (j < hi) top_insert(tv_, ti_, __ldcg(row + j), j);
+      }
     warp_top8(tv_, ti_, ov, oi);
     if (lane == 0) {
 #pragma unroll
@@ -304,9 +330,11 @@ __device__ __forceinline__ void slice_reduce(ExpShared& sh, const float (&x)[kEx
   }
   __syncthreads();
   if (warp == 0) {
+    const float s = warp_sum(lane < kExpWarps ? sh.red_s[lane] : 0.f);
+    const float t = warp_sum(lane < kExpWarps ? sh.red_t[lane] : 0.f) * 0.69314718055994531f;  // base 2 -> e
     if (lane == 0) {
       ExpPart r;
-      r.m = m;
+      r.m = M;
       r.s = s;
       r.t = t;
       r.pad = 0.f;
@@ -317,8 +345,6 @@ __device__ __forceinline__ void slice_reduce(ExpShared& sh, const float (&x)[kEx
       }
       *dst = r;
     }
-  } else if (tid == 32) {
-    sh.cand_n = 0;  // every thread has read it; the next slice appends after its first barrier
   }
 }
 
@@ -344,55 +370,85 @@ __device__ int request_merge(ExpShared& sh, const ExpandParams& p, int b, int n,
   const int n_max = p.n_max;
   float tv_[kExpTop], ov[kExpTop];
   int ti_[kExpTop], oi[kExpTop];
-  // warp w takes rows w, w + 8, ...
+  // warp w takes rows w, w + 8, ...: lanes take the row's slices
+  const bool lane_lists = p.n_slices * kExpTop <= 32;
   for (int r = warp; r < F; r += kExpWarps) {
-    float m = -INFINITY, s = 0.f, t = 0.f;
-    top_clear(tv_, ti_);
     const ExpPart* src = p.part + ((int64_t)b * p.max_frontier + r) * p.n_slices;
-    for (int q = lane; q < p.n_slices; q += 32) {
-      const float4* w4 = reinterpret_cast<const float4*>(src + q);
-      float4 w[5];
+    // every load of the row first (one round trip): the sums of the lane's
+    // first slice, its list entry (one per lane when the lists fit the warp)
+    // and the node's score
+    const int ne = p.n_slices * kExpTop;
+    const bool has = lane_lists && lane < ne;
+    const ExpPart* pq = src + lane / kExpTop;
+    const float v = has ? __ldcg(pq->v + lane % kExpTop) : -INFINITY;
+    const int i = has ? __ldcg(pq->i + lane % kExpTop) : INT_MAX;
+    const float4 w0 = lane < p.n_slices ? __ldcg(reinterpret_cast<const float4*>(src + lane))
+                                        : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+    const float sf = p.scores[(int64_t)b * n_max + ls + r];
+    float m = w0.x, s = w0.y, t = w0.z;
+    for (int q = lane + 32; q < p.n_slices; q += 32) {
+      const float4 wq = __ldcg(reinterpret_cast<const float4*>(src + q));
+      mst_merge(m, s, t, wq.x, wq.y, wq.z);
+    }
+    warp_mst(m, s, t);
+    const float lz = logf(s);  // log of the normaliser, relative to m
+    const float H = lz - t / s;
+    int real;
+    if (lane_lists) {
+      // one list entry per lane, ranked against the others (entries equal in
+      // full, the padding of short lists, by lane)
+      int rank = 0;
+      for (int o = 0; o < ne; ++o) {
+        const float vo = __shfl_sync(0xffffffffu, v, o);
+        const int io = __shfl_sync(0xffffffffu, i, o);
+        rank += top_before(vo, io, v, i) || (vo == v && io == i && o < lane);
+      }
+      const bool top = has && rank < kExpTop;
+      real = __popc(__ballot_sync(0xffffffffu, top && i != INT_MAX));
+      if (top) {
+        sh.row_c[r][rank] = sf + ((v - m) - lz);
+        sh.row_tok[r][rank] = i;
+      }
+    } else {
+      top_clear(tv_, ti_);
+      for (int q = lane; q < p.n_slices; q += 32) {
+        const float4* w4 = reinterpret_cast<const float4*>(src + q);
+        float4 w[4];
 #pragma unroll
-      for (int k = 0; k < 5; ++k) w[k] = __ldcg(w4 + k);
-      mst_merge(m, s, t, w[0].x, w[0].y, w[0].z);
-      const float pv[kExpTop] = {w[1].x, w[1].y, w[1].z, w[1].w, w[2].x, w[2].y, w[2].z, w[2].w};
-      const int pi[kExpTop] = {__float_as_int(w[3].x), __float_as_int(w[3].y), __float_as_int(w[3].z),
-                               __float_as_int(w[3].w), __float_as_int(w[4].x), __float_as_int(w[4].y),
-                               __float_as_int(w[4].z), __float_as_int(w[4].w)};
-      if (q == lane) {  // the lane's first part: its sorted list as is
-#pragma unroll
-        for (int k = 0; k < kExpTop; ++k) {
-          tv_[k] = pv[k];
-          ti_[k] = pi[k];
-        }
-      } else {
+        for (int k = 0; k < 4; ++k) w[k] = __ldcg(w4 + 1 + k);
+        const float pv[kExpTop] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
+        const int pi[kExpTop] = {__float_as_int(w[2].x), __float_as_int(w[2].y), __float_as_int(w[2].z),
+                                 __float_as_int(w[2].w), __float_as_int(w[3].x), __float_as_int(w[3].y),
+                                 __float_as_int(w[3].z), __float_as_int(w[3].w)};
 #pragma unroll
         for (int k = 0; k < kExpTop; ++k)
           if (!top_insert(tv_, ti_, pv[k], pi[k])) break;  // the part's list is sorted
       }
-    }
-    warp_mst(m, s, t);
-    warp_top8(tv_, ti_, ov, oi);
-    if (lane == 0) {
-      const int f = ls + r;
-      const float lz = logf(s);  // log of the normaliser, relative to m
-      const float H = lz - t / s;
-      int w = 1;
-      for (int j = 1; j < p.top_k; ++j)
-        if (H >= logf((float)j + 0.5f)) w = j + 1;
-      int real = 0;
+      warp_top8(tv_, ti_, ov, oi);
+      real = 0;
 #pragma unroll
       for (int k = 0; k < kExpTop; ++k) real += oi[k] != INT_MAX;
+      if (lane < kExpTop) {
+        float vk = ov[0];
+        int ik = oi[0];
+#pragma unroll
+        for (int k = 1; k < kExpTop; ++k)
+          if (lane == k) {
+            vk = ov[k];
+            ik = oi[k];
+          }
+        sh.row_c[r][lane] = sf + ((vk - m) - lz);
+        sh.row_tok[r][lane] = ik;
+      }
+    }
+    if (lane == 0) {
+      int w = 1;
+      for (int j = 1; j < p.top_k; ++j) w += H >= p.width_ln[j];
       w = min(w, real);
+      const int f = ls + r;
       if (p.entropy) p.entropy[(int64_t)b * n_max + f] = H;
       if (p.width) p.width[(int64_t)b * n_max + f] = w;
       sh.row_w[r] = w;
-      const float sf = p.scores[(int64_t)b * n_max + f];
-#pragma unroll
-      for (int k = 0; k < kExpTop; ++k) {
-        sh.row_c[r][k] = sf + ((ov[k] - m) - lz);
-        sh.row_tok[r][k] = oi[k];
-      }
     }
   }
   __syncthreads();
@@ -428,8 +484,7 @@ __device__ int request_merge(ExpShared& sh, const ExpandParams& p, int b, int n,
   const int keep = min(min(p.max_new, p.budget - n), C);
   // rank of each candidate by score (equal scores: earlier in (row, rank)
   // order first); the best `keep` are appended in (row, rank) order
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h * kExpThreads < C; ++h) {  // C is the same in every thread
     const int d = h * kExpThreads + tid;
     bool sel = false;
     if (d < C) {
@@ -470,19 +525,19 @@ __global__ void __launch_bounds__(kExpThreads, 4) tree_expand_kernel(const Expan
   const int tid = threadIdx.x;
   const int n_max = p.n_max, V = p.V;
   griddep_wait();
+  griddep_launch_dependents();  // the next call's CTAs may become resident and wait
   const int st = p.status[b];
   const int n = p.n_nodes[b], ls = p.level_start[b];
   const bool ok = st == 0 && n >= 1 && n <= n_max && ls >= 0 && ls <= n;
   const int F = ok ? n - ls : 0;
   const bool work = ok && y < F && F <= p.max_frontier && n < p.budget;
-  if (tid == 0) sh.cand_n = 0;
 
-  float x[kExpPerThread];
-  int lo = 0, hi = 0;
   if (work) {
+    // CTAs past the frontier only arrive: their parts are never read
+    float x[kExpPerThread];
     const float* row = p.logits + ((int64_t)b * n_max + ls + y) * V;
-    lo = sl * kExpSlice;
-    hi = min(V, lo + kExpSlice);
+    const int lo = sl * kExpSlice;
+    const int hi = min(V, lo + kExpSlice);
     if ((V & 3) == 0) {
       const float4* r4 = reinterpret_cast<const float4*>(row + lo);
 #pragma unroll
@@ -504,9 +559,8 @@ __global__ void __launch_bounds__(kExpThreads, 4) tree_expand_kernel(const Expan
           x[4 * u + c] = j < hi ? __ldcs(row + j) : -INFINITY;
         }
     }
+    slice_reduce(sh, x, row, lo, hi, p.part + ((int64_t)b * p.max_frontier + y) * p.n_slices + sl);
   }
-  ExpPart* dst = p.part + ((int64_t)b * p.max_frontier + y) * p.n_slices + sl;
-  slice_reduce(sh, x, work, lo, hi, dst);
   if (!arrive(sh, p.tickets + b, 1, p.max_frontier * p.n_slices)) return;
 
   // ---- the last CTA of request b
@@ -589,6 +643,7 @@ extern "C" int tv_tree_expand(const float* draft_logits, int32_t* parents, int32
   q.part = reinterpret_cast<tv::ExpPart*>(ws);
   q.tickets = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + (need - (size_t)B * sizeof(int32_t)));
   q.status = status;
+  for (int j = 0; j < tv::kExpTop; ++j) q.width_ln[j] = (float)std::log((double)j + 0.5);
   TV_CUDA_CHECK(tv::launch_pdl(tv::tree_expand_kernel, dim3(q.n_slices, max_frontier, B), dim3(tv::kExpThreads), 0,
                                tv::as_stream(stream), q));
   TV_CUDA_CHECK(cudaGetLastError());
