@@ -29,6 +29,8 @@
 //    reference max that a chain's first stage sets and later stages keep while
 //    their probabilities stay below 2^32 (checked on the row sum, no max pass);
 //    a stage that would pass it raises the reference and rescales O (rare).
+//    Both warpgroups take the epilogue of every item, each half of O's
+//    columns, after swapping their row states; a split's merge runs on both.
 //  * Work division: block c of every KV head runs on the clusters of lane c;
 //    within a lane the plan of verify_attn.cu splits the (request, KV head,
 //    KV tile) sequence evenly over its clusters, so the lanes read each K/V
@@ -48,6 +50,7 @@ constexpr int kPStages = 4;         // K and V ring depth (half tiles)
 constexpr int kPThreads = 384;      // 12 warps
 constexpr int kPHalfKeys = 64;      // keys of this CTA's K half tile
 constexpr uint32_t kWgArrivals = 8; // one arrival per warp of a softmax warpgroup, from both CTAs
+constexpr uint32_t kEpArrivals = 16;  // one arrival per softmax warp of both warpgroups, from both CTAs
 constexpr int kMaxLanes = 4;        // 256-row blocks per KV head (n_max * G <= 1024)
 
 struct PairSmem {
@@ -81,8 +84,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   __shared__ uint64_t bar_q, bar_qe;                        // CTA 0: both Q halves landed; Q free again
   __shared__ uint64_t bar_kf[kPStages], bar_vf[kPStages];  // CTA 0: both halves of the stage landed
   __shared__ uint64_t bar_ke[kPStages], bar_ve[kPStages];  // stage free again (MMA commit, both CTAs)
-  __shared__ uint64_t bar_s[kNT], bar_p[kNT], bar_o[kNT], bar_of[kNT], bar_wg[kNT], bar_ml;
-  __shared__ float ml_sh[2][kBM];  // chain 1's running max and sum per row, for warpgroup 0
+  __shared__ uint64_t bar_s[kNT], bar_p[kNT], bar_o[kNT], bar_of[kNT], bar_ep;
+  __shared__ float ml_sh[2][2][kBM];  // [warpgroup][running max, sum][row]: the chains' row states
+  __shared__ float amax_sh[2][kBM];   // [warpgroup][row]: largest |O| of the warpgroup's columns
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
   __shared__ int64_t plan_W;
@@ -116,10 +120,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       mbar_init(&bar_s[t], 1);
       mbar_init(&bar_p[t], kWgArrivals);
       mbar_init(&bar_o[t], 1);
-      mbar_init(&bar_of[t], kWgArrivals);
-      mbar_init(&bar_wg[t], kBM);
+      mbar_init(&bar_of[t], kEpArrivals);
     }
-    mbar_init(&bar_ml, kBM);
+    mbar_init(&bar_ep, 2 * kBM);
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -422,13 +425,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
     const uint32_t tO = tmem + lane_base + 256 + t * D;
-    const uint32_t tO1 = tmem + lane_base + 256 + D;     // chain 1's O (read by warpgroup 0)
     const float sl2 = p.scale_log2;
     ItemIter it;
     iter_init(it, pv, wk);
     Item item;
     uint32_t kv_it = 0;
-    uint32_t ph_s = 0, ph_o = 0, ph_ml = 0, ph_wg = 0;
+    uint32_t ph_s = 0, ph_ep = 0;
+    uint32_t ph_o[kNT] = {0u, 0u};  // phases of bar_o, waited on by both warpgroups
     uint32_t rag_ph = 0;  // bit s: phase of CTA 1's bar_vf[s] (partial tiles only)
     bool ok = true;
     // one arrival per warp on CTA 0's barrier (after every lane's TMEM writes)
@@ -440,10 +443,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         else mbar_arrive_remote(mapa_shared(smem_u32(bar), 0));
       }
     };
-    auto wg_sync = [&]() -> bool {
-      mbar_arrive(&bar_wg[t]);
-      const bool k = warp_wait(&bar_wg[t], ph_wg, &abort_sh);
-      ph_wg ^= 1u;
+    // both softmax warpgroups of this CTA (the epilogue is split between them)
+    auto ep_sync = [&]() -> bool {
+      mbar_arrive(&bar_ep);
+      const bool k = warp_wait(&bar_ep, ph_ep, &abort_sh);
+      ph_ep ^= 1u;
       return k;
     };
     auto row_max = [&](const uint32_t* x, int n) {
@@ -465,11 +469,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       const uint32_t rag_prev = rag_ph;
       if ((int64_t)item.tile_end * kBN > (int64_t)p.prefix_len[item.b] + p.n_nodes[item.b])
         rag_ph ^= 1u << ((kv_it + T - 1) % kPStages);
-      if (!dual && t == 1) {
-        kv_it += T;
-        continue;
-      }
-      const int n_units = dual ? (T - t + 1) / 2 : T;   // stages of this chain
+      // stages of this chain (none for warpgroup 1 on a single-stage item: it only
+      // takes its half of the epilogue)
+      const int n_units = dual ? (T - t + 1) / 2 : (t == 0 ? T : 0);
       if (tid == 128) last_b_sh = item.b;
       const int L = p.prefix_len[item.b];
       const int N = p.n_nodes[item.b];
@@ -572,31 +574,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       }
       kv_it += T;
       if (!ok) break;
-      // ---- epilogue
-      ok = warp_wait(&bar_o[t], ph_o, &abort_sh);
-      ph_o ^= 1u;
+      // ---- epilogue: warpgroup t takes columns 64t .. 64t + 63 of the combined O
+      // rows (both chains in dual mode, chain 0 otherwise)
+      ok = warp_wait(&bar_o[0], ph_o[0], &abort_sh);
+      ph_o[0] ^= 1u;
+      if (ok && dual) {
+        ok = warp_wait(&bar_o[1], ph_o[1], &abort_sh);
+        ph_o[1] ^= 1u;
+      }
       tc_fence_after();
       if (!ok) break;
-      float m_c = m_run, l_c = l_run, a0 = 1.f, a1 = 0.f;
+      // the two warpgroups swap their row states
+      ml_sh[t][0][r] = m_run;
+      ml_sh[t][1][r] = l_run;
+      ok = ep_sync();
+      if (!ok) break;
+      const float m0 = ml_sh[0][0][r], l0 = ml_sh[0][1][r];
+      float m_c = m0, l_c = l0, a0 = 1.f, a1 = 0.f;
       if (dual) {
-        if (t == 1) {
-          // hand the row state to warpgroup 0, which combines both chains
-          ml_sh[0][r] = m_run;
-          ml_sh[1][r] = l_run;
-          tc_fence_before();
-          mbar_arrive(&bar_ml);
-          continue;
-        }
-        ok = warp_wait(&bar_ml, ph_ml, &abort_sh);
-        ph_ml ^= 1u;
-        tc_fence_after();
-        if (!ok) break;
-        const float m1 = ml_sh[0][r], l1 = ml_sh[1][r];
-        m_c = fmaxf(m_run, m1);
+        const float m1 = ml_sh[1][0][r], l1 = ml_sh[1][1][r];
+        m_c = fmaxf(m0, m1);
         const float mu = (m_c == -INFINITY) ? 0.f : m_c;
-        a0 = (m_run == -INFINITY) ? 0.f : ex2_approx(m_run - mu);
+        a0 = (m0 == -INFINITY) ? 0.f : ex2_approx(m0 - mu);
         a1 = (m1 == -INFINITY) ? 0.f : ex2_approx(m1 - mu);
-        l_c = l_run * a0 + l1 * a1;
+        l_c = l0 * a0 + l1 * a1;
       }
       const float inv_l = l_c > 0.f ? 1.f / l_c : 0.f;
       const float lse_v = l_c > 0.f ? (m_c + __log2f(l_c)) * 0.69314718055994531f : -INFINITY;
@@ -604,10 +605,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       const int64_t orow_idx = ((int64_t)item.b * p.n_max + node) * p.Hq + h;
       const bool direct = item.n_splits == 1;
       const int my_slot = pair_ws_slot(plan_base, item.my_slot, rank);
-      // the normalised row (both chains in dual mode), in chunks of 32 columns
+      const int col0 = t * (D / 2);
+      const uint32_t tO0 = tmem + lane_base + 256, tO1 = tO0 + D;
+      // the normalised row, in chunks of 32 columns
       auto row_chunk = [&](int c0, float* y) {
         uint32_t o[32];
-        tmem_ld32(tO + c0, o);
+        tmem_ld32(tO0 + c0, o);
         if (dual) {
           uint32_t o1[32];
           tmem_ld32(tO1 + c0, o1);
@@ -636,7 +639,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       };
       float amax = 0.f;
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = col0; c0 < col0 + D / 2; c0 += 32) {
         float y[32];
         row_chunk(c0, y);
         if (direct) {
@@ -655,45 +658,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       }
       constexpr float kHalfMax = 65504.f;
       float row_scale = 1.f;
-      if (!direct && __any_sync(0xffffffffu, amax > kHalfMax)) {
-        const bool over = amax > kHalfMax;
-        if (over) row_scale = amax;
-        const float to_half = 1.f / row_scale;
+      if (!direct) {
+        // one scale per row for both halves
+        amax_sh[t][r] = amax;
+        ok = ep_sync();
+        if (!ok) break;
+        const float row_amax = fmaxf(amax_sh[0][r], amax_sh[1][r]);
+        if (__any_sync(0xffffffffu, row_amax > kHalfMax)) {
+          const bool over = row_amax > kHalfMax;
+          if (over) row_scale = row_amax;
+          const float to_half = 1.f / row_scale;
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          float y[32];
-          row_chunk(c0, y);
-          if (row_ok && over) half_store(y, c0, to_half);
+          for (int c0 = col0; c0 < col0 + D / 2; c0 += 32) {
+            float y[32];
+            row_chunk(c0, y);
+            if (row_ok && over) half_store(y, c0, to_half);
+          }
         }
       }
       arrive_leader(&bar_of[0]);  // the accumulator(s) may be overwritten by the next item
       if (dual) arrive_leader(&bar_of[1]);
       if (direct) {
-        if (row_ok && p.lse) p.lse[orow_idx] = lse_v;
+        if (row_ok && t == 0 && p.lse) p.lse[orow_idx] = lse_v;
       } else {
-        if (row_ok) {
+        if (row_ok && t == 0) {
           p.part_lse[(int64_t)my_slot * kRowsPerSlot + r] = lse_v;
           p.part_scale[(int64_t)my_slot * kRowsPerSlot + r] = row_scale;
         }
         // ticket of this CTA's rows: the last split to arrive merges every partial
         __threadfence();
-        ok = wg_sync();
+        ok = ep_sync();
         if (!ok) break;
         const int tick_idx = (((item.b * p.Hkv + item.g) * p.mp_max + lane_id) * kNT) + (int)rank;
-        if (r == 0) ticket_sh[0] = atomicAdd(p.ws_tickets + tick_idx, 1);
-        ok = wg_sync();
+        if (t == 0 && r == 0) ticket_sh[0] = atomicAdd(p.ws_tickets + tick_idx, 1);
+        ok = ep_sync();
         if (!ok) break;
         if (ticket_sh[0] == item.n_splits - 1) {
           __threadfence();
           const int n_rows = min(kBM, N * G - mrow0);
           if (n_rows > 0) {
+            const int r2 = t * kBM + r;  // both warpgroups
             auto slot_of = [&](int sp) { return pair_ws_slot(plan_base, split_slot(item, sp), rank); };
-            if (item.n_splits <= 2) merge_items<D, 2, 8, kBM>(p, item, mrow0, 0, n_rows, r, slot_of);
-            else if (item.n_splits <= 4) merge_items<D, 4, 4, kBM>(p, item, mrow0, 0, n_rows, r, slot_of);
-            else if (item.n_splits <= 6) merge_items<D, 6, 4, kBM>(p, item, mrow0, 0, n_rows, r, slot_of);
-            else merge_items<D, 8, 2, kBM>(p, item, mrow0, 0, n_rows, r, slot_of);
+            if (item.n_splits <= 2) merge_items<D, 2, 8, 2 * kBM>(p, item, mrow0, 0, n_rows, r2, slot_of);
+            else if (item.n_splits <= 4) merge_items<D, 4, 4, 2 * kBM>(p, item, mrow0, 0, n_rows, r2, slot_of);
+            else if (item.n_splits <= 6) merge_items<D, 6, 4, 2 * kBM>(p, item, mrow0, 0, n_rows, r2, slot_of);
+            else merge_items<D, 8, 2, 2 * kBM>(p, item, mrow0, 0, n_rows, r2, slot_of);
           }
-          if (r == 0) p.ws_tickets[tick_idx] = 0;  // ready for the next call
+          if (t == 0 && r == 0) p.ws_tickets[tick_idx] = 0;  // ready for the next call
         }
       }
     }
