@@ -4,9 +4,11 @@
 // the host by the plan's tests.
 //
 // A work group is (request, KV head, M-tile pair); a KV tile of a group with nt
-// active M tiles costs nt + 1 units, and CTA k takes the contiguous cost range
-// [cut(k), cut(k + 1)) of the whole batch.  A group cut between CTAs is split:
-// each split writes a partial into its slot and the last to arrive merges.
+// active M tiles costs nt + 1 units, each end of a group eh more (the fixed cost
+// of an item: its epilogue and the pipeline's restart; eh = 0 charges none),
+// and CTA k takes the contiguous cost range [cut(k), cut(k + 1)) of the whole
+// batch.  A group cut between CTAs is split: each split writes a partial into
+// its slot and the last to arrive merges.
 #ifndef TV_ATTN_PLAN_CUH_
 #define TV_ATTN_PLAN_CUH_
 
@@ -38,6 +40,7 @@ struct PlanView {
   const int32_t* T;      // KV tiles of each request (0 = request skipped)
   const int32_t* MT;     // M tiles of each request
   int B, Hkv;
+  int eh;                // cost units at each end of a group (0: none)
   int64_t W;             // total cost (< 2^40, so k * W fits in 64 bits)
   int C;                 // CTAs that receive work
   bool narrow;           // (C + 1) * W < 2^32: 32-bit division suffices
@@ -62,10 +65,11 @@ struct Item {
 
 // Iterates this CTA's items in the global (request, KV head, pair, tile) order.
 // A tile belongs to the CTA whose cost range holds the tile's first cost unit;
-// a tile of a group with nt active M tiles costs nt + 1 units.
+// a tile of a group with nt active M tiles costs nt + 1 units, and the group's
+// tiles start eh units after the group (its end carries eh more).
 struct ItemIter {
   int b, j;           // request and group index within it (j = g * MP + mp)
-  int64_t gstart;     // cost position of the current group's first tile
+  int64_t gstart;     // cost position of the current group (its first tile starts eh later)
   int c_prev;         // cost per tile of the group before the current one (0: none)
   int produced;
   int64_t lo, hi;     // this CTA's cost range
@@ -89,16 +93,16 @@ TV_PLAN_FN void iter_init(ItemIter& it, const PlanView& pv, int cta) {
   it.gstart = b < pv.B ? pv.start[b] : pv.W;
   if (b < pv.B) {
     const int T = pv.T[b], MT = pv.MT[b], MP = (MT + 1) / 2;
-    const int64_t per_g = (int64_t)T * (MT + MP);
+    const int64_t per_g = (int64_t)T * (MT + MP) + 2ll * pv.eh * MP;  // one KV head
+    const int64_t per_p = 3ll * T + 2 * pv.eh;                          // one full M-tile pair
     const int64_t off = it.lo - pv.start[b];
     if (off > 0) {
       // 32-bit divisions when every cost position fits in 32 bits
       const int g = (int)imin64(pv.Hkv - 1, pv.narrow ? (int64_t)((uint32_t)off / (uint32_t)per_g) : off / per_g);
       const int64_t off2 = off - g * per_g;
-      const int mp = (int)imin64(MP - 1, pv.narrow ? (int64_t)((uint32_t)off2 / (uint32_t)(3 * T))
-                                                   : off2 / (3ll * T));
+      const int mp = (int)imin64(MP - 1, pv.narrow ? (int64_t)((uint32_t)off2 / (uint32_t)per_p) : off2 / per_p);
       it.j = g * MP + mp;
-      it.gstart = pv.start[b] + g * per_g + (int64_t)mp * 3 * T;
+      it.gstart = pv.start[b] + g * per_g + (int64_t)mp * per_p;
     }
     if (it.j > 0) {
       const int mpp = (it.j - 1) % MP;
@@ -128,10 +132,11 @@ TV_PLAN_FN bool iter_next(ItemIter& it, const PlanView& pv, int cta, Item& o) {
     const int nt = imin32(2, MT - 2 * mp);
     const int c = nt + 1;
     const int64_t gs = it.gstart;
-    const int64_t i_lo = imin64(T, ceil_div_c(it.lo - gs, c));
-    const int64_t i_hi = imin64(T, ceil_div_c(it.hi - gs, c));
+    const int64_t t0 = gs + pv.eh;  // the group's first tile
+    const int64_t i_lo = imin64(T, ceil_div_c(it.lo - t0, c));
+    const int64_t i_hi = imin64(T, ceil_div_c(it.hi - t0, c));
     const int c_prev = it.c_prev;
-    it.gstart += (int64_t)T * c;
+    it.gstart += (int64_t)T * c + 2 * pv.eh;
     it.c_prev = c;
     ++it.j;
     if (i_lo >= i_hi) continue;
@@ -141,11 +146,12 @@ TV_PLAN_FN bool iter_next(ItemIter& it, const PlanView& pv, int cta, Item& o) {
     o.nt = nt;
     o.tile_begin = (int)i_lo;
     o.tile_end = (int)i_hi;
-    o.k0 = pv.owner(gs);
-    o.n_splits = pv.owner(gs + (int64_t)(T - 1) * c) - o.k0 + 1;
-    // split 0's slot: 2*k0 when the group is CTA k0's first item, else 2*k0 + 1;
-    // every later split is its CTA's first item
-    const bool first_of_k0 = (c_prev == 0) || pv.owner(gs - c_prev) < o.k0;
+    o.k0 = pv.owner(t0);
+    o.n_splits = pv.owner(t0 + (int64_t)(T - 1) * c) - o.k0 + 1;
+    // split 0's slot: 2*k0 when the group is CTA k0's first item (the previous
+    // group's last tile, eh + c_prev units before gs, is another CTA's), else
+    // 2*k0 + 1; every later split is its CTA's first item
+    const bool first_of_k0 = (c_prev == 0) || pv.owner(gs - pv.eh - c_prev) < o.k0;
     o.slot0 = 2 * o.k0 + (first_of_k0 ? 0 : 1);
     o.my_slot = 2 * cta + (it.produced == 0 ? 0 : 1);
     ++it.produced;
