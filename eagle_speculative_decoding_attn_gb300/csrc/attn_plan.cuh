@@ -4,10 +4,10 @@
 // the host by the plan's tests.
 //
 // A work group is (request, KV head, M-tile pair); a KV tile of a group with nt
-// active M tiles costs nt + 1 units, each end of a group eh more (the fixed cost
-// of an item: its epilogue and the pipeline's restart; eh = 0 charges none),
-// and CTA k takes the contiguous cost range [cut(k), cut(k + 1)) of the whole
-// batch.  A group cut between CTAs is split: each split writes a partial into
+// active M tiles costs nt + 1 units, the start of a group eh more and its end
+// ee more (the fixed costs of an item: the pipeline's restart, the epilogue and
+// a split's merge; 0 charges none), and CTA k takes the contiguous cost range
+// [cut(k), cut(k + 1)) of the whole batch.  A group cut between CTAs is split: each split writes a partial into
 // its slot and the last to arrive merges.
 #ifndef TV_ATTN_PLAN_CUH_
 #define TV_ATTN_PLAN_CUH_
@@ -40,7 +40,7 @@ struct PlanView {
   const int32_t* T;      // KV tiles of each request (0 = request skipped)
   const int32_t* MT;     // M tiles of each request
   int B, Hkv;
-  int eh;                // cost units at each end of a group (0: none)
+  int eh, ee;            // cost units at the start and at the end of a group (0: none)
   int64_t W;             // total cost (< 2^40, so k * W fits in 64 bits)
   int C;                 // CTAs that receive work
   bool narrow;           // (C + 1) * W < 2^32: 32-bit division suffices
@@ -66,7 +66,7 @@ struct Item {
 // Iterates this CTA's items in the global (request, KV head, pair, tile) order.
 // A tile belongs to the CTA whose cost range holds the tile's first cost unit;
 // a tile of a group with nt active M tiles costs nt + 1 units, and the group's
-// tiles start eh units after the group (its end carries eh more).
+// tiles start eh units after the group (its end carries ee more).
 struct ItemIter {
   int b, j;           // request and group index within it (j = g * MP + mp)
   int64_t gstart;     // cost position of the current group (its first tile starts eh later)
@@ -93,8 +93,8 @@ TV_PLAN_FN void iter_init(ItemIter& it, const PlanView& pv, int cta) {
   it.gstart = b < pv.B ? pv.start[b] : pv.W;
   if (b < pv.B) {
     const int T = pv.T[b], MT = pv.MT[b], MP = (MT + 1) / 2;
-    const int64_t per_g = (int64_t)T * (MT + MP) + 2ll * pv.eh * MP;  // one KV head
-    const int64_t per_p = 3ll * T + 2 * pv.eh;                          // one full M-tile pair
+    const int64_t per_g = (int64_t)T * (MT + MP) + (int64_t)(pv.eh + pv.ee) * MP;  // one KV head
+    const int64_t per_p = 3ll * T + pv.eh + pv.ee;                                  // one full M-tile pair
     const int64_t off = it.lo - pv.start[b];
     if (off > 0) {
       // 32-bit divisions when every cost position fits in 32 bits
@@ -136,7 +136,7 @@ TV_PLAN_FN bool iter_next(ItemIter& it, const PlanView& pv, int cta, Item& o) {
     const int64_t i_lo = imin64(T, ceil_div_c(it.lo - t0, c));
     const int64_t i_hi = imin64(T, ceil_div_c(it.hi - t0, c));
     const int c_prev = it.c_prev;
-    it.gstart += (int64_t)T * c + 2 * pv.eh;
+    it.gstart += (int64_t)T * c + pv.eh + pv.ee;
     it.c_prev = c;
     ++it.j;
     if (i_lo >= i_hi) continue;
@@ -149,9 +149,9 @@ TV_PLAN_FN bool iter_next(ItemIter& it, const PlanView& pv, int cta, Item& o) {
     o.k0 = pv.owner(t0);
     o.n_splits = pv.owner(t0 + (int64_t)(T - 1) * c) - o.k0 + 1;
     // split 0's slot: 2*k0 when the group is CTA k0's first item (the previous
-    // group's last tile, eh + c_prev units before gs, is another CTA's), else
+    // group's last tile, ee + c_prev units before gs, is another CTA's), else
     // 2*k0 + 1; every later split is its CTA's first item
-    const bool first_of_k0 = (c_prev == 0) || pv.owner(gs - pv.eh - c_prev) < o.k0;
+    const bool first_of_k0 = (c_prev == 0) || pv.owner(gs - pv.ee - c_prev) < o.k0;
     o.slot0 = 2 * o.k0 + (first_of_k0 ? 0 : 1);
     o.my_slot = 2 * cta + (it.produced == 0 ? 0 : 1);
     ++it.produced;

@@ -329,6 +329,7 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
   pv.B = p.B;
   pv.Hkv = p.Hkv;
   pv.eh = kItemEnd;
+  pv.ee = kItemEnd;
   pv.W = plan_W;
   pv.C = plan_C;
   pv.narrow = (int64_t)(plan_C + 1) * plan_W < (int64_t(1) << 32);

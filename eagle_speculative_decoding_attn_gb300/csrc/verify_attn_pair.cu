@@ -52,11 +52,13 @@ constexpr int kPHalfKeys = 64;      // keys of this CTA's K half tile
 constexpr uint32_t kWgArrivals = 8; // one arrival per warp of a softmax warpgroup, from both CTAs
 constexpr uint32_t kEpArrivals = 16;  // one arrival per softmax warp of both warpgroups, from both CTAs
 constexpr int kMaxLanes = 4;        // 256-row blocks per KV head (n_max * G <= 1024)
-// Plan cost units charged at each end of a (request, KV head) group, on top of
-// 3 units per KV tile: an item's epilogue and the restart of its two chains
-// take about as long as a few stages, so a cluster that crosses more group
-// boundaries gets fewer tiles.
-constexpr int kPairItemEnd = 8;
+// Plan cost units charged at the start and at the end of a (request, KV head)
+// group, on top of 3 units per KV tile: the restart of an item's two chains,
+// its epilogue and a split's merge take about as long as a few stages, so a
+// cluster that crosses more group boundaries gets fewer tiles.
+// (Charging the ends differently, 2-8 units at the start and 12-16 at the end,
+// measured the same on the 70B and long-context batches.)
+constexpr int kPairItemStart = 8, kPairItemEnd = 8;
 
 struct PairSmem {
   static constexpr int kQTile = kBM * kPD * 2;          // [2 dim blocks][128 rows][128 B]
@@ -162,7 +164,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         const int L = p.prefix_len[b], N = p.n_nodes[b];
         const bool skip = p.status[b] != 0 || request_shape_bits(L, N, p.n_max, p.max_pages) != 0;
         if (!skip) {
-          cost = (int64_t)p.Hkv * (((L + N + kBN - 1) / kBN) * 3 + 2 * kPairItemEnd);
+          cost = (int64_t)p.Hkv * (((L + N + kBN - 1) / kBN) * 3 + kPairItemStart + kPairItemEnd);
           chains = (N * p.G + 2 * kBM - 1) / (2 * kBM);
         }
       }
@@ -204,7 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         const bool skip = my_lane < 0 || p.status[b] != 0 || request_shape_bits(L, N, p.n_max, p.max_pages) != 0 ||
                           (N * p.G + 2 * kBM - 1) / (2 * kBM) <= my_lane;
         const int T = skip ? 0 : (L + N + kBN - 1) / kBN;
-        cost = T > 0 ? (int64_t)p.Hkv * (T * 3 + 2 * kPairItemEnd) : 0;
+        cost = T > 0 ? (int64_t)p.Hkv * (T * 3 + kPairItemStart + kPairItemEnd) : 0;
         rq_T[b] = T;
         rq_MT[b] = 2;
       }
@@ -237,7 +239,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   pv.MT = rq_MT;
   pv.B = p.B;
   pv.Hkv = p.Hkv;
-  pv.eh = kPairItemEnd;
+  pv.eh = kPairItemStart;
+  pv.ee = kPairItemEnd;
   pv.W = plan_W;
   pv.C = plan_C;
   pv.narrow = (int64_t)(plan_C + 1) * plan_W < (int64_t(1) << 32);
