@@ -524,8 +524,7 @@ __global__ void __launch_bounds__(kExpThreads, 4) tree_expand_kernel(const Expan
   const int sl = blockIdx.x, y = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
   const int n_max = p.n_max, V = p.V;
-  griddep_wait();
-  griddep_launch_dependents();  // the next call's CTAs may become resident and wait
+  griddep_wait();  // no early trigger: the acceptance reads what this kernel writes before its own wait
   const int st = p.status[b];
   const int n = p.n_nodes[b], ls = p.level_start[b];
   const bool ok = st == 0 && n >= 1 && n <= n_max && ls >= 0 && ls <= n;
