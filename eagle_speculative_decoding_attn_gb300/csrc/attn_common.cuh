@@ -18,7 +18,7 @@ constexpr int kBN = 128;                       // keys per KV tile
 constexpr int kNT = 2;                         // M tiles per work group
 constexpr int kStages = 2;                     // K and V ring depth
 constexpr int kThreads = 384;                  // 12 warps (bf16 cache)
-constexpr int kThreadsQ4 = 512;                // 16 warps (4-bit cache: warps 12-15 decode)
+constexpr int kThreadsQ4 = 640;                // 20 warps (low-bit cache: warps 12-19 decode)
 constexpr int kPagesPerTile = kBN / kPageSize; // 8
 constexpr int kSoftThreads = 256;              // softmax threads of a CTA (warps 4-11)
 constexpr int kRowsPerSlot = kNT * kBM;        // rows of one partial slot
@@ -27,13 +27,20 @@ constexpr int kMaxBatchQ4 = 256;               // the 4-bit cache's code ring le
 constexpr float kRescaleLog2 = 8.0f;           // lazy O rescale threshold (factor 256)
 constexpr float kLog2e = 1.4426950408889634f;
 // register split: 384 threads x 168 at launch = 128 x 88 (warps 0-3) + 256 x 208 (softmax warps)
+constexpr uint32_t kRegsLaunch = 168;
 constexpr uint32_t kRegsControl = 88;
 constexpr uint32_t kRegsSoftmax = 208;
-static_assert(128 * kRegsControl + 256 * kRegsSoftmax == kThreads * 168, "register split must match the launch");
-// 4-bit cache: 512 threads at 128 registers each, no re-split (the compiler's
-// limit is the launch's 128 registers for every role, so the softmax reads the
-// S row in 64-column halves for its maximum and in 32-column chunks for the
-// probabilities)
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax == kThreads * kRegsLaunch, "register split must match the launch");
+// low-bit cache: 640 threads x 96 at launch = 128 x 96 (warps 0-3, no re-split)
+// + 256 x 128 (softmax warps) + 256 x 64 (decoding warps); at 128 registers the
+// softmax reads the S row in 64-column halves for its maximum and in 32-column
+// chunks for the probabilities
+constexpr uint32_t kRegsLaunchQ4 = 96;
+constexpr uint32_t kRegsSoftmaxQ4 = 128;
+constexpr uint32_t kRegsDecodeQ4 = 64;
+static_assert(128 * kRegsLaunchQ4 + 256 * kRegsSoftmaxQ4 + 256 * kRegsDecodeQ4 == kThreadsQ4 * kRegsLaunchQ4,
+              "register split must match the launch");
+static_assert(kThreadsQ4 * (kRegsLaunchQ4 + 8) > 65536, "the launch leaves each thread exactly kRegsLaunchQ4");
 constexpr int kQ4Group = 32;                   // dims sharing one (scale, zero) pair
 constexpr int kHalfKeys = kBN / 2;             // keys of one code slot (half a KV tile)
 

@@ -4,10 +4,12 @@
 // the host by the plan's tests.
 //
 // A work group is (request, KV head, M-tile pair); a KV tile of a group with nt
-// active M tiles costs nt + 1 units, the start of a group eh more and its end
-// ee more (the fixed costs of an item: the pipeline's restart, the epilogue and
-// a split's merge; 0 charges none), and CTA k takes the contiguous cost range
-// [cut(k), cut(k + 1)) of the whole batch.  A group cut between CTAs is split: each split writes a partial into
+// active M tiles costs nt + 1 + tx units (tx: a per-tile cost that does not grow
+// with nt, such as decoding a low-bit cache; 0 charges none), the start of a
+// group eh more and its end ee more (the fixed costs of an item: the pipeline's
+// restart, the epilogue and a split's merge; 0 charges none), and CTA k takes the contiguous cost range
+// [cut(k), cut(k + 1)) of the whole batch.  At most W / (3 + tx) CTAs take work,
+// so each range holds the first unit of at least one tile.  A group cut between CTAs is split: each split writes a partial into
 // its slot and the last to arrive merges.
 #ifndef TV_ATTN_PLAN_CUH_
 #define TV_ATTN_PLAN_CUH_
@@ -29,10 +31,12 @@ TV_PLAN_INL int imin32(int a, int b) { return a < b ? a : b; }
 TV_PLAN_INL uint32_t umin32(uint32_t a, uint32_t b) { return a < b ? a : b; }
 TV_PLAN_INL int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
 TV_PLAN_INL int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
-// ceil(a / c) for a cost per tile c in {2, 3}, 0 when a <= 0
+// ceil(a / c) for a cost per tile c >= 2, 0 when a <= 0 (no division for c = 2)
 TV_PLAN_INL int64_t ceil_div_c(int64_t a, int c) {
   if (a <= 0) return 0;
-  return c == 2 ? (a + 1) >> 1 : (a + 2) / 3;
+  if (c == 2) return (a + 1) >> 1;
+  if (c == 3) return (a + 2) / 3;
+  return (a + c - 1) / c;
 }
 
 struct PlanView {
@@ -41,6 +45,7 @@ struct PlanView {
   const int32_t* MT;     // M tiles of each request
   int B, Hkv;
   int eh, ee;            // cost units at the start and at the end of a group (0: none)
+  int tx;                // cost units of a KV tile on top of nt + 1 (0: none)
   int64_t W;             // total cost (< 2^40, so k * W fits in 64 bits)
   int C;                 // CTAs that receive work
   bool narrow;           // (C + 1) * W < 2^32: 32-bit division suffices
@@ -65,7 +70,7 @@ struct Item {
 
 // Iterates this CTA's items in the global (request, KV head, pair, tile) order.
 // A tile belongs to the CTA whose cost range holds the tile's first cost unit;
-// a tile of a group with nt active M tiles costs nt + 1 units, and the group's
+// a tile of a group with nt active M tiles costs nt + 1 + tx units, and the group's
 // tiles start eh units after the group (its end carries ee more).
 struct ItemIter {
   int b, j;           // request and group index within it (j = g * MP + mp)
@@ -93,8 +98,8 @@ TV_PLAN_FN void iter_init(ItemIter& it, const PlanView& pv, int cta) {
   it.gstart = b < pv.B ? pv.start[b] : pv.W;
   if (b < pv.B) {
     const int T = pv.T[b], MT = pv.MT[b], MP = (MT + 1) / 2;
-    const int64_t per_g = (int64_t)T * (MT + MP) + (int64_t)(pv.eh + pv.ee) * MP;  // one KV head
-    const int64_t per_p = 3ll * T + pv.eh + pv.ee;                                  // one full M-tile pair
+    const int64_t per_g = (int64_t)T * (MT + (int64_t)(1 + pv.tx) * MP) + (int64_t)(pv.eh + pv.ee) * MP;  // one KV head
+    const int64_t per_p = (int64_t)(3 + pv.tx) * T + pv.eh + pv.ee;  // one full M-tile pair
     const int64_t off = it.lo - pv.start[b];
     if (off > 0) {
       // 32-bit divisions when every cost position fits in 32 bits
@@ -106,13 +111,13 @@ TV_PLAN_FN void iter_init(ItemIter& it, const PlanView& pv, int cta) {
     }
     if (it.j > 0) {
       const int mpp = (it.j - 1) % MP;
-      it.c_prev = imin32(2, MT - 2 * mpp) + 1;
+      it.c_prev = imin32(2, MT - 2 * mpp) + 1 + pv.tx;
     } else {
       int bp = b - 1;
       while (bp >= 0 && pv.T[bp] == 0) --bp;
       if (bp >= 0) {
         const int MTp = pv.MT[bp], MPp = (MTp + 1) / 2;
-        it.c_prev = imin32(2, MTp - 2 * (MPp - 1)) + 1;
+        it.c_prev = imin32(2, MTp - 2 * (MPp - 1)) + 1 + pv.tx;
       }
     }
   }
@@ -130,7 +135,7 @@ TV_PLAN_FN bool iter_next(ItemIter& it, const PlanView& pv, int cta, Item& o) {
     }
     const int g = it.j / MP, mp = it.j - g * MP;
     const int nt = imin32(2, MT - 2 * mp);
-    const int c = nt + 1;
+    const int c = nt + 1 + pv.tx;
     const int64_t gs = it.gstart;
     const int64_t t0 = gs + pv.eh;  // the group's first tile
     const int64_t i_lo = imin64(T, ceil_div_c(it.lo - t0, c));

@@ -77,6 +77,20 @@ cudaError_t ensure_smem_attr(const void* func, size_t bytes) {
   return cudaSuccess;
 }
 
+cudaError_t check_launch_regs(const void* func, int expected) {
+  static std::mutex mu;
+  static std::map<const void*, int> regs;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = regs.find(func);
+  if (it == regs.end()) {
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, func);
+    if (e != cudaSuccess) return e;
+    it = regs.emplace(func, fa.numRegs).first;
+  }
+  return it->second == expected ? cudaSuccess : cudaErrorInvalidKernelImage;
+}
+
 }  // namespace tv
 
 extern "C" const char* tv_last_error(void) { return tv::g_last_error.c_str(); }

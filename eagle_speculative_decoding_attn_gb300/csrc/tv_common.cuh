@@ -46,6 +46,10 @@ cudaError_t current_context_id(unsigned long long* id);
 
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (context, kernel).
 cudaError_t ensure_smem_attr(const void* func, size_t bytes);
+// A kernel that moves registers between its warpgroups (setmaxnreg) must have
+// been built with exactly the per-thread count its split assumes: a smaller pool
+// would leave an increase waiting forever.  cudaErrorInvalidKernelImage if not.
+cudaError_t check_launch_regs(const void* func, int expected);
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 

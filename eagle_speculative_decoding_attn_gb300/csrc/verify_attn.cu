@@ -54,6 +54,11 @@ namespace attn {
 // much as a few tiles, so a CTA that crosses more group boundaries takes fewer
 // tiles (serving batch 140 -> 112 us, 7B shape 22.3 -> 20.7 us against no charge).
 constexpr int kItemEnd = 6;
+// Low-bit cache: a KV tile costs its decode, which does not grow with the active
+// M tiles, so the plan charges each tile kTileDecode units more (in units of the
+// bf16 kernel's per-tile cost nt + 1).
+constexpr int kTileDecode = 4;
+constexpr int kItemEndQ4 = 6;
 
 // dynamic shared-memory layout (1024-byte aligned base)
 template <int D, int kLB>
@@ -112,22 +117,22 @@ __device__ __forceinline__ void merge_tile(const AttnParams& p, const Item& it, 
 // mantissa bits of 2^23 and subtracting 2^23; the fused multiply-add then
 // rounds the exact code * scale + zero once to fp32, and the conversion rounds
 // that once to bf16.
+// The groups are a loop, not unrolled: the decoding warps share each SM
+// sub-partition's instruction cache with the softmax, and the unrolled row
+// (about 500 instructions) ran 15-20% slower.  Rows 2i and 2i + 1 start at
+// group i mod 4: code rows are 64 bytes apart, so without the rotation the
+// 16-byte loads of a quarter-warp hit the same four banks four times.
 template <int D>
 __device__ __forceinline__ void decode_row_q4(const uint8_t* codes, const uint8_t* params, uint8_t* stage, int r) {
   constexpr int kGroups = D / kQ4Group;
-  uint32_t pw[kGroups];  // (scale, zero) of each group, scale in the low half
-  if constexpr (kGroups == 4) {
-    const uint4 t = *reinterpret_cast<const uint4*>(params);
-    pw[0] = t.x; pw[1] = t.y; pw[2] = t.z; pw[3] = t.w;
-  } else {
-    const uint2 t = *reinterpret_cast<const uint2*>(params);
-    pw[0] = t.x; pw[1] = t.y;
-  }
   const uint64_t neg_magic = f2_pack(-8388608.f, -8388608.f);
-#pragma unroll
-  for (int gi = 0; gi < kGroups; ++gi) {
+  const int rot = (r >> 1) & (kGroups - 1);
+#pragma unroll 1
+  for (int k = 0; k < kGroups; ++k) {
+    const int gi = (k + rot) & (kGroups - 1);
     const uint4 c = reinterpret_cast<const uint4*>(codes)[gi];  // the group's 32 codes
-    const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&pw[gi]));
+    const uint32_t pw = reinterpret_cast<const uint32_t*>(params)[gi];  // (scale, zero), scale in the low half
+    const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&pw));
     const uint64_t s2 = f2_pack(sz.x, sz.x), z2 = f2_pack(sz.y, sz.y);
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
@@ -158,25 +163,20 @@ __device__ __forceinline__ void decode_row_q4(const uint8_t* codes, const uint8_
 // spread into the bytes of a word: the low-bit pairs by shifts of 6, 12 and 18
 // (each lands at the bottom of its own byte), the third bits by a multiply with
 // 1 + 2^7 + 2^14 + 2^21 (bit k lands at bit 8k); then as in the 4-bit decode.
+// The groups are a loop, as in decode_row_q4 (3-bit code rows are 48 bytes
+// apart, so their loads need no rotation).
 template <int D>
 __device__ __forceinline__ void decode_row_q3(const uint8_t* codes, const uint8_t* params, uint8_t* stage, int r) {
   constexpr int kGroups = D / kQ4Group;
-  uint32_t pw[kGroups];  // (scale, zero) of each group, scale in the low half
-  if constexpr (kGroups == 4) {
-    const uint4 t = *reinterpret_cast<const uint4*>(params);
-    pw[0] = t.x; pw[1] = t.y; pw[2] = t.z; pw[3] = t.w;
-  } else {
-    const uint2 t = *reinterpret_cast<const uint2*>(params);
-    pw[0] = t.x; pw[1] = t.y;
-  }
   const uint2* lo2 = reinterpret_cast<const uint2*>(codes);
   const uint32_t* hi4 = reinterpret_cast<const uint32_t*>(codes + D / 4);
   const uint64_t neg_magic = f2_pack(-8388608.f, -8388608.f);
-#pragma unroll
+#pragma unroll 1
   for (int gi = 0; gi < kGroups; ++gi) {
     const uint2 l = lo2[gi];
     const uint32_t h = hi4[gi];
-    const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&pw[gi]));
+    const uint32_t pw = reinterpret_cast<const uint32_t*>(params)[gi];  // (scale, zero), scale in the low half
+    const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&pw));
     const uint64_t s2 = f2_pack(sz.x, sz.x), z2 = f2_pack(sz.y, sz.y);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {  // dims 8q .. 8q + 7 of the group: one 16-byte chunk
@@ -212,7 +212,7 @@ template <int D, int kLB>
 __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
     verify_attn_kernel(const __grid_constant__ AttnParams p) {
   using S = Smem<D, kLB>;
-  constexpr bool kQ4 = kLB != 0;  // a low-bit cache, decoded by warps 12-15
+  constexpr bool kQ4 = kLB != 0;  // a low-bit cache, decoded by warps 12-19
   constexpr int kNThreads = kQ4 ? kThreadsQ4 : kThreads;
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
@@ -243,10 +243,10 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
     mbar_init(&bar_q, 1);
     mbar_init(&bar_qe, 1);
     for (int s = 0; s < kStages; ++s) {
-      // a bf16 stage is filled by TMA (one arrival plus bytes) or by 64 decoding threads
-      mbar_init(&bar_kf[s], kQ4 ? kHalfKeys : 1);
+      // a bf16 stage is filled by TMA (one arrival plus bytes) or by 128 decoding threads
+      mbar_init(&bar_kf[s], kQ4 ? kBN : 1);
       mbar_init(&bar_ke[s], 1);
-      mbar_init(&bar_vf[s], kQ4 ? kHalfKeys : 1);
+      mbar_init(&bar_vf[s], kQ4 ? kBN : 1);
       mbar_init(&bar_ve[s], 1);
     }
     if (kQ4) {
@@ -297,7 +297,8 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
         if (!skip) {
           T = (L + N + kBN - 1) / kBN;
           MT = (N * p.G + kBM - 1) / kBM;
-          cost = (int64_t)p.Hkv * ((int64_t)T * (MT + (MT + 1) / 2) + 2ll * kItemEnd * ((MT + 1) / 2));
+          constexpr int kTx = kQ4 ? kTileDecode : 0, kEnd = kQ4 ? kItemEndQ4 : kItemEnd;
+          cost = (int64_t)p.Hkv * ((int64_t)T * (MT + (1 + kTx) * ((MT + 1) / 2)) + 2ll * kEnd * ((MT + 1) / 2));
         }
         rq_T[b] = T;
         rq_MT[b] = MT;
@@ -314,7 +315,9 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
     if (lane == 0) {
       rq_start[p.B] = carry;
       plan_W = carry;
-      plan_C = (int)imax64(1, imin64(gridDim.x, carry / 3));
+      // at least one tile's cost (3 + tx units at most) per CTA, so that every CTA
+      // between a group's first and last split holds a tile of it
+      plan_C = (int)imax64(1, imin64(gridDim.x, carry / (3 + (kQ4 ? kTileDecode : 0))));
     }
   }
   tc_fence_before();
@@ -328,8 +331,9 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
   pv.MT = rq_MT;
   pv.B = p.B;
   pv.Hkv = p.Hkv;
-  pv.eh = kItemEnd;
-  pv.ee = kItemEnd;
+  pv.eh = kQ4 ? kItemEndQ4 : kItemEnd;
+  pv.ee = kQ4 ? kItemEndQ4 : kItemEnd;
+  pv.tx = kQ4 ? kTileDecode : 0;
   pv.W = plan_W;
   pv.C = plan_C;
   pv.narrow = (int64_t)(plan_C + 1) * plan_W < (int64_t(1) << 32);
@@ -554,12 +558,19 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
       if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.ws_bits + item.b, TV_DEV_PAGE_OOB);
     }
   } else if (kQ4 && has_work && warp >= 12) {
-    // ------------------------------------------------------------ 4-bit decoders
-    // warps 12-13 decode K, warps 14-15 V: thread i takes key row 64 h + i of half h
-    const bool is_k = warp < 14;
-    const int ri = tid - (is_k ? 384 : 448);
+    // ------------------------------------------------------------ low-bit decoders
+    // warps 12-15 decode K, warps 16-19 V: thread i takes key row i of each tile
+    // (rows 0-63 from code slot 0, rows 64-127 from code slot 1)
+    setmaxnreg_dec<kRegsDecodeQ4>();
+    const bool is_k = warp < 16;
+    const int ri = tid - (is_k ? 384 : 512);
+    const int h = ri / kHalfKeys;
+    const uint8_t* const slot = smem + (is_k ? S::kKC : S::kVC) + h * S::kSlot;
+    const uint8_t* const crow = slot + (ri % kHalfKeys) * S::kCodeRow;
+    const uint8_t* const prow = slot + S::kSlotParams + (ri % kHalfKeys) * S::kParamRow;
+    uint64_t* const cfull = is_k ? &bar_kcf[h] : &bar_vcf[h];
+    uint64_t* const cfree = is_k ? &bar_kce[h] : &bar_vce[h];
     uint8_t* const stage0 = is_k ? sK : sV;
-    const uint8_t* const slots = smem + (is_k ? S::kKC : S::kVC);
     ItemIter it;
     iter_init(it, pv, cta);
     Item item;
@@ -570,26 +581,16 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
       for (int tile = item.tile_begin; tile < item.tile_end && ok; ++tile, ++kv_it) {
         const int s = kv_it % kStages;
         const uint32_t ph = (kv_it / kStages) & 1u;
-        const int key0 = tile * kBN;
-        const int npg = min(kPagesPerTile, (L + N - key0 + kPageSize - 1) / kPageSize);
+        const int npg = min(kPagesPerTile, (L + N - tile * kBN + kPageSize - 1) / kPageSize);
         // the bf16 stage is free once the MMAs of the tile it held have completed
         ok = warp_wait(is_k ? &bar_ke[s] : &bar_ve[s], ph ^ 1u, &abort_sh);
+        ok = ok && warp_wait(cfull, kv_it & 1u, &abort_sh);
         if (!ok) break;
-        uint8_t* const stage = stage0 + s * S::kKVTile;
-        for (int h = 0; h < 2; ++h) {
-          ok = warp_wait(is_k ? &bar_kcf[h] : &bar_vcf[h], kv_it & 1u, &abort_sh);
-          if (!ok) break;
-          const int r = h * kHalfKeys + ri;  // key row of the tile
-          if (r < npg * kPageSize)
-          {
-            const uint8_t* crow = slots + h * S::kSlot + ri * S::kCodeRow;
-            const uint8_t* prow = slots + h * S::kSlot + S::kSlotParams + ri * S::kParamRow;
-            if constexpr (kLB == 3) decode_row_q3<D>(crow, prow, stage, r);
-            else decode_row_q4<D>(crow, prow, stage, r);
-          }
-          mbar_arrive(is_k ? &bar_kce[h] : &bar_vce[h]);
+        if (ri < npg * kPageSize) {
+          if constexpr (kLB == 3) decode_row_q3<D>(crow, prow, stage0 + s * S::kKVTile, ri);
+          else decode_row_q4<D>(crow, prow, stage0 + s * S::kKVTile, ri);
         }
-        if (!ok) break;
+        mbar_arrive(cfree);
         fence_proxy_async_smem();  // the tensor pipe reads what these threads wrote
         mbar_arrive(is_k ? &bar_kf[s] : &bar_vf[s]);
       }
@@ -597,6 +598,7 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
   } else if (has_work && warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
     if constexpr (!kQ4) setmaxnreg_inc<kRegsSoftmax>();
+    else setmaxnreg_inc<kRegsSoftmaxQ4>();
     const int t = (warp - 4) >> 2;
     const int r = (warp & 3) * 32 + lane;                 // row of the M tile = TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -951,6 +953,7 @@ template <int D, int kLB>
 static int launch(const AttnParams& ap, int grid, cudaStream_t st) {
   using S = Smem<D, kLB>;
   TV_CUDA_CHECK(ensure_smem_attr((const void*)verify_attn_kernel<D, kLB>, S::kAlloc));
+  TV_CUDA_CHECK(check_launch_regs((const void*)verify_attn_kernel<D, kLB>, (int)(kLB != 0 ? kRegsLaunchQ4 : kRegsLaunch)));
   TV_CUDA_CHECK(launch_pdl(verify_attn_kernel<D, kLB>, dim3(grid), dim3(kLB != 0 ? kThreadsQ4 : kThreads),
                            (size_t)S::kAlloc, st, ap));
   TV_CUDA_CHECK(cudaGetLastError());

@@ -241,6 +241,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   pv.Hkv = p.Hkv;
   pv.eh = kPairItemStart;
   pv.ee = kPairItemEnd;
+  pv.tx = 0;
   pv.W = plan_W;
   pv.C = plan_C;
   pv.narrow = (int64_t)(plan_C + 1) * plan_W < (int64_t(1) << 32);
@@ -759,6 +760,7 @@ static int pair_clusters_resident() {
 
 int launch_pair(const AttnParams& ap, int max_ctas, cudaStream_t st) {
   TV_CUDA_CHECK(ensure_smem_attr((const void*)verify_attn_pair_kernel, PairSmem::kAlloc));
+  TV_CUDA_CHECK(check_launch_regs((const void*)verify_attn_pair_kernel, (int)kRegsLaunch));
   const int resident = pair_clusters_resident();
   TV_REQUIRE(resident > 0, TV_ERR_CUDA, "tv_tree_verify_attn: no CTA pair of the attention kernel fits an SM pair");
   const int grid = 2 * std::max(1, std::min(resident, max_ctas / 2));

@@ -6,9 +6,9 @@
 //
 // The per-request cost below restates the kernel's planner: T KV tiles of 128
 // keys, MT M tiles of 128 rows, MP = ceil(MT / 2) pairs, a tile of a pair with
-// nt active M tiles costing nt + 1, eh more units at the start of a group and ee
-// more at its end (a few for the kernels; drawn at random here); CTAs that
-// receive work: max(1, min(grid, W / 3)).
+// nt active M tiles costing nt + 1 + tx, eh more units at the start of a group and
+// ee more at its end (a few for the kernels; drawn at random here); CTAs that
+// receive work: max(1, min(grid, W / (3 + tx))).
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
@@ -46,6 +46,8 @@ int main(int argc, char** argv) {
     const int maxL = (c % 3 == 0) ? 40000 : 3000;
     const int ehs[] = {0, 1, 3, 8, 40};
     const int eh = ehs[uni(0, 4)], ee = ehs[uni(0, 4)];
+    const int txs[] = {0, 0, 1, 4, 9};
+    const int tx = txs[uni(0, 4)];
     std::vector<int64_t> start(B + 1);
     std::vector<int32_t> T(B), MT(B);
     int64_t W = 0;
@@ -55,7 +57,9 @@ int main(int argc, char** argv) {
       T[b] = skipped ? 0 : (L + N + 127) / 128;
       MT[b] = skipped ? 0 : (N * G + 127) / 128;
       start[b] = W;
-      if (T[b] > 0) W += (int64_t)Hkv * ((int64_t)T[b] * (MT[b] + (MT[b] + 1) / 2) + (int64_t)(eh + ee) * ((MT[b] + 1) / 2));
+      if (T[b] > 0)
+        W += (int64_t)Hkv * ((int64_t)T[b] * (MT[b] + (int64_t)(1 + tx) * ((MT[b] + 1) / 2)) +
+                             (int64_t)(eh + ee) * ((MT[b] + 1) / 2));
     }
     start[B] = W;
     if (W == 0) continue;
@@ -67,8 +71,9 @@ int main(int argc, char** argv) {
     pv.Hkv = Hkv;
     pv.eh = eh;
     pv.ee = ee;
+    pv.tx = tx;
     pv.W = W;
-    pv.C = (int)std::max<int64_t>(1, std::min<int64_t>(grid, W / 3));
+    pv.C = (int)std::max<int64_t>(1, std::min<int64_t>(grid, W / (3 + tx)));
     pv.narrow = (int64_t)(pv.C + 1) * W < (int64_t(1) << 32);
 
     std::map<std::tuple<int, int, int>, std::vector<Rec>> by_group;

@@ -155,11 +155,12 @@ def test_q4_decode_exact_through_single_key_rows():
 
 def test_q4_matches_bf16_kernel_on_the_decoded_cache():
     """The 4-bit kernel against the bf16 kernel run on the oracle-decoded cache:
-    the same plan, products and probabilities; only the order of one fp32 row
-    sum differs.  That moves a split's fp16 partial (O / max |O|) by at most
-    one fp16 step, 2^-11 of the partial's largest value, which a merge whose
-    terms cancel carries into a small output: outputs agree to a bf16 rounding
-    step plus 2^-13, and almost all of them are identical."""
+    the same products and probabilities, but the 4-bit plan charges each KV tile
+    for its decode, so the two kernels cut a group's tiles into splits at other
+    places.  A split's partial is stored in fp16 (O / max |O|), off by at most
+    2^-11 of its largest value, and that value is at most max |V|; each output
+    then takes one bf16 rounding (2^-7 relative at most).  So outputs agree to
+    2^-7 |o| + 2 * 2^-11 max |V|, and the log-sum-exps (fp32 merges) to 1e-5."""
     dev = require_gpu()
     w = W.make_workload("llama2_7b", with_logits=False)
     cache = _q4_cache(w, 51)
@@ -174,8 +175,10 @@ def test_q4_matches_bf16_kernel_on_the_decoded_cache():
     o2 = o2.float().cpu().numpy()
     n = int(w.n_nodes[0])
     d = np.abs(out[0, :n] - o2[0, :n])
-    assert np.all(d <= 2.0 ** -7 * np.abs(o2[0, :n]) + 2.0 ** -13)
-    assert (d > 0).mean() <= 1e-2
+    vmax = float(np.abs(oracle.bf16_to_f64(vd)).max())
+    bound = 2.0 ** -7 * np.abs(o2[0, :n]) + 2.0 ** -10 * vmax
+    print(f"max |d| {d.max():.3g}, max d / bound {(d / bound).max():.3f}, differing {(d > 0).mean():.4f}")
+    assert np.all(d <= bound)
     assert np.abs(lse[0, :n] - l2.cpu().numpy()[0, :n]).max() <= 1e-5
 
 
