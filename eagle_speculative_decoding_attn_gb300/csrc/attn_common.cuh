@@ -31,14 +31,15 @@ constexpr uint32_t kRegsLaunch = 168;
 constexpr uint32_t kRegsControl = 88;
 constexpr uint32_t kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax == kThreads * kRegsLaunch, "register split must match the launch");
-// low-bit cache: 640 threads x 96 at launch = 128 x 96 (warps 0-3, no re-split)
-// + 256 x 128 (softmax warps) + 256 x 64 (decoding warps); at 128 registers the
-// softmax reads the S row in 64-column halves for its maximum and in 32-column
-// chunks for the probabilities
+// low-bit cache: 640 threads x 96 at launch = 128 x 80 (warps 0-3) + 256 x 128
+// (softmax warps) + 256 x 72 (decoding warps); at 128 registers the softmax reads
+// the S row in 64-column halves for its maximum and in 32-column chunks for the
+// probabilities
 constexpr uint32_t kRegsLaunchQ4 = 96;
+constexpr uint32_t kRegsControlQ4 = 80;
 constexpr uint32_t kRegsSoftmaxQ4 = 128;
-constexpr uint32_t kRegsDecodeQ4 = 64;
-static_assert(128 * kRegsLaunchQ4 + 256 * kRegsSoftmaxQ4 + 256 * kRegsDecodeQ4 == kThreadsQ4 * kRegsLaunchQ4,
+constexpr uint32_t kRegsDecodeQ4 = 72;
+static_assert(128 * kRegsControlQ4 + 256 * kRegsSoftmaxQ4 + 256 * kRegsDecodeQ4 == kThreadsQ4 * kRegsLaunchQ4,
               "register split must match the launch");
 static_assert(kThreadsQ4 * (kRegsLaunchQ4 + 8) > 65536, "the launch leaves each thread exactly kRegsLaunchQ4");
 constexpr int kQ4Group = 32;                   // dims sharing one (scale, zero) pair

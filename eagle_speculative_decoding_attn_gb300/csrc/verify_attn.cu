@@ -108,94 +108,104 @@ __device__ __forceinline__ void merge_tile(const AttnParams& p, const Item& it, 
   }
 }
 
-// Decodes key row r of a 4-bit code slot into a bf16 K or V stage, laid out as
-// the TMA copies of a bf16 cache are (64-dim blocks of 128-byte rows, 16-byte
-// chunks swizzled by the row's low three bits).  Dim d of the row takes the
-// value bf16(fp32(code * scale + zero)) with the (scale, zero) fp16 pair of its
-// 32-dim group; byte j of the codes holds dim 2j in its low nibble and 2j + 1
-// in its high nibble.  A code becomes a float exactly by placing it in the low
-// mantissa bits of 2^23 and subtracting 2^23; the fused multiply-add then
-// rounds the exact code * scale + zero once to fp32, and the conversion rounds
-// that once to bf16.
-// The groups are a loop, not unrolled: the decoding warps share each SM
-// sub-partition's instruction cache with the softmax, and the unrolled row
-// (about 500 instructions) ran 15-20% slower.  Rows 2i and 2i + 1 start at
-// group i mod 4: code rows are 64 bytes apart, so without the rotation the
-// 16-byte loads of a quarter-warp hit the same four banks four times.
-template <int D>
-__device__ __forceinline__ void decode_row_q4(const uint8_t* codes, const uint8_t* params, uint8_t* stage, int r) {
-  constexpr int kGroups = D / kQ4Group;
-  const uint64_t neg_magic = f2_pack(-8388608.f, -8388608.f);
-  const int rot = (r >> 1) & (kGroups - 1);
-#pragma unroll 1
-  for (int k = 0; k < kGroups; ++k) {
-    const int gi = (k + rot) & (kGroups - 1);
-    const uint4 c = reinterpret_cast<const uint4*>(codes)[gi];  // the group's 32 codes
-    const uint32_t pw = reinterpret_cast<const uint32_t*>(params)[gi];  // (scale, zero), scale in the low half
-    const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&pw));
-    const uint64_t s2 = f2_pack(sz.x, sz.x), z2 = f2_pack(sz.y, sz.y);
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+// One key row of a low-bit code slot, held in registers: the decoding thread
+// copies its row out and frees the slot for the next tile's codes before it
+// decodes, so that load overlaps this tile's decode.  4-bit: each 32-dim group's
+// 32 codes (one 16-byte word) and its (scale, zero) fp16 pair, scale in the low
+// half.  3-bit: each group's two words of low bits and one word of third bits.
+template <int D, int kLB>
+struct CodeRow {
+  static constexpr int kGroups = D / kQ4Group;
+  uint4 c[kGroups];      // 4-bit: the group's codes; 3-bit: x, y low bits, z third bits
+  uint32_t pw[kGroups];
+};
+
+// Copies row `codes` / `params` of a code slot.  4-bit rows are 64 bytes apart,
+// so a quarter-warp's 16-byte loads of one group would hit the same four banks
+// four times: rows 2i and 2i + 1 start at group i mod 4 (entry k holds group
+// (k + rot) mod 4).  3-bit rows are 48 bytes apart and need no rotation.
+template <int D, int kLB>
+__device__ __forceinline__ void load_code_row(CodeRow<D, kLB>& x, const uint8_t* codes, const uint8_t* params,
+                                              int rot) {
+  constexpr int kG = CodeRow<D, kLB>::kGroups;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {  // dims 8q .. 8q + 7 of the group: one 16-byte chunk
-      const uint32_t lo = w[q] & 0x0F0F0F0Fu, hi = (w[q] >> 4) & 0x0F0F0F0Fu;
-      uint32_t o[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float ce = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440u + j));
-        const float co = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440u + j));
-        float ve, vo;
-        f2_unpack(f2_fma(f2_add(f2_pack(ce, co), neg_magic), s2, z2), ve, vo);
-        o[j] = pack_bf16x2(ve, vo);
-      }
-      const int d0 = gi * kQ4Group + q * 8;
-      const int db = d0 / 64, ch = (d0 % 64) / 8;
-      *reinterpret_cast<uint4*>(stage + db * (kBN * 128) + r * 128 + ((ch ^ (r & 7)) << 4)) =
-          make_uint4(o[0], o[1], o[2], o[3]);
+  for (int k = 0; k < kG; ++k) {
+    const int gi = (k + rot) & (kG - 1);
+    if constexpr (kLB == 3) {
+      const uint2 l = reinterpret_cast<const uint2*>(codes)[gi];
+      x.c[k] = make_uint4(l.x, l.y, reinterpret_cast<const uint32_t*>(codes + D / 4)[gi], 0u);
+    } else {
+      x.c[k] = reinterpret_cast<const uint4*>(codes)[gi];
     }
+    x.pw[k] = reinterpret_cast<const uint32_t*>(params)[gi];
   }
 }
 
-// Decodes key row r of a 3-bit code slot into a bf16 K or V stage (the layout
-// of decode_row_q4).  The row's codes: its low two bits four per byte (byte j:
-// dims 4j .. 4j+3, dim 4j+i in bits 2i and 2i+1), then its third bits eight per
-// byte (byte D/4 + j: dims 8j .. 8j+7, dim 8j+i in bit i); per group of 32 dims
-// two 32-bit words of low bits and one of third bits.  Four codes at a time are
-// spread into the bytes of a word: the low-bit pairs by shifts of 6, 12 and 18
+// Decodes a code row into key row r of a bf16 K or V stage, laid out as the TMA
+// copies of a bf16 cache are (64-dim blocks of 128-byte rows, 16-byte chunks
+// swizzled by the row's low three bits).  Dim d of the row takes the value
+// bf16(fp32(code * scale + zero)) with the (scale, zero) pair of its 32-dim group.
+// 4-bit codes: byte j of a group holds dim 2j in its low nibble and 2j + 1 in its
+// high nibble.  3-bit codes: the row's low two bits four per byte (byte j: dims
+// 4j .. 4j+3, dim 4j+i in bits 2i and 2i+1), then its third bits eight per byte
+// (byte D/4 + j: dims 8j .. 8j+7, dim 8j+i in bit i); four codes at a time are
+// spread into the bytes of a word, the low-bit pairs by shifts of 6, 12 and 18
 // (each lands at the bottom of its own byte), the third bits by a multiply with
-// 1 + 2^7 + 2^14 + 2^21 (bit k lands at bit 8k); then as in the 4-bit decode.
-// The groups are a loop, as in decode_row_q4 (3-bit code rows are 48 bytes
-// apart, so their loads need no rotation).
-template <int D>
-__device__ __forceinline__ void decode_row_q3(const uint8_t* codes, const uint8_t* params, uint8_t* stage, int r) {
-  constexpr int kGroups = D / kQ4Group;
-  const uint2* lo2 = reinterpret_cast<const uint2*>(codes);
-  const uint32_t* hi4 = reinterpret_cast<const uint32_t*>(codes + D / 4);
+// 1 + 2^7 + 2^14 + 2^21 (bit k lands at bit 8k).  A code becomes a float exactly
+// by placing it in the low mantissa bits of 2^23 and subtracting 2^23; the fused
+// multiply-add then rounds the exact code * scale + zero once to fp32, and the
+// conversion rounds that once to bf16.
+// The groups are a loop, not unrolled (each turn selects its group's registers
+// by compare, so every register index is fixed): the decoding warps share each SM
+// sub-partition's instruction cache with the softmax, and an unrolled row
+// (about 500 instructions) ran 15-20% slower.
+template <int D, int kLB>
+__device__ __forceinline__ void decode_code_row(const CodeRow<D, kLB>& x, uint8_t* stage, int r, int rot) {
+  constexpr int kG = CodeRow<D, kLB>::kGroups;
   const uint64_t neg_magic = f2_pack(-8388608.f, -8388608.f);
 #pragma unroll 1
-  for (int gi = 0; gi < kGroups; ++gi) {
-    const uint2 l = lo2[gi];
-    const uint32_t h = hi4[gi];
-    const uint32_t pw = reinterpret_cast<const uint32_t*>(params)[gi];  // (scale, zero), scale in the low half
+  for (int k = 0; k < kG; ++k) {
+    const int gi = (k + rot) & (kG - 1);
+    uint4 c = x.c[0];
+    uint32_t pw = x.pw[0];
+#pragma unroll
+    for (int u = 1; u < kG; ++u)
+      if (k == u) {
+        c = x.c[u];
+        pw = x.pw[u];
+      }
     const float2 sz = __half22float2(*reinterpret_cast<const __half2*>(&pw));
     const uint64_t s2 = f2_pack(sz.x, sz.x), z2 = f2_pack(sz.y, sz.y);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {  // dims 8q .. 8q + 7 of the group: one 16-byte chunk
-      const uint32_t l16 = (q < 2 ? l.x : l.y) >> (16 * (q & 1));
-      const uint32_t h8 = h >> (8 * q);
-      uint32_t cw[2];  // codes of dims 8q .. 8q+3 and 8q+4 .. 8q+7, one per byte
+      uint32_t cw[2];              // codes of dims 8q .. 8q+3 and 8q+4 .. 8q+7, one per byte
+      uint32_t lo = 0, hi = 0;     // 4-bit: even and odd dims, one per byte
+      if constexpr (kLB == 3) {
+        const uint32_t l16 = (q < 2 ? c.x : c.y) >> (16 * (q & 1));
+        const uint32_t h8 = c.z >> (8 * q);
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint32_t x = (l16 >> (8 * u)) & 0xFFu;
-        const uint32_t lo = (x | (x << 6) | (x << 12) | (x << 18)) & 0x03030303u;
-        const uint32_t hb = (((h8 >> (4 * u)) & 0xFu) * 0x00204081u) & 0x01010101u;
-        cw[u] = lo | (hb << 2);
+        for (int u = 0; u < 2; ++u) {
+          const uint32_t b = (l16 >> (8 * u)) & 0xFFu;
+          const uint32_t lb = (b | (b << 6) | (b << 12) | (b << 18)) & 0x03030303u;
+          const uint32_t hb = (((h8 >> (4 * u)) & 0xFu) * 0x00204081u) & 0x01010101u;
+          cw[u] = lb | (hb << 2);
+        }
+      } else {
+        const uint32_t w = q == 0 ? c.x : q == 1 ? c.y : q == 2 ? c.z : c.w;
+        lo = w & 0x0F0F0F0Fu;
+        hi = (w >> 4) & 0x0F0F0F0Fu;
       }
       uint32_t o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint32_t w = cw[j >> 1];
-        const float ce = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u + 2 * (j & 1)));
-        const float co = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u + 2 * (j & 1) + 1));
+        float ce, co;
+        if constexpr (kLB == 3) {
+          ce = __uint_as_float(__byte_perm(cw[j >> 1], 0x4B000000u, 0x7440u + 2 * (j & 1)));
+          co = __uint_as_float(__byte_perm(cw[j >> 1], 0x4B000000u, 0x7440u + 2 * (j & 1) + 1));
+        } else {
+          ce = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440u + j));
+          co = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440u + j));
+        }
         float ve, vo;
         f2_unpack(f2_fma(f2_add(f2_pack(ce, co), neg_magic), s2, z2), ve, vo);
         o[j] = pack_bf16x2(ve, vo);
@@ -220,6 +230,9 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
   __shared__ uint64_t bar_s[kNT], bar_p[kNT], bar_o[kNT], bar_of[kNT], bar_wg[kNT], bar_ml;
   // 4-bit cache: code slots full / free (K and V), one pair per half tile
   __shared__ uint64_t bar_kcf[2], bar_kce[2], bar_vcf[2], bar_vce[2];
+  // low-bit cache: pages of the tile whose codes a slot holds (-1: no more tiles),
+  // written by the producer before it fills the slot
+  __shared__ int slot_npg[2][2];
   __shared__ float ml_sh[2][kBM];  // dual mode: warpgroup 1's running max and sum per row
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
@@ -348,7 +361,7 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
     // ------------------------------------------------------------ TMA producers
     // warp 0 loads Q and the K stages, warp 2 the V stages: a V stage waits for the
     // PVs of the stage it replaces, which must not hold back later K stages
-    if constexpr (!kQ4) setmaxnreg_dec<kRegsControl>();
+    setmaxnreg_dec<kQ4 ? kRegsControlQ4 : kRegsControl>();
     const bool is_k = warp == 0;
     if (elect_one_sync()) {
       ItemIter it;
@@ -392,6 +405,7 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
               if (!ok) break;
               const int pg0 = h * (kPagesPerTile / 2);
               const int n_pg = max(0, min(kPagesPerTile / 2, npg - pg0));
+              slot_npg[is_k ? 0 : 1][h] = npg;
               mbar_arrive_expect_tx(cfull, (uint32_t)n_pg * (kPgCodes + kPgParams));
               for (int i = 0; i < n_pg; ++i) {
                 int id = pages[pg0 + i];
@@ -422,11 +436,20 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
         }
         ++n_item;
       }
+      if constexpr (kQ4) {
+        // no more tiles: the decoders of each half find -1 in their slot's page count
+        for (int h = 0; h < 2 && ok; ++h) {
+          ok = mbar_wait(is_k ? &bar_kce[h] : &bar_vce[h], (kv_it & 1u) ^ 1u, &abort_sh);
+          if (!ok) break;
+          slot_npg[is_k ? 0 : 1][h] = -1;
+          mbar_arrive(is_k ? &bar_kcf[h] : &bar_vcf[h]);
+        }
+      }
     }
     __syncwarp();
   } else if (has_work && warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if constexpr (!kQ4) setmaxnreg_dec<kRegsControl>();
+    setmaxnreg_dec<kQ4 ? kRegsControlQ4 : kRegsControl>();
     if (elect_one_sync()) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, D, false, true);
@@ -541,7 +564,7 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
     __syncwarp();
   } else if (has_work && warp == 3) {
     // ------------------------------------------------------------ page-table check
-    if constexpr (!kQ4) setmaxnreg_dec<kRegsControl>();
+    setmaxnreg_dec<kQ4 ? kRegsControlQ4 : kRegsControl>();
     // every needed page of each request this CTA touches
     ItemIter it;
     iter_init(it, pv, cta);
@@ -568,32 +591,29 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
     const uint8_t* const slot = smem + (is_k ? S::kKC : S::kVC) + h * S::kSlot;
     const uint8_t* const crow = slot + (ri % kHalfKeys) * S::kCodeRow;
     const uint8_t* const prow = slot + S::kSlotParams + (ri % kHalfKeys) * S::kParamRow;
+    const int rot = kLB == 3 ? 0 : (ri >> 1) & (D / kQ4Group - 1);  // see load_code_row
     uint64_t* const cfull = is_k ? &bar_kcf[h] : &bar_vcf[h];
     uint64_t* const cfree = is_k ? &bar_kce[h] : &bar_vce[h];
     uint8_t* const stage0 = is_k ? sK : sV;
-    ItemIter it;
-    iter_init(it, pv, cta);
-    Item item;
-    uint32_t kv_it = 0;
-    bool ok = true;
-    while (ok && iter_next(it, pv, cta, item)) {
-      const int L = p.prefix_len[item.b], N = p.n_nodes[item.b];
-      for (int tile = item.tile_begin; tile < item.tile_end && ok; ++tile, ++kv_it) {
-        const int s = kv_it % kStages;
-        const uint32_t ph = (kv_it / kStages) & 1u;
-        const int npg = min(kPagesPerTile, (L + N - tile * kBN + kPageSize - 1) / kPageSize);
-        // the bf16 stage is free once the MMAs of the tile it held have completed
-        ok = warp_wait(is_k ? &bar_ke[s] : &bar_ve[s], ph ^ 1u, &abort_sh);
-        ok = ok && warp_wait(cfull, kv_it & 1u, &abort_sh);
-        if (!ok) break;
-        if (ri < npg * kPageSize) {
-          if constexpr (kLB == 3) decode_row_q3<D>(crow, prow, stage0 + s * S::kKVTile, ri);
-          else decode_row_q4<D>(crow, prow, stage0 + s * S::kKVTile, ri);
-        }
-        mbar_arrive(cfree);
-        fence_proxy_async_smem();  // the tensor pipe reads what these threads wrote
-        mbar_arrive(is_k ? &bar_kf[s] : &bar_vf[s]);
-      }
+    // tiles in the producer's order; each slot names its tile's page count
+    for (uint32_t kv_it = 0;; ++kv_it) {
+      const int s = kv_it % kStages;
+      const uint32_t ph = (kv_it / kStages) & 1u;
+      if (!warp_wait(cfull, kv_it & 1u, &abort_sh)) break;
+      const int npg = slot_npg[is_k ? 0 : 1][h];
+      if (npg < 0) break;
+      // the row's codes into registers, and the slot back to the producer
+      const bool live = ri < npg * kPageSize;
+      CodeRow<D, kLB> row;
+      if (live) load_code_row<D, kLB>(row, crow, prow, rot);
+      // the slot's next bulk copy (async proxy) must not overtake these reads
+      fence_proxy_async_smem();
+      mbar_arrive(cfree);
+      // the bf16 stage is free once the MMAs of the tile it held have completed
+      if (!warp_wait(is_k ? &bar_ke[s] : &bar_ve[s], ph ^ 1u, &abort_sh)) break;
+      if (live) decode_code_row<D, kLB>(row, stage0 + s * S::kKVTile, ri, rot);
+      fence_proxy_async_smem();  // the tensor pipe reads what these threads wrote
+      mbar_arrive(is_k ? &bar_kf[s] : &bar_vf[s]);
     }
   } else if (has_work && warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
