@@ -151,10 +151,11 @@ __device__ __forceinline__ void load_code_row(CodeRow<D, kLB>& x, const uint8_t*
 // (byte D/4 + j: dims 8j .. 8j+7, dim 8j+i in bit i); four codes at a time are
 // spread into the bytes of a word, the low-bit pairs by shifts of 6, 12 and 18
 // (each lands at the bottom of its own byte), the third bits by a multiply with
-// 1 + 2^7 + 2^14 + 2^21 (bit k lands at bit 8k).  A code becomes a float exactly
-// by placing it in the low mantissa bits of 2^23 and subtracting 2^23; the fused
-// multiply-add then rounds the exact code * scale + zero once to fp32, and the
-// conversion rounds that once to bf16.
+// 1 + 2^7 + 2^14 + 2^21 (bit k lands at bit 8k).  A code (4-bit: a whole byte of
+// two codes, split in fp32 below) becomes a float exactly by placing it in the
+// low mantissa bits of 2^23 and subtracting 2^23; the fused multiply-add then
+// rounds the exact code * scale + zero once to fp32, and the conversion rounds
+// that once to bf16.
 // The groups are a loop, not unrolled (each turn selects its group's registers
 // by compare, so every register index is fixed): the decoding warps share each SM
 // sub-partition's instruction cache with the softmax, and an unrolled row
@@ -178,8 +179,7 @@ __device__ __forceinline__ void decode_code_row(const CodeRow<D, kLB>& x, uint8_
     const uint64_t s2 = f2_pack(sz.x, sz.x), z2 = f2_pack(sz.y, sz.y);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {  // dims 8q .. 8q + 7 of the group: one 16-byte chunk
-      uint32_t cw[2];              // codes of dims 8q .. 8q+3 and 8q+4 .. 8q+7, one per byte
-      uint32_t lo = 0, hi = 0;     // 4-bit: even and odd dims, one per byte
+      uint32_t cw[2];  // 3-bit: codes of dims 8q .. 8q+3 and 8q+4 .. 8q+7, one per byte
       if constexpr (kLB == 3) {
         const uint32_t l16 = (q < 2 ? c.x : c.y) >> (16 * (q & 1));
         const uint32_t h8 = c.z >> (8 * q);
@@ -190,25 +190,40 @@ __device__ __forceinline__ void decode_code_row(const CodeRow<D, kLB>& x, uint8_
           const uint32_t hb = (((h8 >> (4 * u)) & 0xFu) * 0x00204081u) & 0x01010101u;
           cw[u] = lb | (hb << 2);
         }
-      } else {
-        const uint32_t w = q == 0 ? c.x : q == 1 ? c.y : q == 2 ? c.z : c.w;
-        lo = w & 0x0F0F0F0Fu;
-        hi = (w >> 4) & 0x0F0F0F0Fu;
       }
       uint32_t o[4];
+      if constexpr (kLB == 3) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float ce, co;
-        if constexpr (kLB == 3) {
-          ce = __uint_as_float(__byte_perm(cw[j >> 1], 0x4B000000u, 0x7440u + 2 * (j & 1)));
-          co = __uint_as_float(__byte_perm(cw[j >> 1], 0x4B000000u, 0x7440u + 2 * (j & 1) + 1));
-        } else {
-          ce = __uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440u + j));
-          co = __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440u + j));
+        for (int j = 0; j < 4; ++j) {
+          const float ce = __uint_as_float(__byte_perm(cw[j >> 1], 0x4B000000u, 0x7440u + 2 * (j & 1)));
+          const float co = __uint_as_float(__byte_perm(cw[j >> 1], 0x4B000000u, 0x7440u + 2 * (j & 1) + 1));
+          float ve, vo;
+          f2_unpack(f2_fma(f2_add(f2_pack(ce, co), neg_magic), s2, z2), ve, vo);
+          o[j] = pack_bf16x2(ve, vo);
         }
-        float ve, vo;
-        f2_unpack(f2_fma(f2_add(f2_pack(ce, co), neg_magic), s2, z2), ve, vo);
-        o[j] = pack_bf16x2(ve, vo);
+      } else {
+        // A whole byte b = low + 16 high becomes 2^23 + b, then the nibbles are split
+        // in fp32, exactly: (b - 7.5) / 16 + 1.5 * 2^23 lies within 15/32 of
+        // 1.5 * 2^23 + high, where the spacing of fp32 is 1, so it rounds to that
+        // (no ties); low = b - 16 high.  This takes half the byte permutes and none
+        // of the nibble masks of a permute per code.
+        const uint32_t w = q == 0 ? c.x : q == 1 ? c.y : q == 2 ? c.z : c.w;
+        const uint64_t m75 = f2_pack(-7.5f, -7.5f), r16 = f2_pack(0.0625f, 0.0625f);
+        const uint64_t big = f2_pack(12582912.f, 12582912.f), nbig = f2_pack(-12582912.f, -12582912.f);
+        const uint64_t n16 = f2_pack(-16.f, -16.f);
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {  // bytes 2 pr and 2 pr + 1 of the word: dims 4 pr .. 4 pr + 3
+          const float fa = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u + 2 * pr));
+          const float fb = __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u + 2 * pr + 1));
+          const uint64_t b = f2_add(f2_pack(fa, fb), neg_magic);  // the two bytes
+          const uint64_t hn = f2_add(f2_fma(f2_add(b, m75), r16, big), nbig);  // their high nibbles
+          const uint64_t ln = f2_fma(hn, n16, b);                               // their low nibbles
+          float l0, l1, h0, h1;
+          f2_unpack(f2_fma(ln, s2, z2), l0, l1);
+          f2_unpack(f2_fma(hn, s2, z2), h0, h1);
+          o[2 * pr] = pack_bf16x2(l0, h0);
+          o[2 * pr + 1] = pack_bf16x2(l1, h1);
+        }
       }
       const int d0 = gi * kQ4Group + q * 8;
       const int db = d0 / 64, ch = (d0 % 64) / 8;
