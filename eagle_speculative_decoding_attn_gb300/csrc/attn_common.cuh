@@ -216,6 +216,17 @@ __device__ void merge_items(const AttnParams& p, const Item& it, int mrow0, int 
   }
 }
 
+// A role's first touch of global memory: wait for the previous kernel (its writes
+// become visible) and let the next kernel be scheduled; its CTAs take SMs as this
+// grid's CTAs exit (an SM running this kernel has no room left for another CTA), and it waits for this grid before reading anything this kernel writes.
+__device__ __forceinline__ void after_previous(bool& waited) {
+  if (!waited) {
+    griddep_wait();
+    griddep_launch_dependents();
+    waited = true;
+  }
+}
+
 // Run by every thread of the last CTA to exit, once all CTAs have finished:
 // folds the device-found bits into status and zero-fills each request that is
 // skipped or in error (and clears the split tickets after a timeout, since a

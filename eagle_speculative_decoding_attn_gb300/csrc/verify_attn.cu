@@ -306,12 +306,12 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
     tmem_alloc(&tmem_sh, 512);
     tmem_relinquish();
   }
-  // everything above is on chip; global memory only after the previous kernel
-  griddep_wait();
-  // the next kernel may be scheduled now: its CTAs take SMs as this grid's CTAs
-  // exit (an SM running this kernel has no registers left for another CTA), and
-  // it waits for this grid before reading anything this kernel writes
-  griddep_launch_dependents();
+  // The plan reads only the request lengths, which no call of this library writes,
+  // and the roles' first steps through it read only shared memory: both run before
+  // the wait on the previous kernel, over its tail.  Each role that touches global
+  // memory waits at its first item (after_previous), and the exit path waits before
+  // the workspace.  A request flagged in `status` (which the previous kernel may
+  // write) is computed like any other and zero-filled at exit.
   if (warp == 3) {
     // ---- plan: per-request tiles and costs, exclusive scan of the costs
     int64_t carry = 0;
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
       int64_t cost = 0;
       if (b < p.B) {
         const int L = p.prefix_len[b], N = p.n_nodes[b];
-        const bool skip = p.status[b] != 0 || request_shape_bits(L, N, p.n_max, p.max_pages) != 0;
+        const bool skip = request_shape_bits(L, N, p.n_max, p.max_pages) != 0;
         int T = 0, MT = 0;
         if (!skip) {
           T = (L + N + kBN - 1) / kBN;
@@ -384,8 +384,9 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
       Item item;
       uint32_t kv_it = 0, n_item = 0;
       const int qrows_per_tile = p.q_box_nodes * G;
-      bool ok = true;
+      bool ok = true, waited = false;
       while (ok && iter_next(it, pv, cta, item)) {
+        after_previous(waited);
         if (is_k) {
           // Q of the previous item is free once its last QK^T has completed
           if (n_item > 0) ok = mbar_wait(&bar_qe, (n_item - 1) & 1u, &abort_sh);
@@ -585,7 +586,9 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
     iter_init(it, pv, cta);
     Item item;
     int prev_b = -1;
+    bool waited = false;
     while (iter_next(it, pv, cta, item)) {
+      after_previous(waited);
       if (item.b == prev_b) continue;
       prev_b = item.b;
       const int L = p.prefix_len[item.b], N = p.n_nodes[item.b];
@@ -654,7 +657,9 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
       ph_wg ^= 1u;
       return k;
     };
+    bool waited = false;
     while (ok && iter_next(it, pv, cta, item)) {
+      after_previous(waited);
       const int n_tiles = item.tile_end - item.tile_begin;
       const bool dual = item.nt == 1 && n_tiles >= 2;
       if (!dual && t >= item.nt) {
@@ -925,6 +930,9 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
   }
 
   // ---------------------------------------------------------------- exit
+  // (a no-op for the threads that waited at their first item)
+  griddep_wait();
+  griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -141,9 +141,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     tmem_alloc2(&tmem_sh, 512);
     tmem_relinquish2();
   }
-  // everything above is on chip; global memory only after the previous kernel
-  griddep_wait();
-  griddep_launch_dependents();
+  // The plan reads only the request lengths, which no call of this library writes,
+  // and the roles' first steps through it read only shared memory: both run before
+  // the wait on the previous kernel, over its tail.  Each role that touches global
+  // memory waits at its first item (after_previous), and the exit path waits before
+  // the workspace.  A request flagged in `status` (which the previous kernel may
+  // write) is computed like any other and zero-filled at exit.
   if (warp == 3) {
     // ---- plan.  Block c (query rows 256c .. 256c + 255) of every (request, KV head)
     // belongs to lane c; each lane gets a share of the clusters proportional to its
@@ -162,7 +165,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       int chains = 0;
       if (b < p.B) {
         const int L = p.prefix_len[b], N = p.n_nodes[b];
-        const bool skip = p.status[b] != 0 || request_shape_bits(L, N, p.n_max, p.max_pages) != 0;
+        const bool skip = request_shape_bits(L, N, p.n_max, p.max_pages) != 0;
         if (!skip) {
           cost = (int64_t)p.Hkv * (((L + N + kBN - 1) / kBN) * 3 + kPairItemStart + kPairItemEnd);
           chains = (N * p.G + 2 * kBM - 1) / (2 * kBM);
@@ -203,7 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       int64_t cost = 0;
       if (b < p.B) {
         const int L = p.prefix_len[b], N = p.n_nodes[b];
-        const bool skip = my_lane < 0 || p.status[b] != 0 || request_shape_bits(L, N, p.n_max, p.max_pages) != 0 ||
+        const bool skip = my_lane < 0 || request_shape_bits(L, N, p.n_max, p.max_pages) != 0 ||
                           (N * p.G + 2 * kBM - 1) / (2 * kBM) <= my_lane;
         const int T = skip ? 0 : (L + N + kBN - 1) / kBN;
         cost = T > 0 ? (int64_t)p.Hkv * (T * 3 + kPairItemStart + kPairItemEnd) : 0;
@@ -267,7 +270,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       uint32_t kv_it = 0, n_item = 0;
       bool ok = true;
       auto leader = [&](uint64_t* bar) { return mapa_shared(smem_u32(bar), 0); };
+      bool waited = false;
       while (ok && iter_next(it, pv, wk, item)) {
+        after_previous(waited);
         if (is_k) {
           // Q of the previous item is free once its last QK^T has completed
           if (n_item > 0) ok = mbar_wait(&bar_qe, (n_item - 1) & 1u, &abort_sh);
@@ -415,7 +420,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     iter_init(it, pv, wk);
     Item item;
     int prev_b = -1;
+    bool waited = false;
     while (iter_next(it, pv, wk, item)) {
+      after_previous(waited);
       if (item.b == prev_b) continue;
       prev_b = item.b;
       const int L = p.prefix_len[item.b], N = p.n_nodes[item.b];
@@ -471,7 +478,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           pm[u] = fmax3(pm[u], __uint_as_float(x[c + 2 * u]), __uint_as_float(x[c + 2 * u + 1]));
       return fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
     };
+    bool waited = false;
     while (ok && iter_next(it, pv, wk, item)) {
+      after_previous(waited);
       const int T = item.tile_end - item.tile_begin;
       const bool dual = T >= 2;
       // the item's partial last tile (if any) completes a phase of CTA 1's barrier of
@@ -721,6 +730,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   }
 
   // ---------------------------------------------------------------- exit
+  // (a no-op for the threads that waited at their first item)
+  griddep_wait();
+  griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // nothing of this CTA is read or signalled by its peer any more

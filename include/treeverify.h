@@ -43,15 +43,20 @@
  *  - Launch order: every kernel is launched with programmatic dependent
  *    launch and waits for the preceding kernel in the stream before it writes
  *    any output, and before it reads anything that a call of this library
- *    writes (status, masks, accept outputs, caches).  tv_tree_accept reads its
- *    own inputs (logits, tokens, parents, n_nodes, uniforms) and fills its own
- *    workspace before that wait; no call of this library writes those inputs.  tv_tree_build_mask and
- *    tv_tree_verify_attn(_q4) let the next kernel in the stream be scheduled
- *    before they finish.  So a kernel of the caller's that is launched with
- *    the programmatic-launch attribute must wait (griddepcontrol.wait /
+ *    writes (status, masks, accept outputs, caches).  Two calls read some of
+ *    their inputs before that wait: tv_tree_accept its logits, tokens,
+ *    parents, n_nodes and uniforms (and fills its own workspace), and
+ *    tv_tree_verify_attn(_q4/_q3) its prefix_len and n_nodes (to plan its
+ *    work).  Only tv_tree_build_mask and tv_tree_verify_attn(_q4/_q3) let the
+ *    next kernel in the stream be scheduled before they finish, and neither
+ *    writes those inputs; the calls that may write them (tv_tree_expand:
+ *    parents, tokens, n_nodes; tv_kv_commit_path: new_len, which a caller
+ *    may pass as next step's prefix_len) start their successor only after
+ *    they finish.  So a kernel of the caller's that is launched with the
+ *    programmatic-launch attribute must wait (griddepcontrol.wait /
  *    cudaGridDependencySynchronize) before reading the outputs of a call it
- *    follows, and one that precedes tv_tree_accept and signals its
- *    dependents early must have written the accept's inputs before it
+ *    follows, and one that precedes tv_tree_accept or the attention and
+ *    signals its dependents early must have written those inputs before it
  *    signals.  Kernels launched without that attribute, and host
  *    synchronisation, are unaffected.
  */
