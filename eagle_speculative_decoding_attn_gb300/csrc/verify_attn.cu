@@ -306,12 +306,14 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
     tmem_alloc(&tmem_sh, 512);
     tmem_relinquish();
   }
-  // The plan reads only the request lengths, which no call of this library writes,
-  // and the roles' first steps through it read only shared memory: both run before
-  // the wait on the previous kernel, over its tail.  Each role that touches global
-  // memory waits at its first item (after_previous), and the exit path waits before
-  // the workspace.  A request flagged in `status` (which the previous kernel may
-  // write) is computed like any other and zero-filled at exit.
+  // Nothing that a call starting its successor early writes is read before the wait
+  // on the previous kernel: the plan reads the request lengths, the producers Q, the
+  // cache and the page table (so the first tiles load over the previous kernel's
+  // tail), the MMA issuer and the decoders only on-chip memory.  The softmax and
+  // the page-table check, which read the masks and write outputs and workspace,
+  // wait at their first item (after_previous), and the exit path waits before the
+  // workspace.  A request flagged in `status` (which the previous kernel may write)
+  // is computed like any other and zero-filled at exit.
   if (warp == 3) {
     // ---- plan: per-request tiles and costs, exclusive scan of the costs
     int64_t carry = 0;
@@ -384,9 +386,8 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
       Item item;
       uint32_t kv_it = 0, n_item = 0;
       const int qrows_per_tile = p.q_box_nodes * G;
-      bool ok = true, waited = false;
+      bool ok = true;
       while (ok && iter_next(it, pv, cta, item)) {
-        after_previous(waited);
         if (is_k) {
           // Q of the previous item is free once its last QK^T has completed
           if (n_item > 0) ok = mbar_wait(&bar_qe, (n_item - 1) & 1u, &abort_sh);

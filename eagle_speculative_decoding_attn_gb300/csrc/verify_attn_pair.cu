@@ -141,12 +141,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     tmem_alloc2(&tmem_sh, 512);
     tmem_relinquish2();
   }
-  // The plan reads only the request lengths, which no call of this library writes,
-  // and the roles' first steps through it read only shared memory: both run before
-  // the wait on the previous kernel, over its tail.  Each role that touches global
-  // memory waits at its first item (after_previous), and the exit path waits before
-  // the workspace.  A request flagged in `status` (which the previous kernel may
-  // write) is computed like any other and zero-filled at exit.
+  // Nothing that a call starting its successor early writes is read before the wait
+  // on the previous kernel: the plan reads the request lengths, the producers Q, the
+  // cache and the page table (so the first tiles load over the previous kernel's
+  // tail), the MMA issuer and the decoders only on-chip memory.  The softmax and
+  // the page-table check, which read the masks and write outputs and workspace,
+  // wait at their first item (after_previous), and the exit path waits before the
+  // workspace.  A request flagged in `status` (which the previous kernel may write)
+  // is computed like any other and zero-filled at exit.
   if (warp == 3) {
     // ---- plan.  Block c (query rows 256c .. 256c + 255) of every (request, KV head)
     // belongs to lane c; each lane gets a share of the clusters proportional to its
@@ -270,9 +272,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       uint32_t kv_it = 0, n_item = 0;
       bool ok = true;
       auto leader = [&](uint64_t* bar) { return mapa_shared(smem_u32(bar), 0); };
-      bool waited = false;
       while (ok && iter_next(it, pv, wk, item)) {
-        after_previous(waited);
         if (is_k) {
           // Q of the previous item is free once its last QK^T has completed
           if (n_item > 0) ok = mbar_wait(&bar_qe, (n_item - 1) & 1u, &abort_sh);

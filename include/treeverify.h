@@ -46,13 +46,15 @@
  *    writes (status, masks, accept outputs, caches).  Two calls read some of
  *    their inputs before that wait: tv_tree_accept its logits, tokens,
  *    parents, n_nodes and uniforms (and fills its own workspace), and
- *    tv_tree_verify_attn(_q4/_q3) its prefix_len and n_nodes (to plan its
- *    work).  Only tv_tree_build_mask and tv_tree_verify_attn(_q4/_q3) let the
- *    next kernel in the stream be scheduled before they finish, and neither
- *    writes those inputs; the calls that may write them (tv_tree_expand:
- *    parents, tokens, n_nodes; tv_kv_commit_path: new_len, which a caller
- *    may pass as next step's prefix_len) start their successor only after
- *    they finish.  So a kernel of the caller's that is launched with the
+ *    tv_tree_verify_attn(_q4/_q3) its prefix_len, n_nodes, q, page table and
+ *    K/V cache (to plan its work and load its first tiles).  Only
+ *    tv_tree_build_mask and tv_tree_verify_attn(_q4/_q3) let the next kernel
+ *    in the stream be scheduled before they finish, and neither writes those
+ *    inputs; the calls that may write them (tv_tree_expand: parents, tokens,
+ *    n_nodes; tv_kv_commit_path: the cache, and new_len, which a caller may
+ *    pass as next step's prefix_len; tv_kv_prune_pages: the page table;
+ *    tv_kv_quantize_q4/_q3: the low-bit cache) start their successor only
+ *    after they finish.  So a kernel of the caller's that is launched with the
  *    programmatic-launch attribute must wait (griddepcontrol.wait /
  *    cudaGridDependencySynchronize) before reading the outputs of a call it
  *    follows, and one that precedes tv_tree_accept or the attention and
