@@ -912,16 +912,17 @@ __global__ void __launch_bounds__(kLB != 0 ? kThreadsQ4 : kThreads, 1)
           p.part_lse[(int64_t)item.my_slot * kRowsPerSlot + prow] = lse_v;
           p.part_scale[(int64_t)item.my_slot * kRowsPerSlot + prow] = row_scale;
         }
-        // ticket: the last split of this (group, M tile) to arrive merges every partial
-        __threadfence();
+        // ticket: the last split of this (group, M tile) to arrive merges every partial.
+        // The warpgroup barrier orders every thread's partial stores before the ticket,
+        // whose release (GPU scope) covers them; its acquire, passed on by the second
+        // barrier, covers the other splits' stores for the merge.
         ok = wg_sync();
         if (!ok) break;
         const int tick_idx = (((item.b * p.Hkv + item.g) * p.mp_max + item.mp) * kNT) + mtile;
-        if (r == 0) ticket_sh[t] = atomicAdd(p.ws_tickets + tick_idx, 1);
+        if (r == 0) ticket_sh[t] = atom_add_acq_rel_gpu(p.ws_tickets + tick_idx, 1);
         ok = wg_sync();
         if (!ok) break;
         if (ticket_sh[t] == item.n_splits - 1) {
-          __threadfence();
           const int n_rows = min(kBM, N * G - (item.mp * kNT + mtile) * kBM);  // valid rows of the M tile
           merge_tile<D, kLB>(p, item, mtile, n_rows, r);
           if (r == 0) p.ws_tickets[tick_idx] = 0;  // ready for the next call

@@ -704,16 +704,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           p.part_lse[(int64_t)my_slot * kRowsPerSlot + r] = lse_v;
           p.part_scale[(int64_t)my_slot * kRowsPerSlot + r] = row_scale;
         }
-        // ticket of this CTA's rows: the last split to arrive merges every partial
-        __threadfence();
+        // ticket of this CTA's rows: the last split to arrive merges every partial.  The
+        // barrier of both warpgroups orders every thread's partial stores before the
+        // ticket, whose release (GPU scope) covers them; its acquire, passed on by the
+        // second barrier, covers the other splits' stores for the merge.
         ok = ep_sync();
         if (!ok) break;
         const int tick_idx = (((item.b * p.Hkv + item.g) * p.mp_max + lane_id) * kNT) + (int)rank;
-        if (t == 0 && r == 0) ticket_sh[0] = atomicAdd(p.ws_tickets + tick_idx, 1);
+        if (t == 0 && r == 0) ticket_sh[0] = atom_add_acq_rel_gpu(p.ws_tickets + tick_idx, 1);
         ok = ep_sync();
         if (!ok) break;
         if (ticket_sh[0] == item.n_splits - 1) {
-          __threadfence();
           const int n_rows = min(kBM, N * G - mrow0);
           if (n_rows > 0) {
             const int r2 = t * kBM + r;  // both warpgroups
