@@ -227,13 +227,13 @@ __device__ __forceinline__ void after_previous(bool& waited) {
   }
 }
 
-// Run by every thread of the last CTA to exit, once all CTAs have finished:
+// Run by every thread of the last CTA to exit, once all CTAs have finished (the
+// exit count's acquire, passed on by a barrier, makes their stores visible):
 // folds the device-found bits into status and zero-fills each request that is
 // skipped or in error (and clears the split tickets after a timeout, since a
 // split that gave up never took its ticket).
 template <int D>
 __device__ void finish_requests(const AttnParams& p, int tid, int nthreads) {
-  __threadfence();
   const int64_t per_req = (int64_t)p.n_max * p.Hq * D;
   bool any_timeout = false;
   for (int b = 0; b < p.B; ++b) {

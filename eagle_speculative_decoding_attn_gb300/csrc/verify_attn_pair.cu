@@ -741,8 +741,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
   if (warp == 2) tmem_dealloc2(tmem, 512);
   if (tid == 0) {
     if (abort_sh && last_b_sh >= 0) atomicOr(p.ws_bits + last_b_sh, TV_DEV_TIMEOUT);
-    __threadfence();
-    last_cta_sh = (atomicAdd(p.ws_exit, 1) == (int)gridDim.x - 1);
+    // the barrier above orders this CTA's stores before the count, whose release
+    // covers them; the last CTA's acquire (passed on by the barrier below) covers all
+    last_cta_sh = (atom_add_acq_rel_gpu(p.ws_exit, 1) == (int)gridDim.x - 1);
   }
   __syncthreads();
   if (last_cta_sh) finish_requests<D>(p, tid, kPThreads);
