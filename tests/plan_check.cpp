@@ -44,10 +44,12 @@ int main(int argc, char** argv) {
     const int G = groups[uni(0, 6)];
     const int grid = grids[uni(0, 5)];
     const int maxL = (c % 3 == 0) ? 40000 : 3000;
-    const int ehs[] = {0, 1, 3, 8, 40};
-    const int eh = ehs[uni(0, 4)], ee = ehs[uni(0, 4)];
-    const int txs[] = {0, 0, 1, 4, 9};
-    const int tx = txs[uni(0, 4)];
+    // the charges the kernels use (one CTA: 6 at each end, low-bit tiles 2 more;
+    // CTA pairs: 8) among others
+    const int ehs[] = {0, 1, 3, 6, 8, 40};
+    const int eh = ehs[uni(0, 5)], ee = ehs[uni(0, 5)];
+    const int txs[] = {0, 0, 1, 2, 4, 9};
+    const int tx = txs[uni(0, 5)];
     std::vector<int64_t> start(B + 1);
     std::vector<int32_t> T(B), MT(B);
     int64_t W = 0;
