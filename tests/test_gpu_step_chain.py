@@ -1,6 +1,6 @@
-"""Two steps in one stream: this step's commit, then the next step's mask and
-attention over the cache the commit compacted, with the commit's new_len output
-passed as the next step's prefix_len.
+"""Two steps in one stream: this step's mask, attention, acceptance and commit,
+then the next step's mask and attention over the cache the commit compacted,
+with the commit's new_len output passed as the next step's prefix_len.
 
 The attention reads the lengths, q, the page table and the cache before it waits
 for the previous kernel in the stream; no call that writes those lets its
@@ -52,15 +52,20 @@ def test_commit_then_next_step_attention():
     parents_d, n_d = to_dev(w.parents, dev), to_dev(w.n_nodes, dev)
     pt_d = to_dev(w.page_table, dev)
     k_d, v_d = bf16_dev(w.k_bits, dev), bf16_dev(w.v_bits, dev)
+    L_d = to_dev(w.prefix_len, dev)
     anc, depth, st = tvb.tree_build_mask(parents_d, n_d)
+    out1, lse1 = tvb.tree_verify_attn(bf16_dev(w.q_bits, dev), k_d, v_d, pt_d, L_d, n_d, anc, w.scale, st)
     acc_len, path, _ = tvb.tree_accept(to_dev(w.target_logits, dev), None, to_dev(tokens, dev), parents_d, n_d, anc,
                                        depth, 0.0, None, None, st)
-    _, new_len = tvb.kv_commit_path(k_d, v_d, pt_d, to_dev(w.prefix_len, dev), n_d, acc_len, path, st)
+    _, new_len = tvb.kv_commit_path(k_d, v_d, pt_d, L_d, n_d, acc_len, path, st)
     n2_d = to_dev(n2, dev)
     anc2, _, st2 = tvb.tree_build_mask(to_dev(parents2, dev), n2_d)
     out, lse = tvb.tree_verify_attn(bf16_dev(q2, dev), k_d, v_d, pt_d, new_len, n2_d, anc2, w.scale, st2)
     torch.cuda.synchronize()
 
+    out1_ref, lse1_ref, _ = oracle.tree_verify_attn(w.q_bits, w.k_bits, w.v_bits, w.page_table, w.prefix_len,
+                                                    w.n_nodes, w.parents, w.scale)
+    compare_attn(out1.float().cpu().numpy(), lse1.cpu().numpy(), out1_ref, lse1_ref, w, output_rounding=True)
     np.testing.assert_array_equal(acc_len.cpu().numpy(), a_ref)
     np.testing.assert_array_equal(new_len.cpu().numpy(), new_len_ref)
     assert (st.cpu().numpy() == 0).all() and (st2.cpu().numpy() == 0).all()
