@@ -71,3 +71,30 @@ def test_commit_then_next_step_attention():
     assert (st.cpu().numpy() == 0).all() and (st2.cpu().numpy() == 0).all()
     w2 = W.make_custom(B=B, Hq=Hq, Hkv=w.Hkv, D=D, prefix_len=list(new_len_ref), parents_list=[[-1]] * B, seed=73)
     compare_attn(out.float().cpu().numpy(), lse.cpu().numpy(), out_ref, lse_ref, w2, output_rounding=True)
+
+
+@pytest.mark.parametrize("bits", [4, 3])
+def test_quantize_then_lowbit_attention_same_stream(bits):
+    """The encoder writes the low-bit cache and the attention reads it right after,
+    in the same stream with no synchronisation: the attention's producers copy
+    codes before their kernel waits for the previous one, and the encoder starts
+    its successor only once it has finished.  Against the oracle's encoder and its
+    attention over the decoded cache."""
+    dev = require_gpu()
+    w = W.make_workload("tiny", with_logits=False)
+    quant = tvb.kv_quantize_q4 if bits == 4 else tvb.kv_quantize_q3
+    attn = tvb.tree_verify_attn_q4 if bits == 4 else tvb.tree_verify_attn_q3
+    oq = oracle.quantize_q4 if bits == 4 else oracle.quantize_q3
+    oattn = oracle.tree_verify_attn_q4 if bits == 4 else oracle.tree_verify_attn_q3
+    parents_d, n_d = to_dev(w.parents, dev), to_dev(w.n_nodes, dev)
+    anc, _, st = tvb.tree_build_mask(parents_d, n_d)
+    kc, kp = quant(bf16_dev(w.k_bits, dev))
+    vc, vp = quant(bf16_dev(w.v_bits, dev))
+    out, lse = attn(bf16_dev(w.q_bits, dev), kc, kp, vc, vp, to_dev(w.page_table, dev), to_dev(w.prefix_len, dev), n_d,
+                    anc, w.scale, st)
+    torch.cuda.synchronize()
+    rk, rkp = oq(w.k_bits)
+    rv, rvp = oq(w.v_bits)
+    ref_out, ref_lse, _ = oattn(w.q_bits, rk, rkp, rv, rvp, w.page_table, w.prefix_len, w.n_nodes, w.parents, w.scale)
+    assert (st.cpu().numpy() == 0).all()
+    compare_attn(out.float().cpu().numpy(), lse.cpu().numpy(), ref_out, ref_lse, w)
